@@ -1,0 +1,151 @@
+/*
+ * pskv_oracle.h -- plain fp64 CPU oracle for paged split-KV GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This code exists to check the CUDA library; only
+ * the tests, the smoke check and the bench's CPU-baseline leg may build, load
+ * or call it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [gem]    "Parked D512 fused split-KV decode design" (gem, docs/research):
+ *           intro (online partials, exact rescaling merge, empty states,
+ *           fail-closed states and scratch overflow, fp64 direct reference),
+ *           "Fixed production shape", "Candidate ownership and storage"
+ *           (per-key state update in sequence order, merge identity, scratch
+ *           byte contract).
+ *  [pg1055] pegainfer #1055 "decode the global family through a generated
+ *           split-KV kernel over a folded 640-column pool": Description
+ *           (partial over key chunks, merge in two levels).
+ *  [pg1057] pegainfer #1057 "serve the sliding family through generated
+ *           kernels...": Description (window lower bound; resident pages hold
+ *           up to a page more than the window, those keys masked).
+ *  [tf1619] TensorFold #1619 "gemma4 CUDA: the global layers' caches in pages
+ *           of the core pool...": description "Paged" (K region then V region,
+ *           page p = rows [ps*p, ps*(p+1))), "Leasing" (refuse rows past a
+ *           slot's pages), "Writes" (rows copied into pages keep their bits).
+ *
+ * Pool layout (the library's documented layout, restated here): element
+ * (page, kv_head, row, d) of a region lives at
+ *   ((page * num_kv_heads + kv_head) * page_size + row) * head_dim + d.
+ * Key i of table row b is in page tables[b * table_stride + i / page_size],
+ * row i % page_size.  Query head h reads kv head h / (Hq / Hkv).
+ */
+#ifndef PSKV_ORACLE_H
+#define PSKV_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_INVALID (-1)
+#define ORC_ERR_PAST_PAGES (-2)
+#define ORC_ERR_OVERFLOW (-3)
+#define ORC_ERR_STATE (-4)
+#define ORC_ERR_BAD_PAGE (-5)
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* Geometry of one paged pool (both regions share it). */
+typedef struct orc_pool {
+  const void *k;  /* K region */
+  const void *v;  /* V region */
+  int dtype;      /* ORC_F32 or ORC_BF16 */
+  int64_t num_pages;
+  int page_size;
+  int num_kv_heads;
+  int head_dim_k;
+  int head_dim_v;
+} orc_pool;
+
+/* Online-softmax state of one query head over a set of keys:
+ * m = max score, l = sum exp(s - m), o[dv] = sum exp(s - m) * v.
+ * The empty state is (m = -inf, l = 0, o = 0). */
+typedef struct orc_state {
+  double m;
+  double l;
+  double *o; /* caller-owned, length dv */
+} orc_state;
+
+/* ---- dense (unpaged) attention for one query head ---------------------- */
+
+/* Direct softmax attention over keys [begin, end) of dense K[L][dk], V[L][dv]. */
+int orc_attend_direct(const double *q, const double *k, const double *v, int dk, int dv,
+                      int begin, int end, double scale, double *out);
+
+/* Online partial over keys [begin, end), one key at a time in sequence order. */
+int orc_online_partial(const double *q, const double *k, const double *v, int dk, int dv,
+                       int begin, int end, double scale, double *m, double *l, double *o);
+
+/* Exact rescaling merge of two states into (m, l, o); fails closed on invalid
+ * states.  Merging with an empty state returns the other state bit for bit. */
+int orc_merge(double ma, double la, const double *oa, double mb, double lb, const double *ob,
+              int dv, double *m, double *l, double *o);
+
+/* Finalize out = o / l; fails on the empty state. */
+int orc_finalize(double m, double l, const double *o, int dv, double *out);
+
+/* Online attention over an explicit partition: keys split at bounds[0..P]
+ * (non-decreasing, bounds[0] = begin, bounds[P] = end), one partial per part,
+ * partials folded in groups of group_size (level 1), then the group results
+ * folded (level 2), then finalized. */
+int orc_attend_partitioned(const double *q, const double *k, const double *v, int dk, int dv,
+                           const int *bounds, int num_parts, int group_size, double scale,
+                           double *out);
+
+/* Single-precision twin of the online path (partials + merge + finalize in
+ * float), for the accuracy audit of the gem design's CPU oracle. */
+int orc_attend_partitioned_f32(const float *q, const float *k, const float *v, int dk, int dv,
+                               const int *bounds, int num_parts, float scale, float *out);
+
+/* ---- paged pool ------------------------------------------------------- */
+
+/* Gather the keys and values of (row b, kv head g) into dense double arrays
+ * k_out[len][dk], v_out[len][dv].  Fails on a page id outside the pool or a
+ * length past the table. */
+int orc_gather(const orc_pool *pool, const int32_t *page_tables, int table_stride, int b, int g,
+               int len, double *k_out, double *v_out);
+
+/* Append n rows: row r (k_new/v_new[r][num_kv_heads][head_dim]) goes to table
+ * row row_of[r] at position pos_of[r].  All rows are checked first; a
+ * position at or past num_pages_of_row[row] * page_size refuses the whole
+ * call (ORC_ERR_PAST_PAGES) and nothing is written.  Bytes are copied as is. */
+int orc_append_rows(void *k_region, void *v_region, const orc_pool *pool, const void *k_new,
+                    const void *v_new, const int32_t *row_of, const int32_t *pos_of, int n,
+                    const int32_t *page_tables, int table_stride,
+                    const int32_t *num_pages_of_row, int batch);
+
+/* Direct fp64 decode: out[b][h][dv] for every row and query head.
+ * first_pos / window_lo may be NULL (no window); key i of row b has position
+ * first_pos[b] + i and is attended iff that position >= window_lo[b]. */
+int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
+                      double *out);
+
+/* Online fp64 decode: the attended keys of a row are cut into chunks of
+ * chunk_tokens (aligned to key index 0), the chunks into num_splits
+ * contiguous partitions of ceil(n_chunks / num_splits) chunks (trailing
+ * partitions may be empty), then orc_attend_partitioned. */
+int orc_decode_online(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
+                      int chunk_tokens, int num_splits, int group_size, double *out);
+
+/* Scratch byte contract of the partial buffer: maxima (B*Hq*P*4 bytes),
+ * denominators (same) and numerators (B*Hq*P*Dv*4), each product checked for
+ * size_t overflow. */
+int orc_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_dim_v,
+                              int64_t num_splits, size_t *maxima, size_t *denominators,
+                              size_t *numerators, size_t *total);
+
+/* Number of OpenMP threads the oracle's parallel loops use (1 without OpenMP). */
+int orc_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
