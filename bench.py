@@ -1,0 +1,501 @@
+"""Benchmark: paged split-KV GQA decode attention on GB300.
+
+One step is one pass of the whole decode hot path over one batch of
+synthetic input, as a Gemma-4-31B-shaped decode step runs it:
+  * the global-layer decode (32 query heads on 4 KV heads, head dim 512,
+    bf16 K/V in shuffled pages of 256) at the two contexts 10,602 and
+    40,002: append the step's new K/V row into its page, then the split-KV
+    partial kernel and the two-level merge;
+  * the sliding-window decode (32 query heads on 16 KV heads, head dim 256,
+    window 1,024, pages of 64, resident length window + one page): append,
+    then the windowed partial kernel and merge.
+value = algorithmic bytes (K and V of every attended key) / step time, GB/s.
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream, with a barrier and a device synchronize on both sides;
+every step reads three rotating copies of the pools (433 MB of K/V a step,
+> 3x the 129 MB L2), so no call finds its data in L2.
+
+--impl reference times the CPU oracle (the only reference there is: the
+pages ship no runnable code) on the same workload; see the design doc.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode attn µs/call & effective HBM GB/s (% of 8 TB/s) at 10.6K–163K ctx"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_CONTEXTS = (10602, 40002)
+WINDOW_RESIDENCY = W.WINDOW + 64
+ROTATE = 3
+PARTIAL_SOURCES = ("paged_split_kv_attn_gb300/csrc/partial_kernel.cuh",
+                   "paged_split_kv_attn_gb300/csrc/partial_mma.cu",
+                   "paged_split_kv_attn_gb300/csrc/pskv_internal.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_mma_d512_traffic.json")
+
+
+def partial_kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in PARTIAL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per key of the partial kernel from the committed ncu summary,
+    or None when the kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_hash") != partial_kernel_hash():
+        return None
+    return float(t["dram_bytes_per_key"])
+
+
+# ---- distributed plumbing (replicas only: every rank runs the same step) ----------
+
+class Dist:
+    def __init__(self):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- the workload ----------------------------------------------------------------
+
+class Call:
+    """One decode call of the step: a pool (and rotating copies), its inputs and outputs."""
+
+    def __init__(self, name, case, windowed, splits, dev, rotate):
+        import torch
+        import paged_split_kv_attn_gb300 as pskv
+        self.name, self.case, self.windowed = name, case, windowed
+        self.splits = splits
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        k0, v0 = bf(case.k_pool), bf(case.v_pool)
+        self.k = [k0] + [k0.clone() for _ in range(rotate - 1)]
+        self.v = [v0] + [v0.clone() for _ in range(rotate - 1)]
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.layouts = [pskv.paged_kv_layout_create(k, v, self.status)
+                        for k, v in zip(self.k, self.v)]
+        self.q = bf(case.q)
+        self.tables = torch.from_numpy(case.page_tables).to(dev)
+        self.lens = torch.from_numpy(case.seq_lens).to(dev)
+        self.lens_host = case.seq_lens.copy()
+        self.pages_of_row = torch.from_numpy(case.pages_of_row).to(dev)
+        self.first_pos = None if case.first_pos is None else torch.from_numpy(case.first_pos).to(dev)
+        self.window_lo = None if case.window_lo is None else torch.from_numpy(case.window_lo).to(dev)
+        b, hq, d = case.q.shape
+        hkv = case.num_kv_heads
+        # the step's new token: its K/V row goes to the last position of each row
+        self.pos = [int(n) - 1 for n in case.seq_lens]
+        self.rows = list(range(b))
+        self.row_of = torch.tensor(self.rows, dtype=torch.int32, device=dev)
+        self.pos_of = torch.tensor(self.pos, dtype=torch.int32, device=dev)
+        ps = case.page_size
+        self.k_new = torch.stack([k0[int(case.page_tables[r, p // ps]), :, p % ps]
+                                  for r, p in zip(self.rows, self.pos)]).contiguous()
+        self.v_new = torch.stack([v0[int(case.page_tables[r, p // ps]), :, p % ps]
+                                  for r, p in zip(self.rows, self.pos)]).contiguous()
+        self.out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=dev)
+        self.ws = pskv.workspace(b, hq, d, splits, dev)
+        self.bytes = case.kv_bytes()
+        self.partial_bytes_per_launch = self.bytes
+        self.hkv = hkv
+        # pinned host buffers for the end-to-end measurement
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_k_new = self.k_new.cpu().pin_memory()
+        self.h_v_new = self.v_new.cpu().pin_memory()
+        self.h_pos = self.pos_of.cpu().pin_memory()
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_k_new, self.h_v_new,
+                                                          self.h_pos))
+
+    def d2h_bytes(self) -> int:
+        return self.h_out.numel() * self.h_out.element_size()
+
+    def run(self, it: int, events=None):
+        import paged_split_kv_attn_gb300 as pskv
+        layout = self.layouts[it % len(self.layouts)]
+        pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of, self.tables,
+                            self.pages_of_row)
+        if self.windowed:
+            pskv.decode_attn_windowed(layout, self.q, self.tables, self.lens, self.lens_host,
+                                      self.first_pos, self.window_lo, self.case.scale,
+                                      num_splits=self.splits, workspace=self.ws, out=self.out,
+                                      events=events)
+        else:
+            pskv.decode_attn_splitkv(layout, self.q, self.tables, self.lens, self.lens_host,
+                                     self.case.scale, num_splits=self.splits, workspace=self.ws,
+                                     out=self.out, events=events)
+
+    def run_e2e(self, it: int):
+        """The same call from host buffers: inputs copied in, the output copied back."""
+        self.q.copy_(self.h_q, non_blocking=True)
+        self.k_new.copy_(self.h_k_new, non_blocking=True)
+        self.v_new.copy_(self.h_v_new, non_blocking=True)
+        self.pos_of.copy_(self.h_pos, non_blocking=True)
+        self.run(it)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def make_calls(args, dev):
+    calls = []
+    for ctx in args.contexts:
+        calls.append(Call(f"global_{ctx}", W.global_case(ctx, seed=ctx), False, args.splits, dev,
+                          ROTATE))
+    if not args.no_window:
+        calls.append(Call(f"window_{WINDOW_RESIDENCY}", W.window_case(WINDOW_RESIDENCY, seed=7),
+                          True, args.window_splits, dev, ROTATE))
+    return calls
+
+
+# ---- CPU baseline: the oracle on a bounded sample ----------------------------------
+
+def cpu_baseline(cases, budget_s: float):
+    import oracle
+    done_bytes, reps, t0 = 0, 0, time.perf_counter()
+    while True:
+        for c in cases:
+            oracle.decode_direct(c.q, c.k_pool, c.v_pool, c.page_tables, c.seq_lens, c.scale,
+                                 c.first_pos, c.window_lo)
+            done_bytes += c.kv_bytes()
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} pass(es) of the step's {len(cases)} decode calls "
+                      f"({', '.join(str(int(c.seq_lens.sum())) + ' keys' for c in cases)}), "
+                      f"fp64 direct softmax over the paged pool, {dt:.1f} s"}
+
+
+# ---- main ----------------------------------------------------------------------------
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--contexts", type=int, nargs="+", default=list(DEFAULT_CONTEXTS))
+    ap.add_argument("--splits", type=int, default=0, help="global-layer split count (0 = auto)")
+    ap.add_argument("--window-splits", type=int, default=0)
+    ap.add_argument("--no-window", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", type=int, nargs="*", default=None,
+                    help="also time each global context alone at these split counts")
+    return ap.parse_args()
+
+
+def reference_arm(args):
+    """The CPU oracle on the same workload, each step a full pass (bounded by K)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    cases = [W.global_case(ctx, seed=ctx) for ctx in args.contexts]
+    if not args.no_window:
+        cases.append(W.window_case(WINDOW_RESIDENCY, seed=7))
+    nbytes = sum(c.kv_bytes() for c in cases)
+    for _ in range(min(args.warmup, 1)):
+        for c in cases:
+            oracle.decode_direct(c.q, c.k_pool, c.v_pool, c.page_tables, c.seq_lens, c.scale,
+                                 c.first_pos, c.window_lo)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for c in cases:
+            oracle.decode_direct(c.q, c.k_pool, c.v_pool, c.page_tables, c.seq_lens, c.scale,
+                                 c.first_pos, c.window_lo)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": config_dict(args),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{args.steps} full step(s) of the workload"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(args):
+    return {"workload": "gemma4-31b decode step: global-layer split-KV decode at contexts "
+                        + "/".join(str(c) for c in args.contexts)
+                        + ("" if args.no_window else
+                           f" + sliding-window decode at residency {WINDOW_RESIDENCY}"),
+            "global": {"batch": 1, "num_q_heads": 32, "num_kv_heads": 4, "head_dim": 512,
+                       "page_size": 256, "contexts": list(args.contexts),
+                       "splits": args.splits or "auto"},
+            "window": None if args.no_window else
+            {"batch": 1, "num_q_heads": 32, "num_kv_heads": 16, "head_dim": 256,
+             "page_size": 64, "window": W.WINDOW, "residency": WINDOW_RESIDENCY,
+             "splits": args.window_splits or "auto"},
+            "kv_dtype": "bf16", "accumulate": "f32", "out_dtype": "bf16",
+            "l2": f"inputs larger than L2: {ROTATE} rotating pool copies, >400 MB of K/V per step",
+            "parallelism": "replicas"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+    import paged_split_kv_attn_gb300 as pskv
+    from paged_split_kv_attn_gb300 import build as lib_build
+
+    dist = Dist()
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    lib_build.build()
+    pskv.load_library()
+    calls = make_calls(args, dev)
+    stream = torch.cuda.current_stream()
+    step_bytes = sum(c.bytes for c in calls)
+
+    # per-call partial-kernel events (recorded by the library around the partial launch)
+    ev = {c.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] for c in calls}
+    for c in calls:
+        for b, e in ev[c.name]:
+            b.record()
+            e.record()
+    for it in range(args.warmup):
+        for c in calls:
+            c.run(it)
+    torch.cuda.synchronize()
+    for c in calls:
+        if c.status[0].item() != 0:
+            raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = pskv.pskv_kernel_launches()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for it in range(args.steps):
+        for c in calls:
+            c.run(it, events=ev[c.name][it])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    launches = pskv.pskv_kernel_launches() - launches0
+    clock_info = clocks.stop()
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    ms = dist.max(ms)
+    value = step_bytes * dist.world / (ms * 1e-3) / 1e9
+
+    per_call = {}
+    for c in calls:
+        part = [b.elapsed_time(e) for b, e in ev[c.name]]
+        per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
+                            "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9}
+
+    # per-call µs/call (append + partial + merge), each call timed alone with a cold L2
+    for c in calls:
+        flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+        times = []
+        for it in range(max(5, min(args.steps, 30))):
+            flush.fill_(it & 0xFF)
+            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b.record(stream)
+            c.run(it)
+            e.record(stream)
+            torch.cuda.synchronize()
+            times.append(b.elapsed_time(e) * 1e3)
+        del flush
+        per_call[c.name]["us_per_call_median"] = statistics.median(times)
+        per_call[c.name]["GBps_per_call"] = c.bytes / (statistics.median(times) * 1e-6) / 1e9
+        per_call[c.name]["splits"] = c.splits or pskv.pskv_plan_splits(c.layouts[0], c.lens_host)
+
+    # optional split sweep of the global contexts (each call alone, cold L2)
+    sweep = None
+    if args.sweep:
+        sweep = {}
+        flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+        for c in calls:
+            if c.windowed:
+                continue
+            res = {}
+            for p in args.sweep:
+                c.splits = p
+                c.ws = pskv.workspace(1, 32, 512, p, dev)
+                times = []
+                for it in range(10):
+                    flush.fill_(it & 0xFF)
+                    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    b.record(stream)
+                    c.run(it)
+                    e.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(b.elapsed_time(e) * 1e3)
+                res[p] = statistics.median(times)
+            sweep[c.name] = res
+            c.splits = args.splits
+        del flush
+
+    # end-to-end through the public calls from pinned host buffers
+    for it in range(args.warmup):
+        for c in calls:
+            c.run_e2e(it)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e_b, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_b.record(stream)
+    for it in range(args.steps):
+        for c in calls:
+            c.run_e2e(it)
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(e_b.elapsed_time(e_e) / args.steps)
+
+    for c in calls:
+        if c.status[0].item() != 0:
+            raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
+
+    peak, peak_kind = measured_peak()
+    glob = [c for c in calls if not c.windowed]
+    part_bytes = sum(c.bytes for c in glob)
+    part_s = sum(statistics.mean([b.elapsed_time(e) for b, e in ev[c.name]]) * 1e-3 for c in glob)
+    achieved = part_bytes / part_s / 1e9
+    traffic_per_key = recorded_traffic()
+    keys_per_launch = statistics.mean(int(c.case.seq_lens.sum()) for c in glob)
+    roofline = {"bound": "hbm", "kernel": "pskv_partial_kernel<MmaConsumer<512>>",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": part_bytes / len(glob),
+                "traffic": None if traffic_per_key is None else traffic_per_key * keys_per_launch}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(args), "roofline": roofline,
+            "e2e": {"value": step_bytes * dist.world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": sum(c.h2d_bytes() for c in calls),
+                    "d2h_bytes_per_step": sum(c.d2h_bytes() for c in calls)},
+            "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
+    if sweep is not None:
+        line["split_sweep_us"] = sweep
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline([c.case for c in calls], args.cpu_seconds)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

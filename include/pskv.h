@@ -1,0 +1,252 @@
+/*
+ * pskv.h -- paged split-KV GQA attention for single-token decode on GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no C++ or framework types.
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *   For every table row b and query head h, with G = num_q_heads / num_kv_heads
+ *   query heads per KV head and kv head g = h / G,
+ *     out[b][h][:] = sum_i softmax_i(scale * q[b][h] . k_i) * v_i
+ *   over the keys i of row b, where key i lives in page page_tables[b][i / ps]
+ *   at row i % ps ("TensorFold #1619 ... caches in pages of the core pool",
+ *   description "Paged"; "Parked D512 fused split-KV decode design" (gem),
+ *   "Fixed production shape": exact dense attention, 32 q heads over 4 KV
+ *   heads, D = 512).
+ *   It is computed split-KV: the keys of a row are cut into partitions, each
+ *   produces an online-softmax partial (running max m, sum l, unnormalised
+ *   numerator o), and the partials are merged in two levels by the exact
+ *   rescaling identity m = max(ma, mb), l = la e^(ma-m) + lb e^(mb-m),
+ *   o = oa e^(ma-m) + ob e^(mb-m), then out = o / l (gem design, introduction
+ *   and "Candidate ownership and storage"; pegainfer #1055 "decode the global
+ *   family through a generated split-KV kernel...", Description).
+ *   The windowed variant masks keys below a window lower bound (pegainfer
+ *   #1057 "serve the sliding family through generated kernels...",
+ *   Description).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device memory of the current device; host
+ *     pointers are ordinary host memory.  The caller owns all memory; the
+ *     library never allocates device memory and never synchronizes a stream.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and is
+ *     asynchronous; a return of PSKV_OK means it was enqueued.
+ *   - Every call returns a status code (PSKV_OK or a negative PSKV_ERR_*).
+ *     Host-visible arguments are checked before anything is enqueued; on an
+ *     error nothing is enqueued.  Device-side faults (a bad page id, a length
+ *     out of range) never trap: the kernel skips the bad access and ORs a
+ *     PSKV_FAULT_* bit into the layout's status word, which the caller reads.
+ *   - bf16 data is IEEE bfloat16 (1-8-7), f32 is IEEE binary32.
+ */
+#ifndef PSKV_H
+#define PSKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same types as cudaStream_t / cudaEvent_t, declared without CUDA headers. */
+typedef struct CUstream_st *pskv_stream_t;
+typedef struct CUevent_st *pskv_event_t;
+
+/* ---- status codes --------------------------------------------------------- */
+#define PSKV_OK 0
+#define PSKV_ERR_INVALID_ARG (-1)          /* a null pointer, a bad size or value */
+#define PSKV_ERR_UNSUPPORTED (-2)          /* a shape or format this build refuses */
+#define PSKV_ERR_OVERFLOW (-3)             /* a size product overflows size_t */
+#define PSKV_ERR_WORKSPACE_TOO_SMALL (-4)
+#define PSKV_ERR_PAST_PAGES (-5)           /* an append position past its row's pages */
+#define PSKV_ERR_CUDA (-6)                 /* a CUDA runtime call failed */
+
+/* ---- element types and pool formats ---------------------------------------- */
+#define PSKV_DTYPE_F32 0
+#define PSKV_DTYPE_BF16 1
+
+#define PSKV_FORMAT_SPLIT 0   /* K and V rows kept whole, one region each */
+#define PSKV_FORMAT_FOLDED 1  /* reserved (pegainfer #1055's 640-column row): refused */
+
+/* ---- device fault bits, ORed into status[0] of the layout's status word ------ */
+#define PSKV_FAULT_BAD_PAGE 1u      /* a table entry outside [0, num_pages): that tile or row skipped */
+#define PSKV_FAULT_PAST_PAGES 2u    /* an append past its row's pages: that row skipped */
+#define PSKV_FAULT_BAD_LENGTH 4u    /* a device length outside [1, table_stride * page_size]: clamped */
+#define PSKV_FAULT_WAIT_TIMEOUT 8u  /* a bounded wait on a copy expired: the partition was dropped */
+#define PSKV_FAULT_EMPTY_ROW 16u    /* a row had no attended key: its output was written as zeros */
+#define PSKV_FAULT_BAD_STATE 32u    /* merge input with m = -inf but l != 0, or a NaN m: treated as empty */
+
+/* ---- limits ---------------------------------------------------------------- */
+#define PSKV_MAX_SPLITS 1024       /* most partitions one decode call may use */
+#define PSKV_AUTO_MAX_SPLITS 256   /* most partitions the automatic plan picks */
+#define PSKV_MERGE_GROUP 16        /* partials folded per level-1 group of the merge */
+#define PSKV_KEY_TILE 16           /* keys per kernel tile; partitions are whole tiles */
+
+/* Description of one paged KV pool.
+ *
+ * k_pool / v_pool are the pool's K region and V region (TensorFold #1619,
+ * "Paged": per layer a K region, then a V region; page p is rows
+ * [ps*p, ps*(p+1)) of each).  Within a page the rows are head-major, so
+ * element (page, kv_head, row, d) of a region is at
+ *     ((page * num_kv_heads + kv_head) * page_size + row) * head_dim + d.
+ * This keeps one head's keys of a page contiguous (a design choice of this
+ * library; the pages do not fix the order inside a page).
+ *
+ * status: device int32[4] the caller zeroes; kernels OR PSKV_FAULT_* bits into
+ * status[0].  May be NULL (faults are then skipped silently).
+ * The format is fixed for the pool's life (pegainfer #1055, Description). */
+typedef struct pskv_layout_desc {
+  int64_t num_pages;   /* pages in each region, >= 1 */
+  int32_t page_size;   /* keys per page: a multiple of PSKV_KEY_TILE */
+  int32_t num_kv_heads;
+  int32_t head_dim_k;  /* 256 or 512 */
+  int32_t head_dim_v;  /* must equal head_dim_k in this build */
+  int32_t kv_dtype;    /* PSKV_DTYPE_F32 or PSKV_DTYPE_BF16 (queries use the same type) */
+  int32_t format;      /* PSKV_FORMAT_SPLIT */
+  void *k_pool;        /* device, 16-byte aligned */
+  void *v_pool;        /* device, 16-byte aligned */
+  int32_t *status;     /* device int32[4] or NULL */
+} pskv_layout_desc;
+
+/* Opaque handle: holds a copy of the description (host memory only). */
+typedef struct pskv_layout pskv_layout;
+
+/* Optional per-call settings; pass NULL for the defaults. */
+typedef struct pskv_decode_opts {
+  int32_t merge_group;        /* partials per level-1 merge group, 1..PSKV_MERGE_GROUP; 0 = PSKV_MERGE_GROUP */
+  pskv_event_t partial_begin; /* if not NULL, recorded on the stream just before the partial kernel */
+  pskv_event_t partial_end;   /* if not NULL, recorded on the stream just after the partial kernel */
+} pskv_decode_opts;
+
+/* Validate `desc` and make a layout handle.  Touches no device.
+ * Errors: INVALID_ARG (null pointers, sizes < 1, misaligned pools,
+ * page_size not a multiple of PSKV_KEY_TILE), UNSUPPORTED (format FOLDED,
+ * head_dim not 256/512, head_dim_k != head_dim_v). */
+int paged_kv_layout_create(const pskv_layout_desc *desc, pskv_layout **out);
+
+/* Free a handle (NULL is ignored).  The pools are the caller's. */
+void paged_kv_layout_destroy(pskv_layout *layout);
+
+/* Append n new rows into the pool, bit for bit (TensorFold #1619, "Writes":
+ * rows copied into the pages keep the linear cache's bits).
+ *   k_new, v_new     device [n][num_kv_heads][head_dim], the pool's dtype, 16-byte aligned
+ *   row_of, pos_of   device int32[n]: table row and key position of each new row
+ *   page_tables      device int32[batch][table_stride]
+ *   pages_of_row     device int32[batch]: pages row b holds (its lease)
+ *   row_of_host, pos_of_host, pages_of_row_host: optional host copies of the
+ *     same arrays (all three or none).  When given they are checked before
+ *     launch and a position at or past pages_of_row[row] * page_size refuses
+ *     the whole call with PSKV_ERR_PAST_PAGES (TensorFold #1619, "Leasing":
+ *     rows past a slot's pages are refused), nothing enqueued.  Without them
+ *     the kernel checks each row and skips a bad one, setting
+ *     PSKV_FAULT_PAST_PAGES or PSKV_FAULT_BAD_PAGE.
+ * (row, pos) pairs must be distinct within one call. */
+int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_new,
+                   const int32_t *row_of, const int32_t *pos_of, int32_t n,
+                   const int32_t *page_tables, int32_t table_stride,
+                   const int32_t *pages_of_row, int32_t batch,
+                   const int32_t *row_of_host, const int32_t *pos_of_host,
+                   const int32_t *pages_of_row_host, pskv_stream_t stream);
+
+/* Split-KV decode: one query token per row.
+ *   q              device [batch][num_q_heads][head_dim], the pool's dtype
+ *   page_tables    device int32[batch][table_stride]; entries past a row's
+ *                  pages are never read
+ *   seq_lens_host  host int32[batch]: keys per row, each in [1, table_stride * page_size];
+ *                  the plan (split count, grid) is made from these
+ *   seq_lens       device int32[batch]: the same lengths, read by the kernels
+ *   scale          score scale (e.g. 1/sqrt(head_dim)); no softcap
+ *   num_splits     partitions per (row, KV head): 1..PSKV_MAX_SPLITS, or 0 for
+ *                  the automatic plan (pskv_plan_splits).  Keys are cut into
+ *                  tiles of PSKV_KEY_TILE; partition p of a row takes tiles
+ *                  [p*c, (p+1)*c) of its attended tiles, c = ceil(tiles / num_splits);
+ *                  trailing partitions may be empty.
+ *   workspace      device scratch of at least decode_attn_workspace_bytes(...)
+ *                  bytes, 256-byte aligned.  On return its head holds the
+ *                  partials: float m[batch][num_q_heads][P], then (at the next
+ *                  256-byte boundary) float l[...][P], then float
+ *                  o[batch][num_q_heads][P][head_dim] (m in units of the scaled
+ *                  score; o of a partition with m = -inf is left unwritten).
+ *   out            device [batch][num_q_heads][head_dim] of out_dtype
+ *                  (PSKV_DTYPE_BF16, round to nearest even, or PSKV_DTYPE_F32)
+ * The result is run-to-run deterministic for a fixed split count.
+ * Errors: INVALID_ARG, UNSUPPORTED (num_q_heads % num_kv_heads != 0 or a
+ * query-group size this build has no kernel for), WORKSPACE_TOO_SMALL, CUDA. */
+int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                        int32_t table_stride, const int32_t *seq_lens_host,
+                        const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,
+                        int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
+                        int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Windowed split-KV decode (pegainfer #1057, Description: the resident pages
+ * hold up to a page more than the window and those keys are masked).  As
+ * decode_attn_splitkv, plus:
+ *   first_pos   device int32[batch]: key i of row b has position first_pos[b] + i
+ *   window_lo   device int32[batch]: key i is attended iff its position >= window_lo[b]
+ * Keys below the bound are neither loaded nor used; partitions cover only the
+ * tiles from the one holding the first attended key.  A row whose bound
+ * excludes every key gets zeros and PSKV_FAULT_EMPTY_ROW. */
+int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                         int32_t table_stride, const int32_t *seq_lens_host,
+                         const int32_t *seq_lens, const int32_t *first_pos,
+                         const int32_t *window_lo, int32_t batch, int32_t num_q_heads,
+                         float scale, int32_t num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, int32_t out_dtype,
+                         const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Merge P partials per row in two levels by the exact rescaling identity and
+ * normalise (gem design, "Candidate ownership and storage"; pegainfer #1055,
+ * Description).  Out of place: level 1 writes its group results into
+ * `workspace`, never into the inputs.
+ *   m, l         device float[rows][num_splits]; m in units of the scaled score
+ *   o            device float[rows][num_splits][head_dim_v], 16-byte aligned
+ *   head_dim_v   a multiple of 4
+ *   out          device [rows][head_dim_v] of out_dtype
+ *   workspace    device scratch of merge_partials_workspace_bytes(...) bytes
+ *   status       device int32[4] fault word or NULL
+ * The empty state is (m = -inf, l = 0) and its o is not read; merging an empty
+ * state changes nothing.  Groups are folded in index order. */
+int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
+                   int32_t num_splits, int32_t head_dim_v, void *out, int32_t out_dtype,
+                   void *workspace, size_t workspace_bytes, int32_t *status,
+                   const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Scratch bytes a decode call needs for `num_splits` partitions (0 = enough
+ * for any automatic plan).  Host-only.  Errors: INVALID_ARG, OVERFLOW. */
+int decode_attn_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
+                                int32_t num_splits, size_t *bytes);
+
+/* Scratch bytes merge_partials needs.  Host-only. */
+int merge_partials_workspace_bytes(int32_t rows, int32_t num_splits, int32_t head_dim_v,
+                                   size_t *bytes);
+
+/* The partial buffer's byte contract (gem design, "Candidate ownership and
+ * storage"): maxima batch*num_q_heads*P*4 bytes, denominators the same,
+ * numerators batch*num_q_heads*P*head_dim_v*4; every product checked for
+ * overflow.  Host-only.  Any output pointer may be NULL. */
+int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_dim_v,
+                               int64_t num_splits, size_t *maxima, size_t *denominators,
+                               size_t *numerators, size_t *total);
+
+/* The split count the automatic plan picks for these lengths on the current
+ * device (num_splits = 0 in a decode call).  It reads the device's SM count;
+ * no kernel runs.  The plan aims for one CTA per SM: for one row,
+ * floor(SMs / num_kv_heads) partitions; for a batch, enough partitions that
+ * the longest row's pieces carry about half an SM's fair share of all tiles.
+ * It depends on the lengths only, never on a window bound. */
+int pskv_plan_splits(const pskv_layout *layout, int32_t batch, const int32_t *seq_lens_host,
+                     int32_t *num_splits);
+
+/* Static text for a status code. */
+const char *pskv_strerror(int status);
+
+/* Text of the last CUDA error seen by this thread (empty if none). */
+const char *pskv_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pskv_kernel_launches(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pskv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PSKV_H */

@@ -335,23 +335,95 @@ static int first_key(const int32_t *first_pos, const int32_t *window_lo, int b, 
   return (int)i0;
 }
 
-static int decode_common(const orc_pool *pool, const void *q, const int32_t *page_tables,
-                         int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
-                         const int32_t *window_lo, int batch, int num_q_heads, double scale,
-                         int online, int chunk_tokens, int num_splits, int group_size,
-                         double *out) {
+/* Index of element 0 of key i of (row b, kv head g), found through the page table. */
+static size_t paged_row(const orc_pool *pool, int dim, const int32_t *page_tables, int table_stride,
+                        int b, int g, int i) {
+  const int32_t page = page_tables[(size_t)b * table_stride + i / pool->page_size];
+  const size_t row = ((size_t)page * pool->num_kv_heads + g) * pool->page_size + (size_t)(i % pool->page_size);
+  return row * (size_t)dim;
+}
+
+/* Checks shared by both decode paths. */
+static int decode_args_ok(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                          int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                          const int32_t *window_lo, int batch, int num_q_heads, double *out) {
   if (!pool_valid(pool) || !q || !page_tables || !seq_lens || !out || batch <= 0 ||
       num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0 || table_stride <= 0 ||
       (!first_pos) != (!window_lo))
     return ORC_ERR_INVALID;
-  if (online && (chunk_tokens <= 0 || num_splits <= 0 || group_size <= 0)) return ORC_ERR_INVALID;
-  const int H = pool->num_kv_heads, dk = pool->head_dim_k, dv = pool->head_dim_v;
-  const int G = num_q_heads / H; /* query heads per kv head; head h reads kv head h / G */
   for (int b = 0; b < batch; ++b) {
     if (seq_lens[b] <= 0 || (int64_t)seq_lens[b] > (int64_t)table_stride * pool->page_size)
       return ORC_ERR_INVALID;
     if (first_key(first_pos, window_lo, b, seq_lens[b]) >= seq_lens[b]) return ORC_ERR_INVALID;
+    for (int j = 0; j < (seq_lens[b] + pool->page_size - 1) / pool->page_size; ++j) {
+      const int32_t page = page_tables[(size_t)b * table_stride + j];
+      if (page < 0 || page >= pool->num_pages) return ORC_ERR_BAD_PAGE;
+    }
   }
+  return ORC_OK;
+}
+
+int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
+                      double *out) {
+  int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo,
+                          batch, num_q_heads, out);
+  if (rc) return rc;
+  const int dk = pool->head_dim_k, dv = pool->head_dim_v;
+  const int G = num_q_heads / pool->num_kv_heads; /* head h reads kv head h / G */
+  int rc_all = ORC_OK;
+  const int jobs = batch * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int job = 0; job < jobs; ++job) {
+    const int b = job / num_q_heads, h = job % num_q_heads, g = h / G, len = seq_lens[b];
+    const int i0 = first_key(first_pos, window_lo, b, len);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(len - i0));
+    double *dst = out + ((size_t)b * num_q_heads + h) * dv;
+    if (!qd || !s) {
+#pragma omp critical
+      rc_all = ORC_ERR_INVALID;
+    } else {
+      for (int d = 0; d < dk; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)b * num_q_heads + h) * dk + d);
+      /* s_i = scale * q . k_i over the attended keys */
+      double mx = -INFINITY;
+      for (int i = i0; i < len; ++i) {
+        const size_t kr = paged_row(pool, dk, page_tables, table_stride, b, g, i);
+        double acc = 0.0;
+        for (int d = 0; d < dk; ++d) acc += qd[d] * load_elem(pool->k, pool->dtype, kr + d);
+        s[i - i0] = scale * acc;
+        if (s[i - i0] > mx) mx = s[i - i0];
+      }
+      /* out = sum_i softmax(s)_i v_i */
+      double z = 0.0;
+      for (int i = i0; i < len; ++i) {
+        s[i - i0] = exp(s[i - i0] - mx);
+        z += s[i - i0];
+      }
+      for (int d = 0; d < dv; ++d) dst[d] = 0.0;
+      for (int i = i0; i < len; ++i) {
+        const double w = s[i - i0] / z;
+        const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
+        for (int d = 0; d < dv; ++d) dst[d] += w * load_elem(pool->v, pool->dtype, vr + d);
+      }
+    }
+    free(qd);
+    free(s);
+  }
+  return rc_all;
+}
+
+int orc_decode_online(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
+                      int chunk_tokens, int num_splits, int group_size, double *out) {
+  int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo,
+                          batch, num_q_heads, out);
+  if (rc) return rc;
+  if (chunk_tokens <= 0 || num_splits <= 0 || group_size <= 0) return ORC_ERR_INVALID;
+  const int H = pool->num_kv_heads, dk = pool->head_dim_k, dv = pool->head_dim_v;
+  const int G = num_q_heads / H;
   int rc_all = ORC_OK;
   const int jobs = batch * H;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -360,11 +432,11 @@ static int decode_common(const orc_pool *pool, const void *q, const int32_t *pag
     double *K = (double *)malloc(sizeof(double) * (size_t)len * dk);
     double *V = (double *)malloc(sizeof(double) * (size_t)len * dv);
     double *qd = (double *)malloc(sizeof(double) * (size_t)dk);
-    int *bounds = online ? (int *)malloc(sizeof(int) * (size_t)(num_splits + 1)) : NULL;
-    int rc = (K && V && qd && (!online || bounds)) ? ORC_OK : ORC_ERR_INVALID;
-    if (!rc) rc = orc_gather(pool, page_tables, table_stride, b, g, len, K, V);
+    int *bounds = (int *)malloc(sizeof(int) * (size_t)(num_splits + 1));
+    int jrc = (K && V && qd && bounds) ? ORC_OK : ORC_ERR_INVALID;
+    if (!jrc) jrc = orc_gather(pool, page_tables, table_stride, b, g, len, K, V);
     const int i0 = first_key(first_pos, window_lo, b, len);
-    if (!rc && online) {
+    if (!jrc) {
       /* chunks aligned to key 0; partitions of ceil(n_chunks / P) chunks over [i0, len) */
       const int c_lo = i0 / chunk_tokens, c_hi = (len + chunk_tokens - 1) / chunk_tokens;
       const int per = (c_hi - c_lo + num_splits - 1) / num_splits;
@@ -375,19 +447,16 @@ static int decode_common(const orc_pool *pool, const void *q, const int32_t *pag
         bounds[p] = (int)e;
       }
     }
-    for (int j = 0; j < G && !rc; ++j) {
+    for (int j = 0; j < G && !jrc; ++j) {
       const int h = g * G + j;
       const size_t qoff = ((size_t)b * num_q_heads + h) * dk;
       for (int d = 0; d < dk; ++d) qd[d] = load_elem(q, pool->dtype, qoff + d);
-      double *dst = out + ((size_t)b * num_q_heads + h) * dv;
-      if (online)
-        rc = orc_attend_partitioned(qd, K, V, dk, dv, bounds, num_splits, group_size, scale, dst);
-      else
-        rc = orc_attend_direct(qd, K, V, dk, dv, i0, len, scale, dst);
+      jrc = orc_attend_partitioned(qd, K, V, dk, dv, bounds, num_splits, group_size, scale,
+                                   out + ((size_t)b * num_q_heads + h) * dv);
     }
-    if (rc) {
+    if (jrc) {
 #pragma omp critical
-      rc_all = rc;
+      rc_all = jrc;
     }
     free(K);
     free(V);
@@ -395,22 +464,6 @@ static int decode_common(const orc_pool *pool, const void *q, const int32_t *pag
     free(bounds);
   }
   return rc_all;
-}
-
-int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
-                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
-                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
-                      double *out) {
-  return decode_common(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo, batch,
-                       num_q_heads, scale, 0, 1, 1, 1, out);
-}
-
-int orc_decode_online(const orc_pool *pool, const void *q, const int32_t *page_tables,
-                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
-                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
-                      int chunk_tokens, int num_splits, int group_size, double *out) {
-  return decode_common(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo, batch,
-                       num_q_heads, scale, 1, chunk_tokens, num_splits, group_size, out);
 }
 
 /* ---- scratch byte contract ([gem] "Candidate ownership and storage") ----- */

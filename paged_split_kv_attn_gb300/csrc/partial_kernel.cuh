@@ -1,0 +1,582 @@
+// partial_kernel.cuh -- the split-KV partial kernel (decode, one query token per row).
+//
+// One CTA computes the online-softmax partial of one (row b, KV head g,
+// partition p): for the G query heads that share KV head g it streams the
+// partition's keys and values once and keeps, per head, the running max m,
+// the running sum l and the unnormalised numerator o (gem "Parked D512 fused
+// split-KV decode design", "Candidate ownership and storage": one first-pass
+// worker per (kv_head, partition), each K/V row staged once for all query
+// heads of the group).
+//
+// Structure (GB300):
+//  * warp 4 is the producer: per 16-key tile it reads the tile's page id from
+//    the table (32 ids per warp-wide load, so one table read serves up to 32
+//    pages; TensorFold #1619 measured a per-key page lookup at +5.8..7.9 % and
+//    moved it to once per tile) and issues one bulk async copy (cp.async.bulk)
+//    per valid key row into a ring of NSTAGE shared-memory stages, counted on
+//    the stage's "full" mbarrier;
+//  * warps 0..3 are consumers: warp w takes tiles w, w+4, w+8, ... of the
+//    partition, each keeping its own (m, l, o) in registers, and releases the
+//    stage on its "empty" mbarrier;
+//  * at the end the four warp states are merged in shared memory by the exact
+//    rescaling identity and the partition's (m, l, o) is written to the
+//    workspace.
+// Rows of a tile past the row's length (or below the window bound) are never
+// copied; their scores are set to -inf by selection and their values masked
+// to zero, so stale shared memory can never reach the result.
+// Shared-memory rows are padded by 16 bytes, which makes the 8 row addresses
+// of every ldmatrix phase fall in distinct bank groups.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pskv_internal.cuh"
+
+namespace pskv {
+
+template <int kRowBytes>
+struct RingGeom {
+  static constexpr int kRowStride = kRowBytes + 16;
+  static constexpr int kTileBytes = kKeyTile * kRowStride;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+  static constexpr int kStages =
+      (200000 / kStageBytes) < 2 ? 2 : ((200000 / kStageBytes) > 8 ? 8 : (200000 / kStageBytes));
+  static constexpr int kRingBytes = kStages * kStageBytes;
+};
+
+// -------------------------------------------------------------------------------------------
+// Tensor-core consumer: bf16 K/V, 8 query heads per KV head.
+// Per tile, S^T[16 keys x 8 heads] = K[16 x D] Q^T[D x 8] (mma m16n8k16, keys as
+// M so no row is wasted), then O^T[D x 8] += V^T[D x 16] P^T[16 x 8], with P^T
+// obtained from the S^T accumulator by movmatrix.trans.  P is applied as a
+// bf16 hi+lo pair (p = hi + lo to ~2^-17 relative), so the weights keep
+// nearly fp32 accuracy while V stays bf16.
+// -------------------------------------------------------------------------------------------
+template <int kD>
+struct MmaConsumer {
+  using Elem = __nv_bfloat16;
+  static constexpr int D = kD;
+  static constexpr int G = 8;
+  static constexpr int KS = D / 16;  // k-steps of the QK product = m-tiles of the PV product
+  static constexpr int kExtraSmem = 0;
+  using Geom = RingGeom<D * 2>;
+  static constexpr int RS = Geom::kRowStride;
+
+  uint32_t qf[KS][2];  // Q^T B-fragments: (d = 16k + 2c + {0,1} [+8], head r)
+  float o[KS][4];      // O^T accumulators: (d = 16j + r [+8], heads 2c, 2c+1)
+  float m0, m1;        // running max (log2 units) of heads 2c, 2c+1; warp-uniform per head
+  float l0, l1;        // this lane's share of the running sums of heads 2c, 2c+1
+  float scale_log2;
+  int r, c;
+
+  static __device__ void prologue(const PartialArgs &, int, int, unsigned char *) {}
+
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, const unsigned char *) {
+    r = lane >> 2;
+    c = lane & 3;
+    scale_log2 = a.scale_log2;
+    const uint16_t *q =
+        static_cast<const uint16_t *>(a.q) + ((size_t)b * a.num_q_heads + h0 + r) * D;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      qf[k][0] = *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c);
+      qf[k][1] = *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c);
+    }
+#pragma unroll
+    for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    m0 = m1 = -CUDART_INF_F;
+    l0 = l1 = 0.f;
+  }
+
+  __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
+                       bool skip, int lane) {
+    const int mi = lane >> 3, rr = lane & 7;
+    // ---- scores: S^T = K Q^T, two accumulator chains for latency
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t kaddr = smem_u32(ks) + ((mi & 1) * 8 + rr) * RS + (mi >> 1) * 16;
+#pragma unroll
+    for (int k = 0; k < KS; k += 2) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kaddr + k * 32, a0, a1, a2, a3);
+      mma_bf16(sa, a0, a1, a2, a3, qf[k][0], qf[k][1]);
+      ldsm_x4(kaddr + (k + 1) * 32, a0, a1, a2, a3);
+      mma_bf16(sb, a0, a1, a2, a3, qf[k + 1][0], qf[k + 1][1]);
+    }
+    const int tA = key0 + r, tB = key0 + r + 8;
+    const bool vA = !skip && tA >= i0 && tA < len;
+    const bool vB = !skip && tB >= i0 && tB < len;
+    const float s00 = vA ? (sa[0] + sb[0]) * scale_log2 : -CUDART_INF_F;  // key r, head 2c
+    const float s01 = vA ? (sa[1] + sb[1]) * scale_log2 : -CUDART_INF_F;  // key r, head 2c+1
+    const float s10 = vB ? (sa[2] + sb[2]) * scale_log2 : -CUDART_INF_F;  // key r+8, head 2c
+    const float s11 = vB ? (sa[3] + sb[3]) * scale_log2 : -CUDART_INF_F;  // key r+8, head 2c+1
+
+    // ---- online softmax update (max over the 16 keys: lanes sharing c)
+    float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float u0 = (n0 == -CUDART_INF_F) ? 0.f : n0;  // nothing attended yet: all weights 0
+    const float u1 = (n1 == -CUDART_INF_F) ? 0.f : n1;
+    const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
+    const float p00 = exp2f(s00 - u0), p01 = exp2f(s01 - u1);
+    const float p10 = exp2f(s10 - u0), p11 = exp2f(s11 - u1);
+    l0 = l0 * al0 + (p00 + p10);
+    l1 = l1 * al1 + (p01 + p11);
+    m0 = n0;
+    m1 = n1;
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        o[j][0] *= al0;
+        o[j][1] *= al1;
+        o[j][2] *= al0;
+        o[j][3] *= al1;
+      }
+    }
+
+    // ---- P^T fragments (hi + lo bf16 pairs), transposed in registers
+    const uint32_t hA = pack_bf16x2(p00, p01), hB = pack_bf16x2(p10, p11);
+    const uint32_t lA = pack_bf16x2(p00 - bf16_lo(hA), p01 - bf16_hi(hA));
+    const uint32_t lB = pack_bf16x2(p10 - bf16_lo(hB), p11 - bf16_hi(hB));
+    const uint32_t bh0 = movmatrix_t(hA), bh1 = movmatrix_t(hB);
+    const uint32_t bl0 = movmatrix_t(lA), bl1 = movmatrix_t(lB);
+
+    // ---- O^T += V^T P^T; V rows of keys not attended are masked to zero
+    const bool full = !skip && key0 >= i0 && key0 + kKeyTile <= len;
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (!full) {
+      const int t0 = key0 + 2 * c, t1 = t0 + 8;
+      auto ok = [&](int t) { return !skip && t >= i0 && t < len; };
+      mlo = (ok(t0) ? 0x0000ffffu : 0u) | (ok(t0 + 1) ? 0xffff0000u : 0u);
+      mhi = (ok(t1) ? 0x0000ffffu : 0u) | (ok(t1 + 1) ? 0xffff0000u : 0u);
+    }
+    const uint32_t vaddr = smem_u32(vs) + (rr + 8 * (mi >> 1)) * RS + (mi & 1) * 16;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vaddr + j * 32, a0, a1, a2, a3);
+      a0 &= mlo;
+      a1 &= mlo;
+      a2 &= mhi;
+      a3 &= mhi;
+      mma_bf16(o[j], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16(o[j], a0, a1, a2, a3, bl0, bl1);
+    }
+  }
+
+  // Sum this warp's per-lane l over the 8 lanes that share a head pair.
+  __device__ void finish() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+
+  // o_s: float[G][D] of this warp; m_s, l_s: float[G] of this warp.
+  __device__ void store(float *o_s, float *m_s, float *l_s) const {
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      o_s[(2 * c) * D + 16 * j + r] = o[j][0];
+      o_s[(2 * c + 1) * D + 16 * j + r] = o[j][1];
+      o_s[(2 * c) * D + 16 * j + r + 8] = o[j][2];
+      o_s[(2 * c + 1) * D + 16 * j + r + 8] = o[j][3];
+    }
+    if (r == 0) {
+      m_s[2 * c] = m0;
+      m_s[2 * c + 1] = m1;
+      l_s[2 * c] = l0;
+      l_s[2 * c + 1] = l1;
+    }
+  }
+};
+
+// -------------------------------------------------------------------------------------------
+// CUDA-core consumer for any supported (element type, D, G): f32 pools, bf16
+// pools with G != 8, or windowed rows with few query heads per KV head.
+// Lane owns E = D/32 elements of every row, in 16-byte chunks k at
+// d = (lane + 32k) * VE, so a warp reads each row as contiguous 512-byte runs.
+// Scores are reduced across the warp by butterfly shuffles; keys are processed
+// four at a time so the softmax rescale is paid once per four keys.
+// -------------------------------------------------------------------------------------------
+template <typename T, int kD, int kG>
+struct SimtConsumer {
+  using Elem = T;
+  static constexpr int D = kD;
+  static constexpr int G = kG;
+  static constexpr int E = D / 32;
+  static constexpr int VE = 16 / (int)sizeof(T);
+  static constexpr int NC = E / VE;
+  static constexpr bool kQInRegs = G * E <= 64;
+  static constexpr int kExtraSmem = kQInRegs ? 0 : G * D * 4;
+  using Geom = RingGeom<D * (int)sizeof(T)>;
+  static constexpr int RS = Geom::kRowStride;
+
+  float q[kQInRegs ? G : 1][kQInRegs ? E : 1];
+  float o[G][E];
+  float m[G], l[G];
+  float scale_log2;
+  const float *q_s;
+  int lane_;
+
+  static __device__ float to_f32(float x) { return x; }
+  static __device__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+  // Load the lane's E elements of a row (global or shared) as f32.
+  static __device__ void load_row(const T *row, int lane, float (&dst)[E]) {
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(row + (lane + 32 * k) * VE);
+      if constexpr (sizeof(T) == 4) {
+        dst[k * VE + 0] = __uint_as_float(raw.x);
+        dst[k * VE + 1] = __uint_as_float(raw.y);
+        dst[k * VE + 2] = __uint_as_float(raw.z);
+        dst[k * VE + 3] = __uint_as_float(raw.w);
+      } else {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          dst[k * VE + 2 * i] = bf16_lo(w[i]);
+          dst[k * VE + 2 * i + 1] = bf16_hi(w[i]);
+        }
+      }
+    }
+  }
+
+  // All threads: stage Q of the group as f32 when it does not fit in registers.
+  static __device__ void prologue(const PartialArgs &a, int b, int h0, unsigned char *extra) {
+    if constexpr (!kQInRegs) {
+      float *qs = reinterpret_cast<float *>(extra);
+      const T *q = static_cast<const T *>(a.q) + ((size_t)b * a.num_q_heads + h0) * D;
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = to_f32(q[i]);
+    }
+  }
+
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, const unsigned char *extra) {
+    lane_ = lane;
+    scale_log2 = a.scale_log2;
+    q_s = reinterpret_cast<const float *>(extra);
+    if constexpr (kQInRegs) {
+      const T *qb = static_cast<const T *>(a.q) + ((size_t)b * a.num_q_heads + h0) * D;
+#pragma unroll
+      for (int g = 0; g < G; ++g) load_row(qb + (size_t)g * D, lane, q[g]);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -CUDART_INF_F;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[g][e] = 0.f;
+    }
+  }
+
+  __device__ float qval(int g, int e) const {
+    if constexpr (kQInRegs) {
+      return q[g][e];
+    } else {
+      const int k = e / VE, v = e % VE;
+      return q_s[g * D + (lane_ + 32 * k) * VE + v];
+    }
+  }
+
+  __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
+                       bool skip, int lane) {
+#pragma unroll 1
+    for (int t0 = 0; t0 < kKeyTile; t0 += 4) {
+      float s[4][G];
+      bool valid[4];
+      bool any = false;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = key0 + t0 + u;
+        valid[u] = !skip && t >= i0 && t < len;
+        any |= valid[u];
+#pragma unroll
+        for (int g = 0; g < G; ++g) s[u][g] = -CUDART_INF_F;
+        if (valid[u]) {
+          float kf[E];
+          load_row(reinterpret_cast<const T *>(ks + (t0 + u) * RS), lane, kf);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc = fmaf(qval(g, e), kf[e], acc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            s[u][g] = acc * scale_log2;
+          }
+        }
+      }
+      if (!any) continue;
+      bool rescale = false;
+      float al[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float x = fmaxf(fmaxf(s[0][g], s[1][g]), fmaxf(s[2][g], s[3][g]));
+        const float n = fmaxf(m[g], x);
+        const float u = (n == -CUDART_INF_F) ? 0.f : n;
+        al[g] = exp2f(m[g] - u);
+        rescale |= (al[g] != 1.f);
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s[k][g] = exp2f(s[k][g] - u);
+          sum += s[k][g];
+        }
+        l[g] = l[g] * al[g] + sum;
+        m[g] = n;
+      }
+      if (rescale) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[g][e] *= al[g];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (!valid[u]) continue;
+        float vf[E];
+        load_row(reinterpret_cast<const T *>(vs + (t0 + u) * RS), lane, vf);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[g][e] = fmaf(s[u][g], vf[e], o[g][e]);
+      }
+    }
+  }
+
+  __device__ void finish() {}
+
+  __device__ void store(float *o_s, float *m_s, float *l_s) const {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int k = e / VE, v = e % VE;
+        o_s[g * D + (lane_ + 32 * k) * VE + v] = o[g][e];
+      }
+      if (lane_ == 0) {
+        m_s[g] = m[g];
+        l_s[g] = l[g];
+      }
+    }
+  }
+};
+
+// -------------------------------------------------------------------------------------------
+// The kernel skeleton shared by both consumers.
+// -------------------------------------------------------------------------------------------
+template <class C>
+struct PartialSmem {
+  using Geom = typename C::Geom;
+  static constexpr int kRing = Geom::kRingBytes;
+  static constexpr int kExtraOff = kRing;
+  static constexpr int kBarOff = (kExtraOff + C::kExtraSmem + 15) / 16 * 16;
+  static constexpr int kSkipOff = kBarOff + 2 * Geom::kStages * 8;
+  static constexpr int kRedOff = kSkipOff + 4 * Geom::kStages;
+  static constexpr int kWeightOff = kRedOff + 2 * kConsumerWarps * C::G * 4;
+  static constexpr int kAbortOff = kWeightOff + kConsumerWarps * C::G * 4;
+  static constexpr int kBytes = kAbortOff + 16;
+  // the warp states alias the ring once every stage has been consumed
+  static_assert(kConsumerWarps * C::G * C::D * 4 <= kRing, "merge area must fit in the ring");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const PartialArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Geom = typename C::Geom;
+  using S = PartialSmem<C>;
+  constexpr int D = C::D, G = C::G, NS = Geom::kStages;
+  constexpr int RB = D * (int)sizeof(typename C::Elem);
+  constexpr int RS = Geom::kRowStride;
+  constexpr int TB = Geom::kTileBytes;
+
+  unsigned char *ring = smem;
+  unsigned char *extra = smem + S::kExtraOff;
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
+  uint64_t *empty_bar = full_bar + NS;
+  int *stage_skip = reinterpret_cast<int *>(smem + S::kSkipOff);
+  float *red_m = reinterpret_cast<float *>(smem + S::kRedOff);  // [warps][G] (log2 units)
+  float *red_l = red_m + kConsumerWarps * G;                       // [warps][G]
+  float *weight = reinterpret_cast<float *>(smem + S::kWeightOff); // [warps][G]
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int P = a.num_splits;
+  const int h0 = g * G;
+
+  // ---- this partition's tiles
+  const long long cap = (long long)a.table_stride * a.page_size;
+  long long len_ll = a.seq_lens[b];
+  if (len_ll < 1 || len_ll > cap) {
+    if (threadIdx.x == 0 && p == 0 && g == 0) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
+    len_ll = len_ll < 0 ? 0 : (len_ll > cap ? cap : len_ll);
+  }
+  const int len = (int)len_ll;
+  int i0 = 0;
+  if (a.window_lo != nullptr) {
+    long long d = (long long)a.window_lo[b] - (long long)a.first_pos[b];
+    i0 = (int)(d < 0 ? 0 : (d > len ? len : d));
+  }
+  const int n_tiles = (len + kKeyTile - 1) / kKeyTile;
+  const int t_lo = i0 < len ? i0 / kKeyTile : n_tiles;
+  const long long total = n_tiles - t_lo;
+  const long long per = (total + P - 1) / P;
+  const long long lo_ll = (long long)p * per < total ? (long long)p * per : total;
+  const long long hi_ll = (long long)(p + 1) * per < total ? (long long)(p + 1) * per : total;
+  const int t_begin = t_lo + (int)lo_ll;
+  const int n_my = (int)(hi_ll - lo_ll);
+
+  const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0
+  if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
+    if (threadIdx.x < G) {
+      a.ws_m[row0 + (size_t)threadIdx.x * P] = -CUDART_INF_F;
+      a.ws_l[row0 + (size_t)threadIdx.x * P] = 0.f;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  C::prologue(a, b, h0, extra);
+  __syncthreads();
+
+  C cons;
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp
+    const int32_t *tbl = a.page_tables + (size_t)b * a.table_stride;
+    const int n_slots = (len + a.page_size - 1) / a.page_size;  // table entries in use
+    int cache_base = -1, cached = -1;
+    int issued = 0;
+    for (int j = 0; j < n_my; ++j) {
+      const int s = j % NS;
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;  // one decision for the whole warp
+      if (j >= NS) {
+        const bool freed = mbar_wait(&empty_bar[s], ((j / NS) - 1) & 1);
+        if (!__all_sync(0xffffffffu, freed)) {
+          if (lane == 0) {
+            raise_fault(a.status, PSKV_FAULT_WAIT_TIMEOUT);
+            *abort_flag = 1;
+          }
+          break;
+        }
+      }
+      const int key0 = (t_begin + j) * kKeyTile;
+      const int slot = key0 / a.page_size;
+      if (cache_base < 0 || slot >= cache_base + 32) {
+        cache_base = slot;
+        const int sl = slot + lane;
+        cached = sl < n_slots ? __ldg(tbl + sl) : -1;
+      }
+      const int page = __shfl_sync(0xffffffffu, cached, slot - cache_base);
+      const bool ok = page >= 0 && (long long)page < a.num_pages;
+      const int r_lo = i0 > key0 ? i0 - key0 : 0;
+      const int r_hi = len - key0 < kKeyTile ? len - key0 : kKeyTile;
+      unsigned char *kdst = ring + s * Geom::kStageBytes;
+      unsigned char *vdst = kdst + TB;
+      if (lane == 0) {
+        stage_skip[s] = ok ? 0 : 1;
+        if (!ok) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
+        mbar_arrive_expect_tx(&full_bar[s], ok ? (uint32_t)(2 * (r_hi - r_lo) * RB) : 0u);
+      }
+      __syncwarp();
+      if (ok && lane < r_hi - r_lo) {
+        const int rowi = r_lo + lane;
+        const size_t grow = ((size_t)page * a.num_kv_heads + g) * a.page_size +
+                            (size_t)(key0 % a.page_size) + rowi;
+        bulk_g2s(kdst + rowi * RS, static_cast<const unsigned char *>(a.k_pool) + grow * RB, RB,
+                 &full_bar[s]);
+        bulk_g2s(vdst + rowi * RS, static_cast<const unsigned char *>(a.v_pool) + grow * RB, RB,
+                 &full_bar[s]);
+      }
+      issued = j + 1;
+    }
+    if (*abort_flag) {
+      // never leave a copy in flight into shared memory this CTA gives up
+      const int first = issued > NS ? issued - NS : 0;
+      for (int j = first; j < issued; ++j) mbar_wait(&full_bar[j % NS], (j / NS) & 1);
+    }
+  } else {
+    // ---------------- consumer warps
+    cons.init(a, b, h0, lane, extra);
+    for (int j = warp; j < n_my; j += kConsumerWarps) {
+      const int s = j % NS;
+      const bool landed = mbar_wait(&full_bar[s], (j / NS) & 1);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          raise_fault(a.status, PSKV_FAULT_WAIT_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const unsigned char *kst = ring + s * Geom::kStageBytes;
+      cons.tile(kst, kst + TB, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+    cons.finish();
+  }
+  __syncthreads();
+  if (*abort_flag) return;
+
+  // ---- merge the four warp states (the ring is free now) and write the partial
+  float *o_s = reinterpret_cast<float *>(ring);  // [warps][G][D]
+  if (warp < kConsumerWarps) cons.store(o_s + (size_t)warp * G * D, red_m + warp * G, red_l + warp * G);
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = -CUDART_INF_F;
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
+    float L = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = red_m[w * G + h];
+      const float wt = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+      weight[w * G + h] = wt;
+      L += wt * red_l[w * G + h];
+    }
+    a.ws_m[row0 + (size_t)h * P] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * kLn2;
+    a.ws_l[row0 + (size_t)h * P] = L;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int h = idx / D, d = idx - h * D;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float wt = weight[w * G + h];
+      if (wt != 0.f) acc = fmaf(o_s[(w * G + h) * D + d], wt, acc);
+    }
+    a.ws_o[(row0 + (size_t)h * P) * D + d] = acc;
+  }
+}
+
+template <class C>
+cudaError_t launch_partial_kernel(const PartialArgs &a, dim3 grid, cudaStream_t stream) {
+  constexpr int bytes = PartialSmem<C>::kBytes;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(pskv_partial_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  pskv_partial_kernel<C><<<grid, kThreads, bytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pskv

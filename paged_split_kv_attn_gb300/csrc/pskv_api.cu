@@ -1,0 +1,362 @@
+// pskv_api.cu -- the C entry points declared in include/pskv.h.
+//
+// Each entry point checks its host-visible arguments (pskv_plan.cpp), makes
+// the plan, carves the caller's workspace and enqueues the kernels on the
+// caller's stream.  It never allocates device memory and never synchronizes.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "pskv_internal.cuh"
+#include "pskv_plan.h"
+
+using namespace pskv;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return PSKV_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int sm_count(int *out) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return PSKV_OK;
+    }
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return PSKV_OK;
+}
+
+int merge_group_of(const pskv_decode_opts *opts, int *group) {
+  int g = (opts && opts->merge_group) ? opts->merge_group : PSKV_MERGE_GROUP;
+  if (g < 1 || g > PSKV_MERGE_GROUP) return PSKV_ERR_INVALID_ARG;
+  *group = g;
+  return PSKV_OK;
+}
+
+// Level 2 folds at most this many group results per row.
+constexpr int kMaxGroups = 64;
+
+int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                  int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
+                  const int32_t *first_pos, const int32_t *window_lo, bool windowed,
+                  int32_t batch, int32_t num_q_heads, float scale, int32_t num_splits,
+                  void *workspace, size_t workspace_bytes, void *out, int32_t out_dtype,
+                  const pskv_decode_opts *opts, pskv_stream_t stream) {
+  if (!layout || !q || !page_tables || !seq_lens_host || !seq_lens || !workspace || !out)
+    return PSKV_ERR_INVALID_ARG;
+  if (windowed && (!first_pos || !window_lo)) return PSKV_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 65535 || num_q_heads < 1 || table_stride < 1) return PSKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PSKV_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > PSKV_MAX_SPLITS) return PSKV_ERR_INVALID_ARG;
+  if (out_dtype != PSKV_DTYPE_F32 && out_dtype != PSKV_DTYPE_BF16) return PSKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(workspace, 16) || !aligned(out, 16)) return PSKV_ERR_INVALID_ARG;
+  const pskv_layout_desc &d = layout->d;
+  if (num_q_heads % d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
+  if (d.num_kv_heads > 65535) return PSKV_ERR_UNSUPPORTED;
+  const int group = num_q_heads / d.num_kv_heads;
+  const int kernel = pick_kernel(d.kv_dtype, d.head_dim_k, group);
+  if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
+  int rc = check_lengths(layout, batch, table_stride, seq_lens_host);
+  if (rc) return rc;
+  int mgroup = 0;
+  if ((rc = merge_group_of(opts, &mgroup))) return rc;
+
+  int P = num_splits;
+  if (P == 0) {
+    int n_sm = 0;
+    if ((rc = sm_count(&n_sm))) return rc;
+    P = plan_splits(n_sm, batch, d.num_kv_heads, seq_lens_host);
+  }
+  WorkspacePlan w;
+  if ((rc = plan_workspace(batch, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
+  if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
+  if (workspace_bytes < w.total) return PSKV_ERR_WORKSPACE_TOO_SMALL;
+
+  char *ws = static_cast<char *>(workspace);
+  PartialArgs a;
+  a.q = q;
+  a.k_pool = d.k_pool;
+  a.v_pool = d.v_pool;
+  a.page_tables = page_tables;
+  a.seq_lens = seq_lens;
+  a.first_pos = windowed ? first_pos : nullptr;
+  a.window_lo = windowed ? window_lo : nullptr;
+  a.status = d.status;
+  a.ws_m = reinterpret_cast<float *>(ws + w.m_off);
+  a.ws_l = reinterpret_cast<float *>(ws + w.l_off);
+  a.ws_o = reinterpret_cast<float *>(ws + w.o_off);
+  a.num_pages = d.num_pages;
+  a.table_stride = table_stride;
+  a.page_size = d.page_size;
+  a.num_kv_heads = d.num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.num_splits = P;
+  a.scale_log2 = scale * kLog2e;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(P, d.num_kv_heads, batch);
+  cudaError_t e;
+  if (opts && opts->partial_begin) {
+    e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (kernel == kKernelMma)
+    e = launch_partial_mma(a, d.head_dim_k, grid, s);
+  else if (d.kv_dtype == PSKV_DTYPE_F32)
+    e = launch_partial_simt_f32(a, d.head_dim_k, group, grid, s);
+  else
+    e = launch_partial_simt_bf16(a, d.head_dim_k, group, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (opts && opts->partial_end) {
+    e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_end), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+
+  MergeArgs m;
+  m.m = a.ws_m;
+  m.l = a.ws_l;
+  m.o = a.ws_o;
+  m.rows = batch * num_q_heads;
+  m.count = P;
+  m.dv = d.head_dim_v;
+  m.group = mgroup;
+  m.m1 = reinterpret_cast<float *>(ws + w.m1_off);
+  m.l1 = reinterpret_cast<float *>(ws + w.l1_off);
+  m.o1 = reinterpret_cast<float *>(ws + w.o1_off);
+  m.out = out;
+  m.out_dtype = out_dtype;
+  m.status = d.status;
+  int launched = 0;
+  e = launch_merge(m, s, &launched);
+  g_launches.fetch_add((uint64_t)launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return PSKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_kv_layout_create(const pskv_layout_desc *desc, pskv_layout **out) {
+  if (!out) return PSKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int rc = check_layout_desc(desc);
+  if (rc) return rc;
+  pskv_layout *l = new (std::nothrow) pskv_layout;
+  if (!l) return PSKV_ERR_INVALID_ARG;
+  l->d = *desc;
+  l->elem_size = desc->kv_dtype == PSKV_DTYPE_BF16 ? 2 : 4;
+  l->row_bytes = desc->head_dim_k * l->elem_size;
+  *out = l;
+  return PSKV_OK;
+}
+
+void paged_kv_layout_destroy(pskv_layout *layout) { delete layout; }
+
+int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_new,
+                   const int32_t *row_of, const int32_t *pos_of, int32_t n,
+                   const int32_t *page_tables, int32_t table_stride,
+                   const int32_t *pages_of_row, int32_t batch, const int32_t *row_of_host,
+                   const int32_t *pos_of_host, const int32_t *pages_of_row_host,
+                   pskv_stream_t stream) {
+  if (!layout || n < 0 || batch < 1 || table_stride < 1) return PSKV_ERR_INVALID_ARG;
+  if (n == 0) return PSKV_OK;
+  if (!k_new || !v_new || !row_of || !pos_of || !page_tables || !pages_of_row)
+    return PSKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PSKV_ERR_INVALID_ARG;
+  const int hosts = (row_of_host != nullptr) + (pos_of_host != nullptr) +
+                    (pages_of_row_host != nullptr);
+  if (hosts != 0 && hosts != 3) return PSKV_ERR_INVALID_ARG;
+  if (hosts == 3) {
+    const int rc = check_append_host(layout, n, table_stride, batch, row_of_host, pos_of_host,
+                                     pages_of_row_host);
+    if (rc) return rc;
+  }
+  AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.row_of = row_of;
+  a.pos_of = pos_of;
+  a.n = n;
+  a.page_tables = page_tables;
+  a.table_stride = table_stride;
+  a.pages_of_row = pages_of_row;
+  a.batch = batch;
+  a.k_pool = layout->d.k_pool;
+  a.v_pool = layout->d.v_pool;
+  a.num_pages = layout->d.num_pages;
+  a.page_size = layout->d.page_size;
+  a.num_kv_heads = layout->d.num_kv_heads;
+  a.row_bytes = layout->row_bytes;
+  a.status = layout->d.status;
+  const cudaError_t e = launch_append(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return PSKV_OK;
+}
+
+int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                        int32_t table_stride, const int32_t *seq_lens_host,
+                        const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,
+                        int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
+                        int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream) {
+  return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
+                       nullptr, false, batch, num_q_heads, scale, num_splits, workspace,
+                       workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                         int32_t table_stride, const int32_t *seq_lens_host,
+                         const int32_t *seq_lens, const int32_t *first_pos,
+                         const int32_t *window_lo, int32_t batch, int32_t num_q_heads,
+                         float scale, int32_t num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, int32_t out_dtype,
+                         const pskv_decode_opts *opts, pskv_stream_t stream) {
+  return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, first_pos,
+                       window_lo, true, batch, num_q_heads, scale, num_splits, workspace,
+                       workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
+                   int32_t num_splits, int32_t head_dim_v, void *out, int32_t out_dtype,
+                   void *workspace, size_t workspace_bytes, int32_t *status,
+                   const pskv_decode_opts *opts, pskv_stream_t stream) {
+  if (!m || !l || !o || !out || rows < 1 || num_splits < 1 || num_splits > PSKV_MAX_SPLITS ||
+      head_dim_v < 4 || head_dim_v % 4 != 0)
+    return PSKV_ERR_INVALID_ARG;
+  if (rows > 65535) return PSKV_ERR_UNSUPPORTED;
+  if (out_dtype != PSKV_DTYPE_F32 && out_dtype != PSKV_DTYPE_BF16) return PSKV_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(out, 16) || !aligned(m, 4) || !aligned(l, 4))
+    return PSKV_ERR_INVALID_ARG;
+  int group = 0, rc;
+  if ((rc = merge_group_of(opts, &group))) return rc;
+  WorkspacePlan w;
+  if ((rc = plan_workspace(1, rows, head_dim_v, num_splits, group, &w))) return rc;
+  if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
+  const size_t need = w.total - w.m1_off;  // only the level-1 sections are used
+  if (w.groups > 1 && (!workspace || workspace_bytes < need)) return PSKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace && !aligned(workspace, 16)) return PSKV_ERR_INVALID_ARG;
+  char *ws = static_cast<char *>(workspace);
+  MergeArgs a;
+  a.m = m;
+  a.l = l;
+  a.o = o;
+  a.rows = rows;
+  a.count = num_splits;
+  a.dv = head_dim_v;
+  a.group = group;
+  a.m1 = ws ? reinterpret_cast<float *>(ws) : nullptr;
+  a.l1 = ws ? reinterpret_cast<float *>(ws + (w.l1_off - w.m1_off)) : nullptr;
+  a.o1 = ws ? reinterpret_cast<float *>(ws + (w.o1_off - w.m1_off)) : nullptr;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.status = status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (opts && opts->partial_begin) {
+    e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  int launched = 0;
+  e = launch_merge(a, s, &launched);
+  g_launches.fetch_add((uint64_t)launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (opts && opts->partial_end) {
+    e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_end), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PSKV_OK;
+}
+
+int decode_attn_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
+                                int32_t num_splits, size_t *bytes) {
+  if (!bytes || num_splits < 0 || num_splits > PSKV_MAX_SPLITS) return PSKV_ERR_INVALID_ARG;
+  const int64_t p = num_splits == 0 ? PSKV_AUTO_MAX_SPLITS : num_splits;
+  WorkspacePlan w;
+  const int rc = plan_workspace(batch, num_q_heads, head_dim_v, p, PSKV_MERGE_GROUP, &w);
+  if (rc) return rc;
+  *bytes = w.total;
+  return PSKV_OK;
+}
+
+int merge_partials_workspace_bytes(int32_t rows, int32_t num_splits, int32_t head_dim_v,
+                                   size_t *bytes) {
+  if (!bytes || num_splits < 1 || num_splits > PSKV_MAX_SPLITS) return PSKV_ERR_INVALID_ARG;
+  WorkspacePlan w;
+  const int rc = plan_workspace(1, rows, head_dim_v, num_splits, PSKV_MERGE_GROUP, &w);
+  if (rc) return rc;
+  *bytes = w.total - w.m1_off;
+  return PSKV_OK;
+}
+
+int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_dim_v,
+                               int64_t num_splits, size_t *maxima, size_t *denominators,
+                               size_t *numerators, size_t *total) {
+  if (batch < 1 || num_q_heads < 1 || head_dim_v < 1 || num_splits < 1)
+    return PSKV_ERR_INVALID_ARG;
+  size_t states, nums, sum;
+  if (__builtin_mul_overflow((size_t)batch, (size_t)num_q_heads, &states) ||
+      __builtin_mul_overflow(states, (size_t)num_splits, &states) ||
+      __builtin_mul_overflow(states, (size_t)4, &states) ||
+      __builtin_mul_overflow(states, (size_t)head_dim_v, &nums) ||
+      __builtin_add_overflow(states, states, &sum) || __builtin_add_overflow(sum, nums, &sum))
+    return PSKV_ERR_OVERFLOW;
+  if (maxima) *maxima = states;
+  if (denominators) *denominators = states;
+  if (numerators) *numerators = nums;
+  if (total) *total = sum;
+  return PSKV_OK;
+}
+
+int pskv_plan_splits(const pskv_layout *layout, int32_t batch, const int32_t *seq_lens_host,
+                     int32_t *num_splits) {
+  if (!layout || !seq_lens_host || !num_splits || batch < 1) return PSKV_ERR_INVALID_ARG;
+  int n_sm = 0;
+  const int rc = sm_count(&n_sm);
+  if (rc) return rc;
+  *num_splits = plan_splits(n_sm, batch, layout->d.num_kv_heads, seq_lens_host);
+  return PSKV_OK;
+}
+
+const char *pskv_strerror(int status) {
+  switch (status) {
+    case PSKV_OK: return "ok";
+    case PSKV_ERR_INVALID_ARG: return "invalid argument";
+    case PSKV_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case PSKV_ERR_OVERFLOW: return "size overflow";
+    case PSKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PSKV_ERR_PAST_PAGES: return "position past the row's pages";
+    case PSKV_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char *pskv_last_cuda_error(void) { return g_cuda_error; }
+
+uint64_t pskv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pskv_version(void) { return 100; }
+
+}  // extern "C"

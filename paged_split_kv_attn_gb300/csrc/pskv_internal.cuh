@@ -1,0 +1,197 @@
+// pskv_internal.cuh -- shared declarations of the CUDA library (not installed).
+//
+// Device helpers wrap the sm_90+/sm_100 PTX the kernels use: mbarriers, the
+// bulk async copy engine (cp.async.bulk, "TMA" without a tensor map),
+// ldmatrix / movmatrix and the bf16 mma.  Every wait on an mbarrier is
+// bounded; a wait that expires reports failure instead of spinning forever.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pskv.h"
+
+namespace pskv {
+
+constexpr int kKeyTile = PSKV_KEY_TILE;  // keys per tile
+constexpr int kConsumerWarps = 4;        // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr uint32_t kWaitPolls = 1u << 22;            // try_wait polls before giving up
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Arguments of the split-KV partial kernels (one launch, grid (P, Hkv, B)).
+struct PartialArgs {
+  const void *q;             // [B][Hq][D]
+  const void *k_pool;        // [num_pages][Hkv][ps][D]
+  const void *v_pool;
+  const int32_t *page_tables;  // [B][table_stride]
+  const int32_t *seq_lens;     // [B]
+  const int32_t *first_pos;    // [B] or null
+  const int32_t *window_lo;    // [B] or null
+  int32_t *status;             // fault word or null
+  float *ws_m;                 // [B][Hq][P]
+  float *ws_l;                 // [B][Hq][P]
+  float *ws_o;                 // [B][Hq][P][D]
+  long long num_pages;
+  int table_stride;
+  int page_size;
+  int num_kv_heads;
+  int num_q_heads;
+  int num_splits;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Arguments of the merge kernels.  Level 1 folds groups of `group` partials
+// of each row into (m1, l1, o1); level 2 folds `count` states per row and
+// writes the normalised output.
+struct MergeArgs {
+  const float *m;  // [rows][count]
+  const float *l;
+  const float *o;  // [rows][count][dv]
+  int rows;
+  int count;
+  int dv;
+  int group;
+  float *m1;  // [rows][ceil(count / group)]
+  float *l1;
+  float *o1;  // [rows][ceil(count / group)][dv]
+  void *out;  // [rows][dv]
+  int out_dtype;
+  int32_t *status;
+};
+
+struct AppendArgs {
+  const void *k_new;  // [n][Hkv][D]
+  const void *v_new;
+  const int32_t *row_of;
+  const int32_t *pos_of;
+  int n;
+  const int32_t *page_tables;
+  int table_stride;
+  const int32_t *pages_of_row;
+  int batch;
+  void *k_pool;
+  void *v_pool;
+  long long num_pages;
+  int page_size;
+  int num_kv_heads;
+  int row_bytes;  // head_dim * element size, a multiple of 16
+  int32_t *status;
+};
+
+// Host-side launchers (one per kernel family).  They return a CUDA error code.
+cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, dim3 grid, cudaStream_t s);
+cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int group, dim3 grid,
+                                    cudaStream_t s);
+cudaError_t launch_partial_simt_bf16(const PartialArgs &a, int head_dim, int group, dim3 grid,
+                                     cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void raise_fault(int32_t *status, uint32_t bits) {
+  if (status) atomicOr(reinterpret_cast<unsigned int *>(status), bits);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// One bulk copy global -> shared; completion is counted in bytes on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                        uint32_t &a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                          uint32_t &a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// c += A(16x16, row) * B(16x8, col), bf16 inputs, f32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+#endif  // __CUDACC__
+
+}  // namespace pskv

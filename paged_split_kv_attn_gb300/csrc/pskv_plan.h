@@ -1,0 +1,49 @@
+// pskv_plan.h -- host-only planning and argument checks (no CUDA calls).
+//
+// Kept free of CUDA so it can be compiled and tested on any host, including
+// under the address and undefined-behaviour sanitizers.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pskv.h"
+
+struct pskv_layout {
+  pskv_layout_desc d;
+  int elem_size;  // bytes per element
+  int row_bytes;  // bytes of one key (or value) row of one head
+};
+
+namespace pskv {
+
+// Byte offsets of the workspace sections (each 256-byte aligned).
+struct WorkspacePlan {
+  size_t m_off, l_off, o_off;     // partials: m, l [rows][P], o [rows][P][dv]
+  size_t m1_off, l1_off, o1_off;  // level-1 group results: [rows][ng], [rows][ng][dv]
+  size_t total;
+  int groups;  // ng = ceil(P / group)
+};
+
+int check_layout_desc(const pskv_layout_desc *d);
+
+// Sizes of the decode workspace for `splits` partitions folded in groups of `group`.
+int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64_t splits,
+                   int64_t group, WorkspacePlan *out);
+
+// Checks the host lengths: each in [1, table_stride * page_size].
+int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride,
+                  const int32_t *seq_lens_host);
+
+// Automatic split count for `n_sm` SMs (one CTA per SM at a time).
+int plan_splits(int n_sm, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host);
+
+// Checks host copies of an append's rows against the leases.
+int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride, int32_t batch,
+                      const int32_t *row_of, const int32_t *pos_of, const int32_t *pages_of_row);
+
+// Which partial kernel family serves (dtype, head_dim, group); -1 if none.
+enum { kKernelMma = 0, kKernelSimt = 1 };
+int pick_kernel(int kv_dtype, int head_dim, int group);
+
+}  // namespace pskv
