@@ -288,6 +288,8 @@ def parse():
     ap.add_argument("--no-window", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph")
     ap.add_argument("--sweep", type=int, nargs="*", default=None,
                     help="also time each global context alone at these split counts")
     return ap.parse_args()
@@ -403,28 +405,27 @@ def main():
         per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
                             "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9}
 
-    # per-call µs/call (append + partial + merge), each call timed alone with a cold L2
+    # per-call µs/call (append + partial + merge), each call timed alone with a cold L2:
+    # a 256 MB buffer is READ between calls (reads leave no dirty lines to write back)
+    flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
     for c in calls:
-        flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
         times = []
         for it in range(max(5, min(args.steps, 30))):
-            flush.fill_(it & 0xFF)
+            flush.sum()
             b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b.record(stream)
             c.run(it)
             e.record(stream)
             torch.cuda.synchronize()
             times.append(b.elapsed_time(e) * 1e3)
-        del flush
         per_call[c.name]["us_per_call_median"] = statistics.median(times)
         per_call[c.name]["GBps_per_call"] = c.bytes / (statistics.median(times) * 1e-6) / 1e9
-        per_call[c.name]["splits"] = c.splits or pskv.pskv_plan_splits(c.layouts[0], c.lens_host)
+        per_call[c.name]["splits"] = c.splits or pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads, c.lens_host)
 
     # optional split sweep of the global contexts (each call alone, cold L2)
     sweep = None
     if args.sweep:
         sweep = {}
-        flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
         for c in calls:
             if c.windowed:
                 continue
@@ -434,7 +435,7 @@ def main():
                 c.ws = pskv.workspace(1, 32, 512, p, dev)
                 times = []
                 for it in range(10):
-                    flush.fill_(it & 0xFF)
+                    flush.sum()
                     b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     b.record(stream)
                     c.run(it)
@@ -444,7 +445,36 @@ def main():
                 res[p] = statistics.median(times)
             sweep[c.name] = res
             c.splits = args.splits
-        del flush
+            c.ws = pskv.workspace(1, 32, 512, args.splits, dev)
+    del flush
+
+    # the same step captured once in a CUDA graph and replayed (launch cost amortised)
+    graph_ms = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for it in range(ROTATE):
+                for c in calls:
+                    c.run(it)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for it in range(ROTATE):
+                for c in calls:
+                    c.run(it)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // ROTATE)
+        gb, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gb.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ge.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = gb.elapsed_time(ge) / (reps * ROTATE)
 
     # end-to-end through the public calls from pinned host buffers
     for it in range(args.warmup):
@@ -490,6 +520,11 @@ def main():
             "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
     if sweep is not None:
         line["split_sweep_us"] = sweep
+    if graph_ms is not None:
+        line["graph"] = {"ms_per_step": graph_ms,
+                         "value": step_bytes * dist.world / (graph_ms * 1e-3) / 1e9,
+                         "unit": "GB/s",
+                         "note": "the same step captured once in a CUDA graph and replayed"}
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline([c.case for c in calls], args.cpu_seconds)
     if dist.rank == 0:

@@ -226,13 +226,14 @@ int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_
                                size_t *numerators, size_t *total);
 
 /* The split count the automatic plan picks for these lengths on the current
- * device (num_splits = 0 in a decode call).  It reads the device's SM count;
- * no kernel runs.  The plan aims for one CTA per SM: for one row,
- * floor(SMs / num_kv_heads) partitions; for a batch, enough partitions that
- * the longest row's pieces carry about half an SM's fair share of all tiles.
- * It depends on the lengths only, never on a window bound. */
-int pskv_plan_splits(const pskv_layout *layout, int32_t batch, const int32_t *seq_lens_host,
-                     int32_t *num_splits);
+ * device (num_splits = 0 in a decode call).  It reads the device's SM count
+ * and how many CTAs of the serving kernel fit on an SM; no kernel runs.  The
+ * plan aims for one wave of CTAs: for one row, floor(slots / num_kv_heads)
+ * partitions (slots = SMs x CTAs per SM); for a batch, enough partitions that
+ * the longest row's pieces carry about half a slot's fair share of all
+ * tiles.  It depends on the lengths only, never on a window bound. */
+int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_heads,
+                     const int32_t *seq_lens_host, int32_t *num_splits);
 
 /* Static text for a status code. */
 const char *pskv_strerror(int status);

@@ -96,7 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.decode_attn_workspace_bytes.argtypes = [I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.merge_partials_workspace_bytes.argtypes = [I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pskv_partial_scratch_bytes.argtypes = [I64, I64, I64, I64] + [ctypes.POINTER(SZ)] * 4
-    lib.pskv_plan_splits.argtypes = [P, I32, P, ctypes.POINTER(I32)]
+    lib.pskv_plan_splits.argtypes = [P, I32, I32, P, ctypes.POINTER(I32)]
     lib.pskv_strerror.argtypes = [ctypes.c_int]
     lib.pskv_strerror.restype = ctypes.c_char_p
     lib.pskv_last_cuda_error.argtypes = []
@@ -279,10 +279,11 @@ def pskv_partial_scratch_bytes(batch: int, num_q_heads: int, head_dim_v: int, nu
     return tuple(int(v.value) for v in vals)
 
 
-def pskv_plan_splits(layout: Layout, seq_lens_host) -> int:
+def pskv_plan_splits(layout: Layout, num_q_heads: int, seq_lens_host) -> int:
     lens = _host_i32(seq_lens_host, "seq_lens_host")
     out = ctypes.c_int32()
-    _check(load_library().pskv_plan_splits(layout.handle, len(lens), lens, ctypes.byref(out)),
+    _check(load_library().pskv_plan_splits(layout.handle, len(lens), num_q_heads, lens,
+                                           ctypes.byref(out)),
            "pskv_plan_splits")
     return int(out.value)
 

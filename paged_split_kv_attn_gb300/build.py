@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpskv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
+FLAGS = ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["partial_mma.cu", "partial_simt_f32.cu", "partial_simt_bf16.cu", "merge.cu",
            "append.cu", "pskv_api.cu", "pskv_plan.cpp"]
 
@@ -45,11 +45,11 @@ def _up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, extra: list[str], build_dir: str) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
-        cmd = [nvcc(), *FLAGS, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc(), *FLAGS, *extra, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
     elif verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,23 +58,30 @@ def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
     return obj, res.stdout + res.stderr
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link the library unless it is newer than every source; return its path."""
-    if not force and not verbose_ptxas and _up_to_date():
+def build(force: bool = False, verbose_ptxas: bool = False, defines: dict | None = None,
+          out: str = LIB) -> str:
+    """Compile and link the library unless it is newer than every source; return its path.
+
+    ``defines`` sets the compile-time tuning macros (for example
+    ``{"PSKV_MMA_WARPS": 4}``); a build with defines goes to ``out`` and is
+    always rebuilt."""
+    extra = [f"-D{k}={v}" for k, v in (defines or {}).items()]
+    if not force and not verbose_ptxas and not extra and out == LIB and _up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if out == LIB else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
+        results = list(ex.map(lambda s: _compile(s, verbose_ptxas, extra, build_dir), SOURCES))
     if verbose_ptxas:
         for _, log in results:
             sys.stdout.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -16,6 +16,8 @@ constexpr int kAppendWarps = 4;
 __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const AppendArgs a) {
   const long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_launch_dependents();
   if (item >= (long long)a.n * a.num_kv_heads) return;
   const int r = (int)(item / a.num_kv_heads), h = (int)(item % a.num_kv_heads);
   const int b = a.row_of[r], pos = a.pos_of[r];
@@ -53,8 +55,7 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
   const long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  pskv_append_rows<<<(unsigned)blocks, kAppendWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(pskv_append_rows, dim3((unsigned)blocks), dim3(kAppendWarps * 32), 0, s, a);
 }
 
 }  // namespace pskv

@@ -21,42 +21,88 @@ namespace pskv {
 
 constexpr int kMergeThreads = 128;
 constexpr int kMaxStates = 64;  // states one level-2 block folds (PSKV_MAX_SPLITS / PSKV_MERGE_GROUP)
+constexpr int kChunk = 16;      // states whose o is loaded together (all loads in flight at once)
 
-// Weights e^(m_i - M) of `n` states (thread 0 computes; the block reads them).
+// Warp 0 reads the n states' (m, l) in parallel and computes the weights
+// w_i = e^(m_i - M) (-1 marks an empty state, whose o is skipped), M and l.
 __device__ void state_weights(const float *m, const float *l, int n, float *w_s, float *M_s,
                               float *L_s, int32_t *status) {
-  if (threadIdx.x == 0) {
-    float M = -CUDART_INF_F;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float mi[kMaxStates / 32], li[kMaxStates / 32];
     bool bad = false;
-    for (int i = 0; i < n; ++i) {
-      const float mi = m[i];
-      if (isnan(mi) || (mi == -CUDART_INF_F && l[i] != 0.f)) bad = true;
-      else M = fmaxf(M, mi);
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int k = 0; k < kMaxStates / 32; ++k) {
+      const int i = lane + 32 * k;
+      mi[k] = i < n ? m[i] : -CUDART_INF_F;
+      li[k] = i < n ? l[i] : 0.f;
+      if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
+        bad = true;
+        mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
+      }
+      M = fmaxf(M, mi[k]);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
-    for (int i = 0; i < n; ++i) {
-      const float mi = m[i];
-      const bool empty = isnan(mi) || mi == -CUDART_INF_F;
-      const float w = empty ? 0.f : exp2f((mi - M) * kLog2e);
-      w_s[i] = empty ? -1.f : w;  // -1 marks "skip this state's o"
-      if (!empty) L = fmaf(l[i], w, L);
+#pragma unroll
+    for (int k = 0; k < kMaxStates / 32; ++k) {
+      const int i = lane + 32 * k;
+      const bool empty = mi[k] == -CUDART_INF_F;
+      const float w = empty ? 0.f : exp2f((mi[k] - M) * kLog2e);
+      if (i < n) w_s[i] = empty ? -1.f : w;
+      // fixed-order sum: lane partials, then a butterfly (same bits every run)
+      if (!empty) L = fmaf(li[k], w, L);
     }
-    if (bad) raise_fault(status, PSKV_FAULT_BAD_STATE);
-    *M_s = M;
-    *L_s = L;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_fault(status, PSKV_FAULT_BAD_STATE);
+    if (lane == 0) {
+      *M_s = M;
+      *L_s = L;
+    }
   }
   __syncthreads();
 }
 
+// acc += sum_i w_i o_i[d4] over states [0, n) of `o` (row stride dv floats),
+// kChunk loads in flight at a time; empty states are skipped by selection.
+__device__ __forceinline__ float4 fold_o(const float *o, int n, int dv, int d4, const float *w_s) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < n; i0 += kChunk) {
+    float4 v[kChunk];
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k)
+      if (i0 + k < n && w_s[i0 + k] >= 0.f)
+        v[k] = __ldg(reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4);
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      if (i0 + k < n) {
+        const float w = w_s[i0 + k];
+        if (w >= 0.f) {
+          acc.x = fmaf(v[k].x, w, acc.x);
+          acc.y = fmaf(v[k].y, w, acc.y);
+          acc.z = fmaf(v[k].z, w, acc.z);
+          acc.w = fmaf(v[k].w, w, acc.w);
+        }
+      }
+    }
+  }
+  return acc;
+}
+
 // grid (groups, rows): fold partials [grp*group, min(count, (grp+1)*group)) of a row.
 __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level1(const MergeArgs a) {
-  __shared__ float w_s[PSKV_MERGE_GROUP];
+  __shared__ float w_s[kMaxStates];
   __shared__ float M_s, L_s;
   const int grp = blockIdx.x, row = blockIdx.y;
   const int ng = (a.count + a.group - 1) / a.group;
   const int p0 = grp * a.group;
   const int n = min(a.count - p0, a.group);
   const size_t base = (size_t)row * a.count + p0;
+  pdl_wait();
+  pdl_launch_dependents();
   state_weights(a.m + base, a.l + base, n, w_s, &M_s, &L_s, a.status);
   const size_t out_state = (size_t)row * ng + grp;
   if (threadIdx.x == 0) {
@@ -64,19 +110,9 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level1(const MergeAr
     a.l1[out_state] = L_s;
   }
   const int dv4 = a.dv / 4;
-  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float w = w_s[i];
-      if (w < 0.f) continue;
-      const float4 v = reinterpret_cast<const float4 *>(a.o + (base + i) * a.dv)[d4];
-      acc.x = fmaf(v.x, w, acc.x);
-      acc.y = fmaf(v.y, w, acc.y);
-      acc.z = fmaf(v.z, w, acc.z);
-      acc.w = fmaf(v.w, w, acc.w);
-    }
-    reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] = acc;
-  }
+  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x)
+    reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] =
+        fold_o(a.o + base * a.dv, n, a.dv, d4, w_s);
 }
 
 // grid (rows): fold all `n` states of a row and normalise.
@@ -87,22 +123,15 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *
   __shared__ float M_s, L_s;
   const int row = blockIdx.x;
   const size_t base = (size_t)row * n;
+  pdl_wait();
+  pdl_launch_dependents();
   state_weights(m + base, l + base, n, w_s, &M_s, &L_s, a.status);
   const bool empty_row = (M_s == -CUDART_INF_F);
   if (empty_row && threadIdx.x == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   const float L = L_s;
   const int dv4 = a.dv / 4;
   for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float w = w_s[i];
-      if (w < 0.f) continue;
-      const float4 v = reinterpret_cast<const float4 *>(o + (base + i) * a.dv)[d4];
-      acc.x = fmaf(v.x, w, acc.x);
-      acc.y = fmaf(v.y, w, acc.y);
-      acc.z = fmaf(v.z, w, acc.z);
-      acc.w = fmaf(v.w, w, acc.w);
-    }
+    const float4 acc = fold_o(o + base * a.dv, n, a.dv, d4, w_s);
     float4 r;
     if (empty_row) {
       r = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -123,17 +152,16 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
   *launches = 0;
   if (a.count <= a.group) {  // one group: the second level reads the partials directly
-    pskv_merge_level2<<<a.rows, kMergeThreads, 0, s>>>(a.m, a.l, a.o, a.count, a);
     *launches = 1;
-    return cudaGetLastError();
+    return launch_pdl(pskv_merge_level2, dim3(a.rows), dim3(kMergeThreads), 0, s, a.m, a.l, a.o,
+                      a.count, a);
   }
   const int ng = (a.count + a.group - 1) / a.group;
-  pskv_merge_level1<<<dim3(ng, a.rows), kMergeThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(pskv_merge_level1, dim3(ng, a.rows), dim3(kMergeThreads), 0, s, a);
   if (e != cudaSuccess) return e;
-  pskv_merge_level2<<<a.rows, kMergeThreads, 0, s>>>(a.m1, a.l1, a.o1, ng, a);
   *launches = 2;
-  return cudaGetLastError();
+  return launch_pdl(pskv_merge_level2, dim3(a.rows), dim3(kMergeThreads), 0, s,
+                    (const float *)a.m1, (const float *)a.l1, (const float *)a.o1, ng, a);
 }
 
 }  // namespace pskv

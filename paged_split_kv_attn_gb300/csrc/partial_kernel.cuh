@@ -9,23 +9,30 @@
 // heads of the group).
 //
 // Structure (GB300):
-//  * warp 4 is the producer: per 16-key tile it reads the tile's page id from
-//    the table (32 ids per warp-wide load, so one table read serves up to 32
-//    pages; TensorFold #1619 measured a per-key page lookup at +5.8..7.9 % and
-//    moved it to once per tile) and issues one bulk async copy (cp.async.bulk)
-//    per valid key row into a ring of NSTAGE shared-memory stages, counted on
-//    the stage's "full" mbarrier;
-//  * warps 0..3 are consumers: warp w takes tiles w, w+4, w+8, ... of the
-//    partition, each keeping its own (m, l, o) in registers, and releases the
-//    stage on its "empty" mbarrier;
-//  * at the end the four warp states are merged in shared memory by the exact
+//  * the last warp is the producer: per 16-key tile it reads the tile's page id
+//    from the table (32 ids per warp-wide load, so one table read serves up to
+//    32 pages; TensorFold #1619 measured a per-key page lookup at +5.8..7.9 %
+//    and moved it to once per tile) and issues one bulk async copy
+//    (cp.async.bulk) per valid key row into a ring of shared-memory stages,
+//    counted on the stage's "full" mbarrier;
+//  * the other CW warps are consumers: warp w takes tiles w, w+CW, w+2CW, ...
+//    of the partition, each keeping its own (m, l, o) in registers, and
+//    releases the stage on its "empty" mbarrier.  Stage s always belongs to
+//    warp s % CW;
+//  * at the end the warp states are merged in shared memory by the exact
 //    rescaling identity and the partition's (m, l, o) is written to the
 //    workspace.
 // Rows of a tile past the row's length (or below the window bound) are never
 // copied; their scores are set to -inf by selection and their values masked
 // to zero, so stale shared memory can never reach the result.
-// Shared-memory rows are padded by 16 bytes, which makes the 8 row addresses
-// of every ldmatrix phase fall in distinct bank groups.
+//
+// Copy granularity: the bulk copy engine's per-copy cost dominates below
+// about 2 KB (1 KB copies streamed at ~4.6 TB/s on GB300, 2 KB copies at
+// ~7.1 TB/s), so key rows are copied in groups of R consecutive rows, one copy
+// per group.  In shared memory each group is followed by 16 bytes of padding:
+// with R = 2 and 1 KB rows, the 8 even keys of a tile start in 8 distinct
+// 16-byte bank groups, and so do the 8 odd keys, which the tensor-core
+// consumer exploits by ordering its MMA rows even keys first.
 #pragma once
 
 #include <math_constants.h>
@@ -34,49 +41,104 @@
 
 namespace pskv {
 
-template <int kRowBytes>
+#ifndef PSKV_STAGE_BUDGET
+#define PSKV_STAGE_BUDGET 100000  // shared-memory bytes given to the stage ring
+#endif
+
+// Ring of stages for `kWarps` consumer warps.  Warp w owns stages w, w + kWarps, ...
+// (the stage count is a multiple of kWarps), so every stage is always consumed
+// by the same warp, in order: a consumer never waits on a phase more than one
+// ahead of its barrier's current phase.  Rows are copied in groups of kRows.
+template <int kRowBytes, int kRows, int kWarps>
 struct RingGeom {
-  static constexpr int kRowStride = kRowBytes + 16;
-  static constexpr int kTileBytes = kKeyTile * kRowStride;
+  static constexpr int kRowsPerCopy = kRows;
+  static constexpr int kGroupStride = kRows * kRowBytes + 16;
+  static constexpr int kTileBytes = (kKeyTile / kRows) * kGroupStride;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-  static constexpr int kStages =
-      (200000 / kStageBytes) < 2 ? 2 : ((200000 / kStageBytes) > 8 ? 8 : (200000 / kStageBytes));
+  static constexpr int kPerWarpFit = PSKV_STAGE_BUDGET / (kWarps * kStageBytes);
+  static constexpr int kPerWarpMax = 8 / kWarps > 0 ? 8 / kWarps : 1;
+  static constexpr int kPerWarp =
+      kPerWarpFit < 1 ? 1 : (kPerWarpFit > kPerWarpMax ? kPerWarpMax : kPerWarpFit);
+  static constexpr int kStages = kWarps * kPerWarp;
   static constexpr int kRingBytes = kStages * kStageBytes;
+  // byte offset of key row t (0..15) of a tile
+  static __device__ __forceinline__ int row_off(int t) {
+    return (t / kRows) * kGroupStride + (t % kRows) * kRowBytes;
+  }
+  static_assert(kKeyTile % kRows == 0, "row groups must divide the tile");
 };
 
 // -------------------------------------------------------------------------------------------
 // Tensor-core consumer: bf16 K/V, 8 query heads per KV head.
-// Per tile, S^T[16 keys x 8 heads] = K[16 x D] Q^T[D x 8] (mma m16n8k16, keys as
-// M so no row is wasted), then O^T[D x 8] += V^T[D x 16] P^T[16 x 8], with P^T
-// obtained from the S^T accumulator by movmatrix.trans.  P is applied as a
-// bf16 hi+lo pair (p = hi + lo to ~2^-17 relative), so the weights keep
-// nearly fp32 accuracy while V stays bf16.
+// The four consumer warps work on every tile together, each on one quarter of
+// the head dimension (so each SM sub-partition's tensor unit takes a quarter
+// of the products; one warp alone issues mma.sync too slowly to keep up with
+// HBM):
+//  1. warp w forms the partial scores S_w^T[16 keys x 8 heads] = K[:, dw] Q^T[dw, :]
+//     over its d range dw (mma m16n8k16, keys as M so no row is wasted);
+//  2. the four partials are summed through shared memory in a fixed order,
+//     so every warp holds the same S^T and runs the same online-softmax update;
+//  3. warp w accumulates O^T[dw x 8] += V^T[dw x 16] P^T[16 x 8], with P^T
+//     obtained from the S^T accumulator by movmatrix.trans.  P is applied as a
+//     bf16 hi+lo pair (p = hi + lo to ~2^-17 relative), so the weights keep
+//     nearly fp32 accuracy while V stays bf16.
+// MMA row m holds key 2m (m < 8) or key 2(m-8)+1 (m >= 8): with rows stored in
+// padded pairs, each 8x8 ldmatrix phase then reads 8 distinct bank groups.
 // -------------------------------------------------------------------------------------------
+#ifndef PSKV_MMA_WARPS
+#define PSKV_MMA_WARPS 4
+#endif
+
+// bar.sync on a named barrier shared by the `n` threads of the consumer warps.
+__device__ __forceinline__ void consumers_sync(int n) {
+  asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
+
+// The same barrier with an AND vote: true iff `pred` holds in every consumer thread.
+__device__ __forceinline__ bool consumers_all(int n, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(n)
+      : "memory");
+  return out != 0;
+}
+
 template <int kD>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
   static constexpr int G = 8;
-  static constexpr int KS = D / 16;  // k-steps of the QK product = m-tiles of the PV product
-  static constexpr int kExtraSmem = 0;
-  using Geom = RingGeom<D * 2>;
-  static constexpr int RS = Geom::kRowStride;
+  static constexpr int kWarps = PSKV_MMA_WARPS;
+  static constexpr bool kCooperative = true;   // every warp takes part in every tile
+  static constexpr int DW = D / kWarps;        // head-dim columns per warp
+  static constexpr int KS = DW / 16;           // k-steps of QK = m-tiles of PV per warp
+  static constexpr int kExtraSmem = 2 * kWarps * 32 * 16;  // double-buffered score exchange
+  using Geom = RingGeom<D * 2, 2, 1>;
+  static constexpr int RB = D * 2;               // bytes of one key row
+  static constexpr int GS = Geom::kGroupStride;  // bytes of a padded pair of rows
+  static_assert(KS >= 2 && KS % 2 == 0, "two QK accumulator chains");
 
-  uint32_t qf[KS][2];  // Q^T B-fragments: (d = 16k + 2c + {0,1} [+8], head r)
-  float o[KS][4];      // O^T accumulators: (d = 16j + r [+8], heads 2c, 2c+1)
-  float m0, m1;        // running max (log2 units) of heads 2c, 2c+1; warp-uniform per head
+  uint32_t qf[KS][2];  // Q^T B-fragments: (d = dw0 + 16k + 2c + {0,1} [+8], head r)
+  float o[KS][4];      // O^T accumulators: (d = dw0 + 16j + r [+8], heads 2c, 2c+1)
+  float m0, m1;        // running max (log2 units) of heads 2c, 2c+1, the same in every warp
   float l0, l1;        // this lane's share of the running sums of heads 2c, 2c+1
   float scale_log2;
-  int r, c;
+  float4 *xchg;        // [2][kWarps][32] partial scores
+  int r, c, warp;
 
   static __device__ void prologue(const PartialArgs &, int, int, unsigned char *) {}
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, const unsigned char *) {
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra) {
     r = lane >> 2;
     c = lane & 3;
+    warp = threadIdx.x >> 5;
     scale_log2 = a.scale_log2;
+    xchg = reinterpret_cast<float4 *>(extra);
     const uint16_t *q =
-        static_cast<const uint16_t *>(a.q) + ((size_t)b * a.num_q_heads + h0 + r) * D;
+        static_cast<const uint16_t *>(a.q) + ((size_t)b * a.num_q_heads + h0 + r) * D + warp * DW;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
       qf[k][0] = *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c);
@@ -89,11 +151,13 @@ struct MmaConsumer {
   }
 
   __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
-                       bool skip, int lane) {
+                       bool skip, int lane, int j_tile) {
     const int mi = lane >> 3, rr = lane & 7;
-    // ---- scores: S^T = K Q^T, two accumulator chains for latency
+    // ---- partial scores over this warp's d range, two accumulator chains for latency
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t kaddr = smem_u32(ks) + ((mi & 1) * 8 + rr) * RS + (mi >> 1) * 16;
+    // A rows m = (mi&1)*8 + rr hold key 2*rr + (mi&1): pair rr, row (mi&1) of the pair
+    const uint32_t kaddr =
+        smem_u32(ks) + rr * GS + (mi & 1) * RB + (mi >> 1) * 16 + warp * DW * 2;
 #pragma unroll
     for (int k = 0; k < KS; k += 2) {
       uint32_t a0, a1, a2, a3;
@@ -102,13 +166,27 @@ struct MmaConsumer {
       ldsm_x4(kaddr + (k + 1) * 32, a0, a1, a2, a3);
       mma_bf16(sb, a0, a1, a2, a3, qf[k + 1][0], qf[k + 1][1]);
     }
-    const int tA = key0 + r, tB = key0 + r + 8;
+    // ---- sum the four warps' partials (fixed order: every warp gets the same bits)
+    float4 *slot = xchg + (j_tile & 1) * kWarps * 32;
+    slot[warp * 32 + lane] = make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
+    consumers_sync(kWarps * 32);
+    float4 st = slot[lane];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 x = slot[w * 32 + lane];
+      st.x += x.x;
+      st.y += x.y;
+      st.z += x.z;
+      st.w += x.w;
+    }
+
+    const int tA = key0 + 2 * r, tB = tA + 1;  // keys of MMA rows r and r + 8
     const bool vA = !skip && tA >= i0 && tA < len;
     const bool vB = !skip && tB >= i0 && tB < len;
-    const float s00 = vA ? (sa[0] + sb[0]) * scale_log2 : -CUDART_INF_F;  // key r, head 2c
-    const float s01 = vA ? (sa[1] + sb[1]) * scale_log2 : -CUDART_INF_F;  // key r, head 2c+1
-    const float s10 = vB ? (sa[2] + sb[2]) * scale_log2 : -CUDART_INF_F;  // key r+8, head 2c
-    const float s11 = vB ? (sa[3] + sb[3]) * scale_log2 : -CUDART_INF_F;  // key r+8, head 2c+1
+    const float s00 = vA ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, head 2c
+    const float s01 = vA ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, head 2c+1
+    const float s10 = vB ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, head 2c
+    const float s11 = vB ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, head 2c+1
 
     // ---- online softmax update (max over the 16 keys: lanes sharing c)
     float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
@@ -144,16 +222,19 @@ struct MmaConsumer {
     const uint32_t bh0 = movmatrix_t(hA), bh1 = movmatrix_t(hB);
     const uint32_t bl0 = movmatrix_t(lA), bl1 = movmatrix_t(lB);
 
-    // ---- O^T += V^T P^T; V rows of keys not attended are masked to zero
+    // ---- O^T += V^T P^T over this warp's d range; values of keys not attended masked to zero
     const bool full = !skip && key0 >= i0 && key0 + kKeyTile <= len;
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (!full) {
-      const int t0 = key0 + 2 * c, t1 = t0 + 8;
+      // B rows k = 2c, 2c+1 hold keys 4c, 4c+2; k = 2c+8, 2c+9 hold keys 4c+1, 4c+3
+      const int t0 = key0 + 4 * c;
       auto ok = [&](int t) { return !skip && t >= i0 && t < len; };
-      mlo = (ok(t0) ? 0x0000ffffu : 0u) | (ok(t0 + 1) ? 0xffff0000u : 0u);
-      mhi = (ok(t1) ? 0x0000ffffu : 0u) | (ok(t1 + 1) ? 0xffff0000u : 0u);
+      mlo = (ok(t0) ? 0x0000ffffu : 0u) | (ok(t0 + 2) ? 0xffff0000u : 0u);
+      mhi = (ok(t0 + 1) ? 0x0000ffffu : 0u) | (ok(t0 + 3) ? 0xffff0000u : 0u);
     }
-    const uint32_t vaddr = smem_u32(vs) + (rr + 8 * (mi >> 1)) * RS + (mi & 1) * 16;
+    // V^T A-fragment: source row k = rr + 8*(mi>>1) holds key 2*rr + (mi>>1)
+    const uint32_t vaddr =
+        smem_u32(vs) + rr * GS + (mi >> 1) * RB + (mi & 1) * 16 + warp * DW * 2;
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
       uint32_t a0, a1, a2, a3;
@@ -176,20 +257,23 @@ struct MmaConsumer {
     }
   }
 
-  // o_s: float[G][D] of this warp; m_s, l_s: float[G] of this warp.
-  __device__ void store(float *o_s, float *m_s, float *l_s) const {
+  // Write this partition's (m, l, o): every warp writes its d range; warp 0 the scalars.
+  __device__ void write_partial(const PartialArgs &a, size_t row0, int P) const {
+    const int d0 = warp * DW;
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
-      o_s[(2 * c) * D + 16 * j + r] = o[j][0];
-      o_s[(2 * c + 1) * D + 16 * j + r] = o[j][1];
-      o_s[(2 * c) * D + 16 * j + r + 8] = o[j][2];
-      o_s[(2 * c + 1) * D + 16 * j + r + 8] = o[j][3];
+      float *o_h0 = a.ws_o + (row0 + (size_t)(2 * c) * P) * D + d0 + 16 * j + r;
+      float *o_h1 = a.ws_o + (row0 + (size_t)(2 * c + 1) * P) * D + d0 + 16 * j + r;
+      o_h0[0] = o[j][0];
+      o_h1[0] = o[j][1];
+      o_h0[8] = o[j][2];
+      o_h1[8] = o[j][3];
     }
-    if (r == 0) {
-      m_s[2 * c] = m0;
-      m_s[2 * c + 1] = m1;
-      l_s[2 * c] = l0;
-      l_s[2 * c + 1] = l1;
+    if (warp == 0 && r == 0) {
+      a.ws_m[row0 + (size_t)(2 * c) * P] = m0 == -CUDART_INF_F ? -CUDART_INF_F : m0 * kLn2;
+      a.ws_m[row0 + (size_t)(2 * c + 1) * P] = m1 == -CUDART_INF_F ? -CUDART_INF_F : m1 * kLn2;
+      a.ws_l[row0 + (size_t)(2 * c) * P] = l0;
+      a.ws_l[row0 + (size_t)(2 * c + 1) * P] = l1;
     }
   }
 };
@@ -212,8 +296,10 @@ struct SimtConsumer {
   static constexpr int NC = E / VE;
   static constexpr bool kQInRegs = G * E <= 64;
   static constexpr int kExtraSmem = kQInRegs ? 0 : G * D * 4;
-  using Geom = RingGeom<D * (int)sizeof(T)>;
-  static constexpr int RS = Geom::kRowStride;
+  // four consumer warps, two when a stage is too big for four of them
+  static constexpr int kWarps = (D * (int)sizeof(T) > 1024) ? 2 : 4;
+  static constexpr bool kCooperative = false;  // warp w takes tiles w, w + kWarps, ...
+  using Geom = RingGeom<D * (int)sizeof(T), kKeyTile, kWarps>;  // one copy per tile
 
   float q[kQInRegs ? G : 1][kQInRegs ? E : 1];
   float o[G][E];
@@ -255,7 +341,7 @@ struct SimtConsumer {
     }
   }
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, const unsigned char *extra) {
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra) {
     lane_ = lane;
     scale_log2 = a.scale_log2;
     q_s = reinterpret_cast<const float *>(extra);
@@ -283,7 +369,7 @@ struct SimtConsumer {
   }
 
   __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
-                       bool skip, int lane) {
+                       bool skip, int lane, int) {
 #pragma unroll 1
     for (int t0 = 0; t0 < kKeyTile; t0 += 4) {
       float s[4][G];
@@ -298,7 +384,7 @@ struct SimtConsumer {
         for (int g = 0; g < G; ++g) s[u][g] = -CUDART_INF_F;
         if (valid[u]) {
           float kf[E];
-          load_row(reinterpret_cast<const T *>(ks + (t0 + u) * RS), lane, kf);
+          load_row(reinterpret_cast<const T *>(ks + Geom::row_off(t0 + u)), lane, kf);
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             float acc = 0.f;
@@ -339,7 +425,7 @@ struct SimtConsumer {
       for (int u = 0; u < 4; ++u) {
         if (!valid[u]) continue;
         float vf[E];
-        load_row(reinterpret_cast<const T *>(vs + (t0 + u) * RS), lane, vf);
+        load_row(reinterpret_cast<const T *>(vs + Geom::row_off(t0 + u)), lane, vf);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -377,23 +463,63 @@ struct PartialSmem {
   static constexpr int kBarOff = (kExtraOff + C::kExtraSmem + 15) / 16 * 16;
   static constexpr int kSkipOff = kBarOff + 2 * Geom::kStages * 8;
   static constexpr int kRedOff = kSkipOff + 4 * Geom::kStages;
-  static constexpr int kWeightOff = kRedOff + 2 * kConsumerWarps * C::G * 4;
-  static constexpr int kAbortOff = kWeightOff + kConsumerWarps * C::G * 4;
+  static constexpr int kWeightOff = kRedOff + 2 * C::kWarps * C::G * 4;
+  static constexpr int kAbortOff = kWeightOff + C::kWarps * C::G * 4;
   static constexpr int kBytes = kAbortOff + 16;
   // the warp states alias the ring once every stage has been consumed
-  static_assert(kConsumerWarps * C::G * C::D * 4 <= kRing, "merge area must fit in the ring");
+  static_assert(C::kCooperative || C::kWarps * C::G * C::D * 4 <= kRing,
+                "merge area must fit in the ring");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(C::kCooperative || Geom::kStages % C::kWarps == 0,
+                "stages must divide among the consumer warps");
 };
 
+// Merge the independent warps' states (the ring is free now) and write the partial.
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const PartialArgs a) {
+__device__ __forceinline__ void merge_warp_states(const C &cons, const PartialArgs &a,
+                                                  unsigned char *ring, float *red_m, float *red_l,
+                                                  float *weight, size_t row0, int P, int warp) {
+  constexpr int D = C::D, G = C::G, CW = C::kWarps, NT = (CW + 1) * 32;
+  float *o_s = reinterpret_cast<float *>(ring);  // [warps][G][D]
+  if (warp < CW) cons.store(o_s + (size_t)warp * G * D, red_m + warp * G, red_l + warp * G);
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = -CUDART_INF_F;
+    for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * G + h]);
+    float L = 0.f;
+    for (int w = 0; w < CW; ++w) {
+      const float mw = red_m[w * G + h];
+      const float wt = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+      weight[w * G + h] = wt;
+      L += wt * red_l[w * G + h];
+    }
+    a.ws_m[row0 + (size_t)h * P] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * kLn2;
+    a.ws_l[row0 + (size_t)h * P] = L;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += NT) {
+    const int h = idx / D, d = idx - h * D;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < CW; ++w) {
+      const float wt = weight[w * G + h];
+      if (wt != 0.f) acc = fmaf(o_s[(w * G + h) * D + d], wt, acc);
+    }
+    a.ws_o[(row0 + (size_t)h * P) * D + d] = acc;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(const PartialArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using Geom = typename C::Geom;
   using S = PartialSmem<C>;
   constexpr int D = C::D, G = C::G, NS = Geom::kStages;
   constexpr int RB = D * (int)sizeof(typename C::Elem);
-  constexpr int RS = Geom::kRowStride;
   constexpr int TB = Geom::kTileBytes;
+  constexpr int R = Geom::kRowsPerCopy;
+  constexpr int CW = C::kWarps;  // consumer warps; warp CW is the producer
 
   unsigned char *ring = smem;
   unsigned char *extra = smem + S::kExtraOff;
@@ -401,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
   uint64_t *empty_bar = full_bar + NS;
   int *stage_skip = reinterpret_cast<int *>(smem + S::kSkipOff);
   float *red_m = reinterpret_cast<float *>(smem + S::kRedOff);  // [warps][G] (log2 units)
-  float *red_l = red_m + kConsumerWarps * G;                       // [warps][G]
+  float *red_l = red_m + CW * G;                                   // [warps][G]
   float *weight = reinterpret_cast<float *>(smem + S::kWeightOff); // [warps][G]
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
 
@@ -434,6 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
 
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
+    pdl_wait();
+    pdl_launch_dependents();
     if (threadIdx.x < G) {
       a.ws_m[row0 + (size_t)threadIdx.x * P] = -CUDART_INF_F;
       a.ws_l[row0 + (size_t)threadIdx.x * P] = 0.f;
@@ -444,16 +572,19 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kCooperative ? CW : 1);  // released by every warp that reads it
     }
     *abort_flag = 0;
     mbar_fence_init();
   }
   C::prologue(a, b, h0, extra);
   __syncthreads();
+  // everything above overlaps the previous kernel; pools and workspace are touched only below
+  pdl_wait();
+  pdl_launch_dependents();
 
   C cons;
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ---------------- producer warp
     const int32_t *tbl = a.page_tables + (size_t)b * a.table_stride;
     const int n_slots = (len + a.page_size - 1) / a.page_size;  // table entries in use
@@ -491,14 +622,17 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
         mbar_arrive_expect_tx(&full_bar[s], ok ? (uint32_t)(2 * (r_hi - r_lo) * RB) : 0u);
       }
       __syncwarp();
-      if (ok && lane < r_hi - r_lo) {
-        const int rowi = r_lo + lane;
+      // one copy per group of R rows (clipped to the valid rows); lane i copies
+      // K group i, lane 16 + i V group i
+      const int grp = lane & 15;
+      const int g_lo = max(grp * R, r_lo), g_hi = min(grp * R + R, r_hi);
+      if (ok && grp < kKeyTile / R && g_lo < g_hi) {
         const size_t grow = ((size_t)page * a.num_kv_heads + g) * a.page_size +
-                            (size_t)(key0 % a.page_size) + rowi;
-        bulk_g2s(kdst + rowi * RS, static_cast<const unsigned char *>(a.k_pool) + grow * RB, RB,
-                 &full_bar[s]);
-        bulk_g2s(vdst + rowi * RS, static_cast<const unsigned char *>(a.v_pool) + grow * RB, RB,
-                 &full_bar[s]);
+                            (size_t)(key0 % a.page_size) + g_lo;
+        const unsigned char *src =
+            static_cast<const unsigned char *>(lane < 16 ? a.k_pool : a.v_pool) + grow * RB;
+        bulk_g2s((lane < 16 ? kdst : vdst) + Geom::row_off(g_lo), src,
+                 (uint32_t)((g_hi - g_lo) * RB), &full_bar[s]);
       }
       issued = j + 1;
     }
@@ -509,20 +643,27 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
     }
   } else {
     // ---------------- consumer warps
+    // cooperative consumers all take every tile; the others take every CW-th
     cons.init(a, b, h0, lane, extra);
-    for (int j = warp; j < n_my; j += kConsumerWarps) {
+    const int j0 = C::kCooperative ? 0 : warp, dj = C::kCooperative ? 1 : CW;
+    for (int j = j0; j < n_my; j += dj) {
       const int s = j % NS;
-      const bool landed = mbar_wait(&full_bar[s], (j / NS) & 1);
-      if (!__all_sync(0xffffffffu, landed)) {
+      const bool landed = mbar_wait(&full_bar[s], (j / NS) & 1) && !*abort_flag;
+      // one decision for every thread that will meet at the consumers' barrier
+      bool go;
+      if constexpr (C::kCooperative)
+        go = consumers_all(CW * 32, landed);
+      else
+        go = __all_sync(0xffffffffu, landed);
+      if (!go) {
         if (lane == 0) {
           raise_fault(a.status, PSKV_FAULT_WAIT_TIMEOUT);
           *abort_flag = 1;
         }
         break;
       }
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const unsigned char *kst = ring + s * Geom::kStageBytes;
-      cons.tile(kst, kst + TB, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane);
+      cons.tile(kst, kst + TB, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane, j);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -531,52 +672,44 @@ __global__ void __launch_bounds__(kThreads, 1) pskv_partial_kernel(const Partial
   __syncthreads();
   if (*abort_flag) return;
 
-  // ---- merge the four warp states (the ring is free now) and write the partial
-  float *o_s = reinterpret_cast<float *>(ring);  // [warps][G][D]
-  if (warp < kConsumerWarps) cons.store(o_s + (size_t)warp * G * D, red_m + warp * G, red_l + warp * G);
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
-    float M = -CUDART_INF_F;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
-    float L = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float mw = red_m[w * G + h];
-      const float wt = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
-      weight[w * G + h] = wt;
-      L += wt * red_l[w * G + h];
-    }
-    a.ws_m[row0 + (size_t)h * P] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * kLn2;
-    a.ws_l[row0 + (size_t)h * P] = L;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-    const int h = idx / D, d = idx - h * D;
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float wt = weight[w * G + h];
-      if (wt != 0.f) acc = fmaf(o_s[(w * G + h) * D + d], wt, acc);
-    }
-    a.ws_o[(row0 + (size_t)h * P) * D + d] = acc;
+  if constexpr (C::kCooperative) {
+    if (warp < CW) cons.write_partial(a, row0, P);
+    return;
+  } else {
+    merge_warp_states<C>(cons, a, ring, red_m, red_l, weight, row0, P, warp);
   }
 }
 
 template <class C>
-cudaError_t launch_partial_kernel(const PartialArgs &a, dim3 grid, cudaStream_t stream) {
+cudaError_t set_partial_smem_attr() {
   constexpr int bytes = PartialSmem<C>::kBytes;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(pskv_partial_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  pskv_partial_kernel<C><<<grid, kThreads, bytes, stream>>>(a);
-  return cudaGetLastError();
+  if (dev >= 0 && dev < 64 && attr_set[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(pskv_partial_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
+  return e;
+}
+
+template <class C>
+cudaError_t launch_partial_kernel(const PartialArgs &a, dim3 grid, cudaStream_t stream) {
+  cudaError_t e = set_partial_smem_attr<C>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(pskv_partial_kernel<C>, grid, dim3((C::kWarps + 1) * 32),
+                    PartialSmem<C>::kBytes, stream, a);
+}
+
+// CTAs of this kernel that fit on one SM at once.
+template <class C>
+cudaError_t partial_kernel_occupancy(int *ctas) {
+  cudaError_t e = set_partial_smem_attr<C>();
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, pskv_partial_kernel<C>,
+                                                       (C::kWarps + 1) * 32,
+                                                       PartialSmem<C>::kBytes);
 }
 
 }  // namespace pskv

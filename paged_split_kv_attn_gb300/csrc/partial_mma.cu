@@ -9,4 +9,10 @@ cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, dim3 grid, cu
   return cudaErrorInvalidValue;
 }
 
+cudaError_t occupancy_partial_mma(int head_dim, int *ctas) {
+  if (head_dim == 512) return partial_kernel_occupancy<MmaConsumer<512>>(ctas);
+  if (head_dim == 256) return partial_kernel_occupancy<MmaConsumer<256>>(ctas);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace pskv

@@ -3,25 +3,34 @@
 
 namespace pskv {
 
-template <int kD>
-static cudaError_t by_group(const PartialArgs &a, int group, dim3 grid, cudaStream_t s) {
+// Calls f.template operator()<Consumer>() for the consumer serving (kD, group).
+template <int kD, class F>
+static cudaError_t by_group(int group, F &&f) {
   switch (group) {
-    case 1: return launch_partial_kernel<SimtConsumer<float, kD, 1>>(a, grid, s);
-    case 2: return launch_partial_kernel<SimtConsumer<float, kD, 2>>(a, grid, s);
-    case 4: return launch_partial_kernel<SimtConsumer<float, kD, 4>>(a, grid, s);
-    case 8: return launch_partial_kernel<SimtConsumer<float, kD, 8>>(a, grid, s);
+    case 1: return f.template operator()<SimtConsumer<float, kD, 1>>();
+    case 2: return f.template operator()<SimtConsumer<float, kD, 2>>();
+    case 4: return f.template operator()<SimtConsumer<float, kD, 4>>();
+    case 8: return f.template operator()<SimtConsumer<float, kD, 8>>();
     default: break;
   }
   if constexpr (kD == 256) {
-    if (group == 16) return launch_partial_kernel<SimtConsumer<float, kD, 16>>(a, grid, s);
+    if (group == 16) return f.template operator()<SimtConsumer<float, kD, 16>>();
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                     cudaStream_t s) {
-  if (head_dim == 512) return by_group<512>(a, group, grid, s);
-  if (head_dim == 256) return by_group<256>(a, group, grid, s);
+  auto launch = [&]<class C>() { return launch_partial_kernel<C>(a, grid, s); };
+  if (head_dim == 512) return by_group<512>(group, launch);
+  if (head_dim == 256) return by_group<256>(group, launch);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas) {
+  auto query = [&]<class C>() { return partial_kernel_occupancy<C>(ctas); };
+  if (head_dim == 512) return by_group<512>(group, query);
+  if (head_dim == 256) return by_group<256>(group, query);
   return cudaErrorInvalidValue;
 }
 

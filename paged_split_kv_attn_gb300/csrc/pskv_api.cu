@@ -47,6 +47,26 @@ int sm_count(int *out) {
   return PSKV_OK;
 }
 
+// CTA slots of the partial kernel serving (dtype, head_dim, group): SMs x CTAs per SM.
+int partial_slots(int kv_dtype, int head_dim, int group, int *slots) {
+  int n_sm = 0, rc = sm_count(&n_sm);
+  if (rc) return rc;
+  const int kernel = pick_kernel(kv_dtype, head_dim, group);
+  int per = 0;
+  cudaError_t e;
+  if (kernel == kKernelMma)
+    e = occupancy_partial_mma(head_dim, &per);
+  else if (kernel == kKernelSimt && kv_dtype == PSKV_DTYPE_F32)
+    e = occupancy_partial_simt_f32(head_dim, group, &per);
+  else if (kernel == kKernelSimt)
+    e = occupancy_partial_simt_bf16(head_dim, group, &per);
+  else
+    return PSKV_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_fail(e);
+  *slots = n_sm * (per > 0 ? per : 1);
+  return PSKV_OK;
+}
+
 int merge_group_of(const pskv_decode_opts *opts, int *group) {
   int g = (opts && opts->merge_group) ? opts->merge_group : PSKV_MERGE_GROUP;
   if (g < 1 || g > PSKV_MERGE_GROUP) return PSKV_ERR_INVALID_ARG;
@@ -84,9 +104,9 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
 
   int P = num_splits;
   if (P == 0) {
-    int n_sm = 0;
-    if ((rc = sm_count(&n_sm))) return rc;
-    P = plan_splits(n_sm, batch, d.num_kv_heads, seq_lens_host);
+    int slots = 0;
+    if ((rc = partial_slots(d.kv_dtype, d.head_dim_k, group, &slots))) return rc;
+    P = plan_splits(slots, batch, d.num_kv_heads, seq_lens_host);
   }
   WorkspacePlan w;
   if ((rc = plan_workspace(batch, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
@@ -330,13 +350,16 @@ int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_
   return PSKV_OK;
 }
 
-int pskv_plan_splits(const pskv_layout *layout, int32_t batch, const int32_t *seq_lens_host,
-                     int32_t *num_splits) {
-  if (!layout || !seq_lens_host || !num_splits || batch < 1) return PSKV_ERR_INVALID_ARG;
-  int n_sm = 0;
-  const int rc = sm_count(&n_sm);
+int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_heads,
+                     const int32_t *seq_lens_host, int32_t *num_splits) {
+  if (!layout || !seq_lens_host || !num_splits || batch < 1 || num_q_heads < 1)
+    return PSKV_ERR_INVALID_ARG;
+  if (num_q_heads % layout->d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
+  int slots = 0;
+  const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_k,
+                               num_q_heads / layout->d.num_kv_heads, &slots);
   if (rc) return rc;
-  *num_splits = plan_splits(n_sm, batch, layout->d.num_kv_heads, seq_lens_host);
+  *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host);
   return PSKV_OK;
 }
 

@@ -10,13 +10,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pskv.h"
 
 namespace pskv {
 
 constexpr int kKeyTile = PSKV_KEY_TILE;  // keys per tile
-constexpr int kConsumerWarps = 4;        // warps that compute
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr uint32_t kWaitPolls = 1u << 22;            // try_wait polls before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -87,10 +87,43 @@ cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int grou
                                     cudaStream_t s);
 cudaError_t launch_partial_simt_bf16(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                      cudaStream_t s);
+cudaError_t occupancy_partial_mma(int head_dim, int *ctas);
+cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas);
+cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 
+// Launch `kernel` with programmatic dependent launch allowed: it may start
+// while the previous kernel on the stream is still running, and must execute
+// pdl_wait() before touching memory that kernel (or any earlier one) uses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 #ifdef __CUDACC__
+
+// Wait until the previous grid on the stream has completed and its writes are
+// visible (a no-op when the kernel was not launched with PDL).  Every kernel of
+// this library executes it before its first global access that could conflict
+// and before it exits, so stream order holds transitively across a chain.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -68,8 +68,8 @@ int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride
   return PSKV_OK;
 }
 
-int plan_splits(int n_sm, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host) {
-  if (n_sm < 1) n_sm = 1;
+int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host) {
+  if (slots < 1) slots = 1;
   int64_t total_tiles = 0, max_tiles = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t len = seq_lens_host[b] > 0 ? seq_lens_host[b] : 0;
@@ -78,10 +78,10 @@ int plan_splits(int n_sm, int32_t batch, int32_t num_kv_heads, const int32_t *se
     if (t > max_tiles) max_tiles = t;
   }
   if (max_tiles == 0) return 1;
-  // The longest row's pieces should carry about total_tiles * Hkv / n_sm tiles
+  // The longest row's pieces should carry about total_tiles * Hkv / slots tiles
   // each (one wave of CTAs when all rows are equal); for a batch, twice as
   // many pieces, so that short rows' CTAs fill the tail.
-  int64_t p = (max_tiles * (int64_t)n_sm) / (total_tiles * (int64_t)num_kv_heads);
+  int64_t p = (max_tiles * (int64_t)slots) / (total_tiles * (int64_t)num_kv_heads);
   if (batch > 1) p *= 2;
   if (p < 1) p = 1;
   if (p > max_tiles) p = max_tiles;

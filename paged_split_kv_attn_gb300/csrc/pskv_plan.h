@@ -35,8 +35,8 @@ int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64
 int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride,
                   const int32_t *seq_lens_host);
 
-// Automatic split count for `n_sm` SMs (one CTA per SM at a time).
-int plan_splits(int n_sm, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host);
+// Automatic split count for `slots` CTA slots (SMs x CTAs per SM).
+int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host);
 
 // Checks host copies of an append's rows against the leases.
 int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride, int32_t batch,

@@ -78,7 +78,7 @@ def test_append_past_pages_is_refused():
                              page_size=256)
     dc = DevCase(case)
     before_k, before_v = dc.k_pool.clone(), dc.v_pool.clone()
-    kn = torch.ones((2, 1, 512), dtype=torch.bfloat16, device="cuda")
+    kn = torch.full((2, 1, 512), 1000.0, dtype=torch.bfloat16, device="cuda")  # never drawn
     row_of, pos_of = [0, 1], [5, 256]   # row 1 holds one page: position 256 is past it
     with pytest.raises(pskv.PskvError) as e:   # host copies given: refused before launch
         pskv.kv_append_rows(dc.layout, kn, kn, i32(row_of), i32(pos_of), dc.tables,
@@ -124,7 +124,7 @@ def test_global_decode(context):
     case = W.global_case(context, seed=1)
     dc = DevCase(case)
     ref = ref_direct(case)
-    auto = pskv.pskv_plan_splits(dc.layout, case.seq_lens)
+    auto = pskv.pskv_plan_splits(dc.layout, 32, case.seq_lens)
     assert 1 <= auto <= pskv.PSKV_AUTO_MAX_SPLITS
     for splits in (0, 1, 8, 64, 256):
         check_decode(dc, ref, num_splits=splits)
