@@ -45,7 +45,7 @@ ROTATE = 3
 PARTIAL_SOURCES = ("paged_split_kv_attn_gb300/csrc/partial_kernel.cuh",
                    "paged_split_kv_attn_gb300/csrc/partial_mma.cu",
                    "paged_split_kv_attn_gb300/csrc/pskv_internal.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_mma_d512_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_mma_d512_ctx40002.md")
 
 
 def partial_kernel_hash() -> str:
@@ -68,14 +68,18 @@ def measured_peak():
 def recorded_traffic():
     """DRAM bytes per key of the partial kernel from the committed ncu summary,
     or None when the kernel source changed since the counters were taken."""
+    rec = {}
     try:
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
-    except Exception:
+            for line in f:
+                key, _, val = line.strip().partition(":")
+                if key in ("dram_bytes_per_key", "source_hash"):
+                    rec[key] = val.strip()
+    except OSError:
         return None
-    if t.get("source_hash") != partial_kernel_hash():
+    if rec.get("source_hash") != partial_kernel_hash() or "dram_bytes_per_key" not in rec:
         return None
-    return float(t["dram_bytes_per_key"])
+    return float(rec["dram_bytes_per_key"])
 
 
 # ---- distributed plumbing (replicas only: every rank runs the same step) ----------
