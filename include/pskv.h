@@ -235,6 +235,36 @@ int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_
 int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_heads,
                      const int32_t *seq_lens_host, int32_t *num_splits);
 
+/* Bytes of the scratch array that decode_attn_splitkv_static uses (16 MiB). */
+#define PSKV_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/* decode_attn_splitkv for callers that cannot allocate device memory.
+ * No passage of the source pages corresponds to this entry point: it exists
+ * for callers that have no way to obtain a workspace (code that must not call
+ * cudaMalloc, such as a host callback, a real-time or signal-safe path, or a
+ * plugin whose host framework owns every device allocation).
+ * It takes the arguments of decode_attn_splitkv except the workspace and the
+ * options, and uses instead a scratch array of PSKV_STATIC_SCRATCH_BYTES
+ * compiled into the library (held on every GPU that loads the library until
+ * the process exits).  It allocates nothing and frees nothing.
+ *   - num_splits = 0 picks the automatic plan, lowered to the largest split
+ *     count whose workspace (decode_attn_workspace_bytes) fits the array;
+ *     an explicit count whose workspace does not fit is refused with
+ *     PSKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture on the device.
+ *   - All calls share the array.  Calls that may run at the same time on the
+ *     GPU (other streams or host threads without ordering) overwrite each
+ *     other's partials: order them.  Nothing in the array needs clearing;
+ *     every call writes what it reads. */
+int decode_attn_splitkv_static(const pskv_layout *layout, const void *q,
+                               const int32_t *page_tables, int32_t table_stride,
+                               const int32_t *seq_lens_host, const int32_t *seq_lens,
+                               int32_t batch, int32_t num_q_heads, float scale,
+                               int32_t num_splits, void *out, int32_t out_dtype,
+                               pskv_stream_t stream);
+
 /* Static text for a status code. */
 const char *pskv_strerror(int status);
 

@@ -39,13 +39,14 @@ PSKV_MAX_SPLITS = 1024
 PSKV_AUTO_MAX_SPLITS = 256
 PSKV_MERGE_GROUP = 16
 PSKV_KEY_TILE = 16
+PSKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 # Every function the header declares, in the header's order.
 EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows",
            "decode_attn_splitkv", "decode_attn_windowed", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
-           "pskv_partial_scratch_bytes", "pskv_plan_splits", "pskv_strerror",
-           "pskv_last_cuda_error", "pskv_kernel_launches", "pskv_version")
+           "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
+           "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches", "pskv_version")
 
 
 class PskvError(RuntimeError):
@@ -97,6 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.merge_partials_workspace_bytes.argtypes = [I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pskv_partial_scratch_bytes.argtypes = [I64, I64, I64, I64] + [ctypes.POINTER(SZ)] * 4
     lib.pskv_plan_splits.argtypes = [P, I32, I32, P, ctypes.POINTER(I32)]
+    lib.decode_attn_splitkv_static.argtypes = [P, P, P, I32, P, P, I32, I32, F, I32, P, I32, P]
     lib.pskv_strerror.argtypes = [ctypes.c_int]
     lib.pskv_strerror.restype = ctypes.c_char_p
     lib.pskv_last_cuda_error.argtypes = []
@@ -341,6 +343,29 @@ def decode_attn_windowed(layout: Layout, q, page_tables, seq_lens, seq_lens_host
     """Windowed split-KV decode; keys at positions below ``window_lo`` are masked."""
     return _decode(True, layout, q, page_tables, seq_lens, seq_lens_host, scale, num_splits,
                    workspace, out, out_dtype, merge_group, events, stream, first_pos, window_lo)
+
+
+def decode_attn_splitkv_static(layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,
+                               num_splits: int = 0, out=None, out_dtype=None,
+                               stream=None) -> torch.Tensor:
+    """Split-KV decode using the library's built-in scratch array instead of a
+    workspace, for callers that cannot allocate device memory (see pskv.h)."""
+    lib = load_library()
+    if q.dim() != 3:
+        raise ValueError("q must be [batch, num_q_heads, head_dim]")
+    batch, hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((batch, hq, layout.desc.head_dim_v), device=q.device,
+                          dtype=out_dtype or torch.bfloat16)
+    lens_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if len(lens_h) != batch:
+        raise ValueError("seq_lens_host must have one entry per row")
+    _check(lib.decode_attn_splitkv_static(
+        layout.handle, _dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
+        page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32), batch, hq,
+        float(scale), num_splits, _dev(out, "out"), _dtype_code(out.dtype), _stream(stream)),
+        "decode_attn_splitkv_static")
+    return out
 
 
 def merge_partials(m, l, o, out=None, out_dtype=None, workspace=None, status=None,
