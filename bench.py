@@ -13,8 +13,13 @@ value = algorithmic bytes (K and V of every attended key) / step time, GB/s.
 
 Timing: W untimed warm-up steps, then K steps between CUDA events on the
 launching stream, with a barrier and a device synchronize on both sides;
-every step reads three rotating copies of the pools (433 MB of K/V a step,
-> 3x the 129 MB L2), so no call finds its data in L2.
+consecutive steps read three rotating copies of the pools (433 MB of K/V a
+step, > 3x the 129 MB L2), so no call finds its data in L2.  The timed steps
+are replays of CUDA graphs captured once (one per pool copy) from the same
+library calls, as a decode engine runs its step; the eager (stream-launched)
+time of the same K steps is reported beside it.  The partial kernels'
+durations for the roofline come from a further pass of K eager steps with
+CUDA events recorded around each partial launch.
 
 --impl reference times the CPU oracle (the only reference there is: the
 pages ship no runnable code) on the same workload; see the design doc.
@@ -85,16 +90,22 @@ def recorded_traffic():
 # ---- distributed plumbing (replicas only: every rank runs the same step) ----------
 
 class Dist:
-    def __init__(self):
+    """Rank bookkeeping for `--gpus N` under torchrun: N independent replicas of
+    the step, a barrier around the timed region and the max time over ranks.
+    NCCL on GPUs; gloo when `backend="gloo"` (the CPU tests use it)."""
+
+    def __init__(self, backend: str | None = None):
         import torch
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.backend = backend or "nccl"
         if self.world > 1:
             import torch.distributed as dist
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl")
+            if self.backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(self.backend)
             self.pg = dist
 
     def barrier(self):
@@ -105,13 +116,20 @@ class Dist:
         if self.pg is None:
             return x
         import torch
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if self.backend == "nccl" else "cpu")
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
     def close(self):
         if self.pg is not None:
             self.pg.destroy_process_group()
+
+
+def whole_job_gbps(step_bytes: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed per step over the
+    slowest rank's step time (every rank runs the same step)."""
+    return step_bytes * world / (ms_per_step_max * 1e-3) / 1e9
 
 
 # ---- clocks --------------------------------------------------------------------
@@ -292,8 +310,8 @@ def parse():
     ap.add_argument("--no-window", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--graph", action="store_true",
-                    help="also time the step captured in a CUDA graph")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager stream launches instead of CUDA graph replays")
     ap.add_argument("--sweep", type=int, nargs="*", default=None,
                     help="also time each global context alone at these split counts")
     return ap.parse_args()
@@ -382,27 +400,66 @@ def main():
         if c.status[0].item() != 0:
             raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
 
+    # ---- the step as CUDA graphs: one graph per pool copy, captured once
+    graphs = None
+    if not args.eager:
+        graphs = []
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for c in calls:  # warm the capture path (plans, attributes) outside capture
+                c.run(0)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        n0 = pskv.pskv_kernel_launches()
+        for r in range(ROTATE):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for c in calls:
+                    c.run(r)
+            graphs.append(g)
+        launches_per_step = (pskv.pskv_kernel_launches() - n0) / ROTATE
+        for r in range(ROTATE):
+            graphs[r].replay()
+        torch.cuda.synchronize()
+
+    def timed(run_step):
+        """K steps between events on the stream, barrier and synchronize on both sides."""
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for it in range(args.steps):
+            run_step(it)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        return dist.max(t0.elapsed_time(t1) / args.steps)
+
+    def eager_step(it):
+        for c in calls:
+            c.run(it)
+
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
-    dist.barrier()
-    torch.cuda.synchronize()
     launches0 = pskv.pskv_kernel_launches()
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_begin.record(stream)
+    if graphs is not None:
+        ms = timed(lambda it: graphs[it % ROTATE].replay())
+        launches = int(round(launches_per_step * args.steps))
+    else:
+        ms = timed(eager_step)
+        launches = pskv.pskv_kernel_launches() - launches0
+    clock_info = clocks.stop()
+    value = whole_job_gbps(step_bytes, dist.world, ms)
+    eager_ms = ms if graphs is None else timed(eager_step)
+
+    # ---- the partial kernels' durations: a second pass of K eager steps with CUDA
+    # events recorded by the library right around each partial launch
     for it in range(args.steps):
         for c in calls:
             c.run(it, events=ev[c.name][it])
-    t_end.record(stream)
     torch.cuda.synchronize()
-    dist.barrier()
-    launches = pskv.pskv_kernel_launches() - launches0
-    clock_info = clocks.stop()
-    ms = t_begin.elapsed_time(t_end) / args.steps
-    ms = dist.max(ms)
-    value = step_bytes * dist.world / (ms * 1e-3) / 1e9
-
     per_call = {}
     for c in calls:
         part = [b.elapsed_time(e) for b, e in ev[c.name]]
@@ -452,34 +509,6 @@ def main():
             c.ws = pskv.workspace(1, 32, 512, args.splits, dev)
     del flush
 
-    # the same step captured once in a CUDA graph and replayed (launch cost amortised)
-    graph_ms = None
-    if args.graph:
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            for it in range(ROTATE):
-                for c in calls:
-                    c.run(it)
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g):
-            for it in range(ROTATE):
-                for c in calls:
-                    c.run(it)
-        for _ in range(2):
-            g.replay()
-        torch.cuda.synchronize()
-        reps = max(1, args.steps // ROTATE)
-        gb, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        gb.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ge.record(stream)
-        torch.cuda.synchronize()
-        graph_ms = gb.elapsed_time(ge) / (reps * ROTATE)
-
     # end-to-end through the public calls from pinned host buffers
     for it in range(args.warmup):
         for c in calls:
@@ -517,18 +546,17 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config_dict(args), "roofline": roofline,
-            "e2e": {"value": step_bytes * dist.world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": whole_job_gbps(step_bytes, dist.world, e2e_ms), "unit": "GB/s",
                     "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": sum(c.h2d_bytes() for c in calls),
                     "d2h_bytes_per_step": sum(c.d2h_bytes() for c in calls)},
             "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
     if sweep is not None:
         line["split_sweep_us"] = sweep
-    if graph_ms is not None:
-        line["graph"] = {"ms_per_step": graph_ms,
-                         "value": step_bytes * dist.world / (graph_ms * 1e-3) / 1e9,
-                         "unit": "GB/s",
-                         "note": "the same step captured once in a CUDA graph and replayed"}
+    line["step_launch"] = ("CUDA graph replay (one graph per pool copy, captured once)"
+                           if graphs is not None else "eager stream launches")
+    line["eager"] = {"ms_per_step": eager_ms, "unit": "GB/s",
+                     "value": whole_job_gbps(step_bytes, dist.world, eager_ms)}
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline([c.case for c in calls], args.cpu_seconds)
     if dist.rank == 0:
