@@ -13,6 +13,9 @@ namespace pskv {
 
 constexpr int kAppendWarps = 4;
 
+// Longest row handled: 2048 bytes (head dim 512 in f32) = 4 vectors of 16 bytes per lane.
+constexpr int kMaxVecsPerLane = 4;
+
 __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const AppendArgs a) {
   const long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -20,33 +23,48 @@ __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const Appe
   pdl_launch_dependents();
   if (item >= (long long)a.n * a.num_kv_heads) return;
   const int r = (int)(item / a.num_kv_heads), h = (int)(item % a.num_kv_heads);
+  const size_t src_row = (size_t)r * a.num_kv_heads + h;
+  const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.k_new) +
+                                                    src_row * a.row_bytes);
+  const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.v_new) +
+                                                    src_row * a.row_bytes);
+  const int vecs = a.row_bytes / 16;
+  // the row's bytes and its indices are independent: load them all before any check
+  uint4 kb[kMaxVecsPerLane], vb[kMaxVecsPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxVecsPerLane; ++i) {
+    const int v = lane + 32 * i;
+    if (v < vecs) {
+      kb[i] = ks[v];
+      vb[i] = vs[v];
+    }
+  }
   const int b = a.row_of[r], pos = a.pos_of[r];
   if (b < 0 || b >= a.batch || pos < 0) {
     if (lane == 0 && h == 0) raise_fault(a.status, PSKV_FAULT_PAST_PAGES);
     return;
   }
   const int lease = a.pages_of_row[b];
+  const long long slot = pos / a.page_size;
+  const int page = slot < a.table_stride ? a.page_tables[(size_t)b * a.table_stride + slot] : -1;
   if (lease < 0 || lease > a.table_stride || (long long)pos >= (long long)lease * a.page_size) {
     if (lane == 0 && h == 0) raise_fault(a.status, PSKV_FAULT_PAST_PAGES);
     return;
   }
-  const int page = a.page_tables[(size_t)b * a.table_stride + pos / a.page_size];
   if (page < 0 || (long long)page >= a.num_pages) {
     if (lane == 0 && h == 0) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
     return;
   }
   const size_t dst_row = ((size_t)page * a.num_kv_heads + h) * a.page_size + pos % a.page_size;
-  const size_t src_row = (size_t)r * a.num_kv_heads + h;
-  const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.k_new) +
-                                                    src_row * a.row_bytes);
-  const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.v_new) +
-                                                    src_row * a.row_bytes);
   uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(a.k_pool) + dst_row * a.row_bytes);
   uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(a.v_pool) + dst_row * a.row_bytes);
-  const int vecs = a.row_bytes / 16;
-  for (int i = lane; i < vecs; i += 32) {
-    kd[i] = ks[i];
-    vd[i] = vs[i];
+#pragma unroll
+  for (int i = 0; i < kMaxVecsPerLane; ++i) {
+    const int v = lane + 32 * i;
+    if (v < vecs) {
+      kd[v] = kb[i];
+      vd[v] = vb[i];
+    }
   }
 }
 

@@ -25,6 +25,7 @@ constexpr int kChunk = 16;      // states whose o is loaded together (all loads 
 
 // Warp 0 reads the n states' (m, l) in parallel and computes the weights
 // w_i = e^(m_i - M) (-1 marks an empty state, whose o is skipped), M and l.
+template <bool kCoherent = false>
 __device__ void state_weights(const float *m, const float *l, int n, float *w_s, float *M_s,
                               float *L_s, int32_t *status) {
   if (threadIdx.x < 32) {
@@ -35,8 +36,8 @@ __device__ void state_weights(const float *m, const float *l, int n, float *w_s,
 #pragma unroll
     for (int k = 0; k < kMaxStates / 32; ++k) {
       const int i = lane + 32 * k;
-      mi[k] = i < n ? m[i] : -CUDART_INF_F;
-      li[k] = i < n ? l[i] : 0.f;
+      mi[k] = i < n ? (kCoherent ? __ldcg(m + i) : m[i]) : -CUDART_INF_F;
+      li[k] = i < n ? (kCoherent ? __ldcg(l + i) : l[i]) : 0.f;
       if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
         bad = true;
         mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
@@ -68,14 +69,18 @@ __device__ void state_weights(const float *m, const float *l, int n, float *w_s,
 
 // acc += sum_i w_i o_i[d4] over states [0, n) of `o` (row stride dv floats),
 // kChunk loads in flight at a time; empty states are skipped by selection.
+// kCoherent loads through L2 only (for data other CTAs of this grid just wrote).
+template <bool kCoherent = false>
 __device__ __forceinline__ float4 fold_o(const float *o, int n, int dv, int d4, const float *w_s) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i0 = 0; i0 < n; i0 += kChunk) {
     float4 v[kChunk];
 #pragma unroll
     for (int k = 0; k < kChunk; ++k)
-      if (i0 + k < n && w_s[i0 + k] >= 0.f)
-        v[k] = __ldg(reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4);
+      if (i0 + k < n && w_s[i0 + k] >= 0.f) {
+        const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4;
+        v[k] = kCoherent ? __ldcg(src) : __ldg(src);
+      }
 #pragma unroll
     for (int k = 0; k < kChunk; ++k) {
       if (i0 + k < n) {
@@ -115,23 +120,18 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level1(const MergeAr
         fold_o(a.o + base * a.dv, n, a.dv, d4, w_s);
 }
 
-// grid (rows): fold all `n` states of a row and normalise.
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *m, const float *l,
-                                                                   const float *o, int n,
-                                                                   const MergeArgs a) {
-  __shared__ float w_s[kMaxStates];
-  __shared__ float M_s, L_s;
-  const int row = blockIdx.x;
+// Fold all `n` states of `row` and write the normalised output row.
+template <bool kCoherent>
+__device__ void fold_and_finalize(const float *m, const float *l, const float *o, int n, int row,
+                                  const MergeArgs &a, float *w_s, float &M_s, float &L_s) {
   const size_t base = (size_t)row * n;
-  pdl_wait();
-  pdl_launch_dependents();
-  state_weights(m + base, l + base, n, w_s, &M_s, &L_s, a.status);
+  state_weights<kCoherent>(m + base, l + base, n, w_s, &M_s, &L_s, a.status);
   const bool empty_row = (M_s == -CUDART_INF_F);
   if (empty_row && threadIdx.x == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   const float L = L_s;
   const int dv4 = a.dv / 4;
   for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
-    const float4 acc = fold_o(o + base * a.dv, n, a.dv, d4, w_s);
+    const float4 acc = fold_o<kCoherent>(o + base * a.dv, n, a.dv, d4, w_s);
     float4 r;
     if (empty_row) {
       r = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -149,6 +149,53 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *
   }
 }
 
+// grid (rows): fold all `n` states of a row and normalise.
+__global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *m, const float *l,
+                                                                   const float *o, int n,
+                                                                   const MergeArgs a) {
+  __shared__ float w_s[kMaxStates];
+  __shared__ float M_s, L_s;
+  pdl_wait();
+  pdl_launch_dependents();
+  fold_and_finalize<false>(m, l, o, n, blockIdx.x, a, w_s, M_s, L_s);
+}
+
+// Both levels in one launch, grid (groups, rows): each block folds one group
+// of partials (level 1) into the group buffer; the block that finishes a row's
+// last group (counted on a per-row counter that the partial kernel zeroed)
+// folds that row's group results (level 2).  The level-2 fold reads the group
+// buffer in index order, so which block finishes last does not change a bit.
+__global__ void __launch_bounds__(kMergeThreads) pskv_merge_two_level(const MergeArgs a) {
+  __shared__ float w_s[kMaxStates];
+  __shared__ float M_s, L_s;
+  __shared__ bool last_s;
+  const int grp = blockIdx.x, row = blockIdx.y;
+  const int ng = (a.count + a.group - 1) / a.group;
+  const int p0 = grp * a.group;
+  const int n = min(a.count - p0, a.group);
+  const size_t base = (size_t)row * a.count + p0;
+  pdl_wait();
+  pdl_launch_dependents();
+  state_weights(a.m + base, a.l + base, n, w_s, &M_s, &L_s, a.status);
+  const size_t out_state = (size_t)row * ng + grp;
+  if (threadIdx.x == 0) {
+    a.m1[out_state] = M_s;
+    a.l1[out_state] = L_s;
+  }
+  const int dv4 = a.dv / 4;
+  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x)
+    reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] =
+        fold_o(a.o + base * a.dv, n, a.dv, d4, w_s);
+  // publish this group's result, then count it
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_s = atomicAdd(a.counters + row, 1u) == (unsigned)(ng - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  fold_and_finalize<true>(a.m1, a.l1, a.o1, ng, row, a, w_s, M_s, L_s);
+}
+
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
   *launches = 0;
   if (a.count <= a.group) {  // one group: the second level reads the partials directly
@@ -157,6 +204,10 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
                       a.count, a);
   }
   const int ng = (a.count + a.group - 1) / a.group;
+  if (a.counters != nullptr) {  // both levels in one launch
+    *launches = 1;
+    return launch_pdl(pskv_merge_two_level, dim3(ng, a.rows), dim3(kMergeThreads), 0, s, a);
+  }
   cudaError_t e = launch_pdl(pskv_merge_level1, dim3(ng, a.rows), dim3(kMergeThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   *launches = 2;

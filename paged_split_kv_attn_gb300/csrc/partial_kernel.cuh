@@ -559,9 +559,14 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   const int n_my = (int)(hi_ll - lo_ll);
 
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0
+  // the merge that follows counts finished groups per (row, head): start it at zero
+  const bool zero_counters = a.merge_counters != nullptr && p == 0 && g == 0;
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
     pdl_wait();
     pdl_launch_dependents();
+    if (zero_counters)
+      for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
+        a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
     if (threadIdx.x < G) {
       a.ws_m[row0 + (size_t)threadIdx.x * P] = -CUDART_INF_F;
       a.ws_l[row0 + (size_t)threadIdx.x * P] = 0.f;
@@ -582,6 +587,9 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   // everything above overlaps the previous kernel; pools and workspace are touched only below
   pdl_wait();
   pdl_launch_dependents();
+  if (zero_counters)
+    for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
+      a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
 
   C cons;
   if (warp == CW) {

@@ -126,6 +126,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.ws_m = reinterpret_cast<float *>(ws + w.m_off);
   a.ws_l = reinterpret_cast<float *>(ws + w.l_off);
   a.ws_o = reinterpret_cast<float *>(ws + w.o_off);
+  a.merge_counters = reinterpret_cast<unsigned int *>(ws + w.cnt_off);
   a.num_pages = d.num_pages;
   a.table_stride = table_stride;
   a.page_size = d.page_size;
@@ -168,6 +169,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   m.out = out;
   m.out_dtype = out_dtype;
   m.status = d.status;
+  m.counters = a.merge_counters;
   int launched = 0;
   e = launch_merge(m, s, &launched);
   g_launches.fetch_add((uint64_t)launched, std::memory_order_relaxed);
@@ -275,7 +277,7 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
   WorkspacePlan w;
   if ((rc = plan_workspace(1, rows, head_dim_v, num_splits, group, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
-  const size_t need = w.total - w.m1_off;  // only the level-1 sections are used
+  const size_t need = w.cnt_off - w.m1_off;  // only the level-1 sections are used
   if (w.groups > 1 && (!workspace || workspace_bytes < need)) return PSKV_ERR_WORKSPACE_TOO_SMALL;
   if (workspace && !aligned(workspace, 16)) return PSKV_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
@@ -293,6 +295,7 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
   a.out = out;
   a.out_dtype = out_dtype;
   a.status = status;
+  a.counters = nullptr;  // level 1 and level 2 as two launches
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (opts && opts->partial_begin) {
@@ -327,7 +330,7 @@ int merge_partials_workspace_bytes(int32_t rows, int32_t num_splits, int32_t hea
   WorkspacePlan w;
   const int rc = plan_workspace(1, rows, head_dim_v, num_splits, PSKV_MERGE_GROUP, &w);
   if (rc) return rc;
-  *bytes = w.total - w.m1_off;
+  *bytes = w.cnt_off - w.m1_off;
   return PSKV_OK;
 }
 

@@ -53,7 +53,8 @@ int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64
   w.m1_off = align256(w.o_off + ostate);
   w.l1_off = align256(w.m1_off + states1);
   w.o1_off = align256(w.l1_off + states1);
-  w.total = align256(w.o1_off + ostate1);
+  w.cnt_off = align256(w.o1_off + ostate1);
+  w.total = align256(w.cnt_off + rows * 4);
   w.groups = (int)ng;
   *out = w;
   return PSKV_OK;

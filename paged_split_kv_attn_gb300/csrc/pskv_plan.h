@@ -21,6 +21,7 @@ namespace pskv {
 struct WorkspacePlan {
   size_t m_off, l_off, o_off;     // partials: m, l [rows][P], o [rows][P][dv]
   size_t m1_off, l1_off, o1_off;  // level-1 group results: [rows][ng], [rows][ng][dv]
+  size_t cnt_off;                 // per-row counters of finished level-1 groups: uint32 [rows]
   size_t total;
   int groups;  // ng = ceil(P / group)
 };
