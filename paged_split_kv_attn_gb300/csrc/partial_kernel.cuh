@@ -106,11 +106,14 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
   return out != 0;
 }
 
-template <int kD>
+// G < 8 query heads per KV head run on the same 8-column products with the
+// unused columns' queries set to zero (their results are never written).
+template <int kD, int kG = 8>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
-  static constexpr int G = 8;
+  static constexpr int G = kG;
+  static_assert(kG == 1 || kG == 2 || kG == 4 || kG == 8, "query heads per KV head");
   static constexpr int kWarps = PSKV_MMA_WARPS;
   static constexpr bool kCooperative = true;   // every warp takes part in every tile
   static constexpr int DW = D / kWarps;        // head-dim columns per warp
@@ -137,12 +140,12 @@ struct MmaConsumer {
     warp = threadIdx.x >> 5;
     scale_log2 = a.scale_log2;
     xchg = reinterpret_cast<float4 *>(extra);
-    const uint16_t *q =
-        static_cast<const uint16_t *>(a.q) + ((size_t)b * a.num_q_heads + h0 + r) * D + warp * DW;
+    const uint16_t *q = static_cast<const uint16_t *>(a.q) +
+                        ((size_t)b * a.num_q_heads + h0 + (r < G ? r : 0)) * D + warp * DW;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      qf[k][0] = *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c);
-      qf[k][1] = *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c);
+      qf[k][0] = r < G ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
+      qf[k][1] = r < G ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -260,20 +263,29 @@ struct MmaConsumer {
   // Write this partition's (m, l, o): every warp writes its d range; warp 0 the scalars.
   __device__ void write_partial(const PartialArgs &a, size_t row0, int P) const {
     const int d0 = warp * DW;
+    const bool h0_real = 2 * c < G, h1_real = 2 * c + 1 < G;  // columns holding real heads
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
       float *o_h0 = a.ws_o + (row0 + (size_t)(2 * c) * P) * D + d0 + 16 * j + r;
       float *o_h1 = a.ws_o + (row0 + (size_t)(2 * c + 1) * P) * D + d0 + 16 * j + r;
-      o_h0[0] = o[j][0];
-      o_h1[0] = o[j][1];
-      o_h0[8] = o[j][2];
-      o_h1[8] = o[j][3];
+      if (h0_real) {
+        o_h0[0] = o[j][0];
+        o_h0[8] = o[j][2];
+      }
+      if (h1_real) {
+        o_h1[0] = o[j][1];
+        o_h1[8] = o[j][3];
+      }
     }
     if (warp == 0 && r == 0) {
-      a.ws_m[row0 + (size_t)(2 * c) * P] = m0 == -CUDART_INF_F ? -CUDART_INF_F : m0 * kLn2;
-      a.ws_m[row0 + (size_t)(2 * c + 1) * P] = m1 == -CUDART_INF_F ? -CUDART_INF_F : m1 * kLn2;
-      a.ws_l[row0 + (size_t)(2 * c) * P] = l0;
-      a.ws_l[row0 + (size_t)(2 * c + 1) * P] = l1;
+      if (h0_real) {
+        a.ws_m[row0 + (size_t)(2 * c) * P] = m0 == -CUDART_INF_F ? -CUDART_INF_F : m0 * kLn2;
+        a.ws_l[row0 + (size_t)(2 * c) * P] = l0;
+      }
+      if (h1_real) {
+        a.ws_m[row0 + (size_t)(2 * c + 1) * P] = m1 == -CUDART_INF_F ? -CUDART_INF_F : m1 * kLn2;
+        a.ws_l[row0 + (size_t)(2 * c + 1) * P] = l1;
+      }
     }
   }
 };
@@ -536,6 +548,20 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   const int P = a.num_splits;
   const int h0 = g * G;
 
+  // Only set-up that touches no global memory overlaps the previous kernel;
+  // every read of caller memory (lengths, window bounds, tables, queries,
+  // pools) and every write comes after pdl_wait().
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kCooperative ? CW : 1);  // released by every warp that reads it
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+
   // ---- this partition's tiles
   const long long cap = (long long)a.table_stride * a.page_size;
   long long len_ll = a.seq_lens[b];
@@ -560,36 +586,18 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
 
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0
   // the merge that follows counts finished groups per (row, head): start it at zero
-  const bool zero_counters = a.merge_counters != nullptr && p == 0 && g == 0;
+  if (a.merge_counters != nullptr && p == 0 && g == 0)
+    for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
+      a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
-    pdl_wait();
-    pdl_launch_dependents();
-    if (zero_counters)
-      for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
-        a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
     if (threadIdx.x < G) {
       a.ws_m[row0 + (size_t)threadIdx.x * P] = -CUDART_INF_F;
       a.ws_l[row0 + (size_t)threadIdx.x * P] = 0.f;
     }
     return;
   }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], C::kCooperative ? CW : 1);  // released by every warp that reads it
-    }
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
   C::prologue(a, b, h0, extra);
   __syncthreads();
-  // everything above overlaps the previous kernel; pools and workspace are touched only below
-  pdl_wait();
-  pdl_launch_dependents();
-  if (zero_counters)
-    for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
-      a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
 
   C cons;
   if (warp == CW) {

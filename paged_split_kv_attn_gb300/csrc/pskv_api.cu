@@ -55,7 +55,7 @@ int partial_slots(int kv_dtype, int head_dim, int group, int *slots) {
   int per = 0;
   cudaError_t e;
   if (kernel == kKernelMma)
-    e = occupancy_partial_mma(head_dim, &per);
+    e = occupancy_partial_mma(head_dim, group, &per);
   else if (kernel == kKernelSimt && kv_dtype == PSKV_DTYPE_F32)
     e = occupancy_partial_simt_f32(head_dim, group, &per);
   else if (kernel == kKernelSimt)
@@ -143,7 +143,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (kernel == kKernelMma)
-    e = launch_partial_mma(a, d.head_dim_k, grid, s);
+    e = launch_partial_mma(a, d.head_dim_k, group, grid, s);
   else if (d.kv_dtype == PSKV_DTYPE_F32)
     e = launch_partial_simt_f32(a, d.head_dim_k, group, grid, s);
   else

@@ -84,12 +84,13 @@ struct AppendArgs {
 };
 
 // Host-side launchers (one per kernel family).  They return a CUDA error code.
-cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, dim3 grid, cudaStream_t s);
+cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, dim3 grid,
+                               cudaStream_t s);
 cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                     cudaStream_t s);
 cudaError_t launch_partial_simt_bf16(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                      cudaStream_t s);
-cudaError_t occupancy_partial_mma(int head_dim, int *ctas);
+cudaError_t occupancy_partial_mma(int head_dim, int group, int *ctas);
 cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas);
 cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);

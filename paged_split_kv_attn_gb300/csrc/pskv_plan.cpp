@@ -104,7 +104,8 @@ int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride
 }
 
 int pick_kernel(int kv_dtype, int head_dim, int group) {
-  if (kv_dtype == PSKV_DTYPE_BF16 && group == 8 && (head_dim == 256 || head_dim == 512))
+  const bool mma_group = group == 1 || group == 2 || group == 4 || group == 8;
+  if (kv_dtype == PSKV_DTYPE_BF16 && mma_group && (head_dim == 256 || head_dim == 512))
     return kKernelMma;
   const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8 ||
                     (group == 16 && head_dim == 256);

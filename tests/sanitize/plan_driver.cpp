@@ -77,7 +77,8 @@ int main() {
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 512, 8) == kKernelMma);
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 8) == kKernelMma);
   CHECK(pick_kernel(PSKV_DTYPE_F32, 512, 8) == kKernelSimt);
-  CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 2) == kKernelSimt);
+  CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 2) == kKernelMma);
+  CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 16) == kKernelSimt);
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 512, 16) == -1);
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 128, 8) == -1);
   std::puts("plan driver ok");
