@@ -201,8 +201,9 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
  *   out          device [rows][head_dim_v] of out_dtype
  *   workspace    device scratch of merge_partials_workspace_bytes(...) bytes
  *   status       device int32[4] fault word or NULL
- * The empty state is (m = -inf, l = 0) and its o is not read; merging an empty
- * state changes nothing.  Groups are folded in index order. */
+ * The empty state is (m = -inf, l = 0); its o is never used (it may be
+ * uninitialised); merging an empty state changes nothing.  Groups are folded
+ * in index order. */
 int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
                    int32_t num_splits, int32_t head_dim_v, void *out, int32_t out_dtype,
                    void *workspace, size_t workspace_bytes, int32_t *status,

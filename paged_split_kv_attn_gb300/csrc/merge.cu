@@ -11,7 +11,7 @@
 // removes that race by construction).  Level 2 folds the group results of a
 // row and writes out = o / l.  Folding order is fixed (index order), so the
 // result is deterministic.  An empty state (m = -inf) contributes nothing and
-// its o is never read; an empty state that carries l != 0 (or a NaN m) is
+// its o is never used; an empty state that carries l != 0 (or a NaN m) is
 // flagged PSKV_FAULT_BAD_STATE and treated as empty.
 #include <math_constants.h>
 
@@ -67,34 +67,59 @@ __device__ void state_weights(const float *m, const float *l, int n, float *w_s,
   __syncthreads();
 }
 
-// acc += sum_i w_i o_i[d4] over states [0, n) of `o` (row stride dv floats),
-// kChunk loads in flight at a time; empty states are skipped by selection.
-// kCoherent loads through L2 only (for data other CTAs of this grid just wrote).
-template <bool kCoherent = false>
-__device__ __forceinline__ float4 fold_o(const float *o, int n, int dv, int d4, const float *w_s) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < n; i0 += kChunk) {
-    float4 v[kChunk];
+// Load o_i[d4] of states [i0, i0 + kChunk) (those below n), all in flight at once.
+// The values of empty states are loaded too but never used (their o may be
+// uninitialised); loading them keeps the loads independent of the weights, so
+// they overlap the (m, l) loads.  kCoherent reads through L2 only (for data
+// other blocks of this grid just wrote).
+template <bool kCoherent>
+__device__ __forceinline__ void load_chunk(const float *o, int n, int dv, int d4, int i0,
+                                           float4 (&v)[kChunk]) {
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k)
-      if (i0 + k < n && w_s[i0 + k] >= 0.f) {
-        const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4;
-        v[k] = kCoherent ? __ldcg(src) : __ldg(src);
-      }
+  for (int k = 0; k < kChunk; ++k)
+    if (i0 + k < n) {
+      const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4;
+      v[k] = kCoherent ? __ldcg(src) : __ldg(src);
+    }
+}
+
+// acc += w_i v[i - i0] over the chunk's states, in index order; empty states
+// (w < 0) are skipped by selection, so whatever their o holds never reaches acc.
+__device__ __forceinline__ void combine_chunk(float4 &acc, const float4 (&v)[kChunk], int n,
+                                              int i0, const float *w_s) {
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      if (i0 + k < n) {
-        const float w = w_s[i0 + k];
-        if (w >= 0.f) {
-          acc.x = fmaf(v[k].x, w, acc.x);
-          acc.y = fmaf(v[k].y, w, acc.y);
-          acc.z = fmaf(v[k].z, w, acc.z);
-          acc.w = fmaf(v[k].w, w, acc.w);
-        }
+  for (int k = 0; k < kChunk; ++k) {
+    if (i0 + k < n) {
+      const float w = w_s[i0 + k];
+      if (w >= 0.f) {
+        acc.x = fmaf(v[k].x, w, acc.x);
+        acc.y = fmaf(v[k].y, w, acc.y);
+        acc.z = fmaf(v[k].z, w, acc.z);
+        acc.w = fmaf(v[k].w, w, acc.w);
       }
     }
   }
-  return acc;
+}
+
+// Fold the n states of one row: (m, l) weights by warp 0, o by every thread,
+// with the first chunk of each thread's first column loaded before the weights.
+// Calls f(d4, acc) for every column d4 of the row.
+template <bool kCoherent, class F>
+__device__ __forceinline__ void fold_states(const float *m, const float *l, const float *o, int n,
+                                            int dv, float *w_s, float *M_s, float *L_s,
+                                            int32_t *status, F &&f) {
+  const int dv4 = dv / 4;
+  float4 v[kChunk];
+  if ((int)threadIdx.x < dv4) load_chunk<kCoherent>(o, n, dv, threadIdx.x, 0, v);
+  state_weights<kCoherent>(m, l, n, w_s, M_s, L_s, status);
+  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < n; i0 += kChunk) {
+      if (d4 != (int)threadIdx.x || i0 != 0) load_chunk<kCoherent>(o, n, dv, d4, i0, v);
+      combine_chunk(acc, v, n, i0, w_s);
+    }
+    f(d4, acc);
+  }
 }
 
 // grid (groups, rows): fold partials [grp*group, min(count, (grp+1)*group)) of a row.
@@ -106,18 +131,17 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_level1(const MergeAr
   const int p0 = grp * a.group;
   const int n = min(a.count - p0, a.group);
   const size_t base = (size_t)row * a.count + p0;
+  const size_t out_state = (size_t)row * ng + grp;
   pdl_wait();
   pdl_launch_dependents();
-  state_weights(a.m + base, a.l + base, n, w_s, &M_s, &L_s, a.status);
-  const size_t out_state = (size_t)row * ng + grp;
+  fold_states<false>(a.m + base, a.l + base, a.o + base * a.dv, n, a.dv, w_s, &M_s, &L_s,
+                     a.status, [&](int d4, float4 acc) {
+                       reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] = acc;
+                     });
   if (threadIdx.x == 0) {
     a.m1[out_state] = M_s;
     a.l1[out_state] = L_s;
   }
-  const int dv4 = a.dv / 4;
-  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x)
-    reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] =
-        fold_o(a.o + base * a.dv, n, a.dv, d4, w_s);
 }
 
 // Fold all `n` states of `row` and write the normalised output row.
@@ -125,19 +149,12 @@ template <bool kCoherent>
 __device__ void fold_and_finalize(const float *m, const float *l, const float *o, int n, int row,
                                   const MergeArgs &a, float *w_s, float &M_s, float &L_s) {
   const size_t base = (size_t)row * n;
-  state_weights<kCoherent>(m + base, l + base, n, w_s, &M_s, &L_s, a.status);
-  const bool empty_row = (M_s == -CUDART_INF_F);
-  if (empty_row && threadIdx.x == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
-  const float L = L_s;
-  const int dv4 = a.dv / 4;
-  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
-    const float4 acc = fold_o<kCoherent>(o + base * a.dv, n, a.dv, d4, w_s);
-    float4 r;
-    if (empty_row) {
-      r = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      r = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
-    }
+  fold_states<kCoherent>(m + base, l + base, o + base * a.dv, n, a.dv, w_s, &M_s, &L_s, a.status,
+                         [&](int d4, float4 acc) {
+    const bool empty_row = (M_s == -CUDART_INF_F);
+    const float L = L_s;
+    const float4 r = empty_row ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
     if (a.out_dtype == PSKV_DTYPE_BF16) {
       uint2 packed;
       packed.x = pack_bf16x2(r.x, r.y);
@@ -146,7 +163,8 @@ __device__ void fold_and_finalize(const float *m, const float *l, const float *o
     } else {
       reinterpret_cast<float4 *>(static_cast<char *>(a.out) + (size_t)row * a.dv * 4)[d4] = r;
     }
-  }
+  });
+  if (threadIdx.x == 0 && M_s == -CUDART_INF_F) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
 }
 
 // grid (rows): fold all `n` states of a row and normalise.
@@ -176,16 +194,15 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_two_level(const Merg
   const size_t base = (size_t)row * a.count + p0;
   pdl_wait();
   pdl_launch_dependents();
-  state_weights(a.m + base, a.l + base, n, w_s, &M_s, &L_s, a.status);
   const size_t out_state = (size_t)row * ng + grp;
+  fold_states<false>(a.m + base, a.l + base, a.o + base * a.dv, n, a.dv, w_s, &M_s, &L_s,
+                     a.status, [&](int d4, float4 acc) {
+                       reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] = acc;
+                     });
   if (threadIdx.x == 0) {
     a.m1[out_state] = M_s;
     a.l1[out_state] = L_s;
   }
-  const int dv4 = a.dv / 4;
-  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x)
-    reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] =
-        fold_o(a.o + base * a.dv, n, a.dv, d4, w_s);
   // publish this group's result, then count it
   __threadfence();
   __syncthreads();
