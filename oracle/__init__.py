@@ -10,8 +10,10 @@ source pages each step follows.
 
 Arrays:
   * bf16 data is passed as ``uint16`` bit patterns, f32 data as ``float32``;
-  * pools are ``[num_pages, num_kv_heads, page_size, head_dim]``;
-  * ``q`` is ``[batch, num_q_heads, head_dim_k]``, outputs are float64
+  * pools are ``[num_pages, num_kv_heads, page_size, head_dim]``; a K pool
+    narrower than its V pool is a folded pool (see pskv_oracle.h);
+  * ``q`` is ``[batch, num_q_heads, key width]`` (head_dim_k for a split pool,
+    head_dim_v for a folded one), outputs are float64
     ``[batch, num_q_heads, head_dim_v]``.
 """
 from __future__ import annotations
@@ -49,7 +51,7 @@ class _Pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dtype", ctypes.c_int),
                 ("num_pages", ctypes.c_int64), ("page_size", ctypes.c_int),
                 ("num_kv_heads", ctypes.c_int), ("head_dim_k", ctypes.c_int),
-                ("head_dim_v", ctypes.c_int)]
+                ("head_dim_v", ctypes.c_int), ("format", ctypes.c_int)]
 
 
 _lib = None
@@ -173,15 +175,18 @@ def _pool(k_pool, v_pool):
     v_pool, vt = _data(v_pool)
     if kt != vt or k_pool.ndim != 4 or v_pool.ndim != 4 or k_pool.shape[:3] != v_pool.shape[:3]:
         raise ValueError("k_pool / v_pool must be [num_pages, num_kv_heads, page_size, d] of one dtype")
+    # a K region narrower than the V region is a folded pool
+    fmt = 1 if k_pool.shape[3] < v_pool.shape[3] else 0
     p = _Pool(k_pool.ctypes.data, v_pool.ctypes.data, kt, k_pool.shape[0], k_pool.shape[2],
-              k_pool.shape[1], k_pool.shape[3], v_pool.shape[3])
+              k_pool.shape[1], k_pool.shape[3], v_pool.shape[3], fmt)
     return p, (k_pool, v_pool)
 
 
 def gather(k_pool, v_pool, page_tables, b, g, length):
+    """Keys (as a query meets them) and values of (row b, KV head g)."""
     pool, keep = _pool(k_pool, v_pool)
     tables = _c(page_tables, np.int32)
-    k = np.zeros((length, pool.head_dim_k), np.float64)
+    k = np.zeros((length, pool.head_dim_v if pool.format else pool.head_dim_k), np.float64)
     v = np.zeros((length, pool.head_dim_v), np.float64)
     _check(_load().orc_gather(ctypes.byref(pool), _ptr(tables), tables.shape[1], b, g, length,
                               _ptr(k), _ptr(v)), "gather")

@@ -270,9 +270,24 @@ int orc_attend_partitioned_f32(const float *q, const float *k, const float *v, i
 /* ---- paged pool ---------------------------------------------------------- */
 
 static int pool_valid(const orc_pool *p) {
-  return p && p->k && p->v && (p->dtype == ORC_F32 || p->dtype == ORC_BF16) &&
-         p->num_pages > 0 && p->page_size > 0 && p->num_kv_heads > 0 && p->head_dim_k > 0 &&
-         p->head_dim_v > 0;
+  if (!(p && p->k && p->v && (p->dtype == ORC_F32 || p->dtype == ORC_BF16) &&
+        p->num_pages > 0 && p->page_size > 0 && p->num_kv_heads > 0 && p->head_dim_k > 0 &&
+        p->head_dim_v > 0))
+    return 0;
+  if (p->format == ORC_SPLIT) return 1;
+  return p->format == ORC_FOLDED && p->head_dim_k < p->head_dim_v;
+}
+
+/* Width of the key a query meets (and of the query). */
+static int key_width(const orc_pool *p) {
+  return p->format == ORC_FOLDED ? p->head_dim_v : p->head_dim_k;
+}
+
+/* Element d of the key stored at element offsets kr (K region) and vr (V
+ * region): a folded pool takes columns past its K width from V. */
+static double key_elem(const orc_pool *p, size_t kr, size_t vr, int d) {
+  if (p->format == ORC_FOLDED && d >= p->head_dim_k) return load_elem(p->v, p->dtype, vr + d);
+  return load_elem(p->k, p->dtype, kr + d);
 }
 
 int orc_gather(const orc_pool *pool, const int32_t *page_tables, int table_stride, int b, int g,
@@ -282,12 +297,12 @@ int orc_gather(const orc_pool *pool, const int32_t *page_tables, int table_strid
     return ORC_ERR_INVALID;
   if ((int64_t)len > (int64_t)table_stride * pool->page_size) return ORC_ERR_INVALID;
   const int ps = pool->page_size, H = pool->num_kv_heads;
-  const int dk = pool->head_dim_k, dv = pool->head_dim_v;
+  const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
   for (int i = 0; i < len; ++i) {
     const int32_t page = page_tables[(size_t)b * table_stride + i / ps];
     if (page < 0 || page >= pool->num_pages) return ORC_ERR_BAD_PAGE;
     const size_t row = ((size_t)page * H + g) * ps + (size_t)(i % ps);
-    for (int d = 0; d < dk; ++d) k_out[(size_t)i * dk + d] = load_elem(pool->k, pool->dtype, row * dk + d);
+    for (int d = 0; d < kw; ++d) k_out[(size_t)i * kw + d] = key_elem(pool, row * dk, row * dv, d);
     for (int d = 0; d < dv; ++d) v_out[(size_t)i * dv + d] = load_elem(pool->v, pool->dtype, row * dv + d);
   }
   return ORC_OK;
@@ -370,7 +385,7 @@ int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_t
   int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo,
                           batch, num_q_heads, out);
   if (rc) return rc;
-  const int dk = pool->head_dim_k, dv = pool->head_dim_v;
+  const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
   const int G = num_q_heads / pool->num_kv_heads; /* head h reads kv head h / G */
   int rc_all = ORC_OK;
   const int jobs = batch * num_q_heads;
@@ -378,20 +393,21 @@ int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_t
   for (int job = 0; job < jobs; ++job) {
     const int b = job / num_q_heads, h = job % num_q_heads, g = h / G, len = seq_lens[b];
     const int i0 = first_key(first_pos, window_lo, b, len);
-    double *qd = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)kw);
     double *s = (double *)malloc(sizeof(double) * (size_t)(len - i0));
     double *dst = out + ((size_t)b * num_q_heads + h) * dv;
     if (!qd || !s) {
 #pragma omp critical
       rc_all = ORC_ERR_INVALID;
     } else {
-      for (int d = 0; d < dk; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)b * num_q_heads + h) * dk + d);
+      for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)b * num_q_heads + h) * kw + d);
       /* s_i = scale * q . k_i over the attended keys */
       double mx = -INFINITY;
       for (int i = i0; i < len; ++i) {
         const size_t kr = paged_row(pool, dk, page_tables, table_stride, b, g, i);
+        const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
         double acc = 0.0;
-        for (int d = 0; d < dk; ++d) acc += qd[d] * load_elem(pool->k, pool->dtype, kr + d);
+        for (int d = 0; d < kw; ++d) acc += qd[d] * key_elem(pool, kr, vr, d);
         s[i - i0] = scale * acc;
         if (s[i - i0] > mx) mx = s[i - i0];
       }
@@ -422,7 +438,7 @@ int orc_decode_online(const orc_pool *pool, const void *q, const int32_t *page_t
                           batch, num_q_heads, out);
   if (rc) return rc;
   if (chunk_tokens <= 0 || num_splits <= 0 || group_size <= 0) return ORC_ERR_INVALID;
-  const int H = pool->num_kv_heads, dk = pool->head_dim_k, dv = pool->head_dim_v;
+  const int H = pool->num_kv_heads, dk = key_width(pool), dv = pool->head_dim_v;
   const int G = num_q_heads / H;
   int rc_all = ORC_OK;
   const int jobs = batch * H;

@@ -49,7 +49,15 @@ extern "C" {
 #define ORC_F32 0
 #define ORC_BF16 1
 
-/* Geometry of one paged pool (both regions share it). */
+#define ORC_SPLIT 0
+#define ORC_FOLDED 1
+
+/* Geometry of one paged pool (both regions share it).
+ * Split pools store whole K rows (head_dim_k == head_dim_v).  Folded pools
+ * ([pg1055] Description: K kept only where the rotation touches it, V in
+ * full, K's norm weight folded into the query) store only the first
+ * head_dim_k < head_dim_v columns of K; the key a query meets is then
+ * [k[0:head_dim_k], v[head_dim_k:head_dim_v]] and queries are head_dim_v wide. */
 typedef struct orc_pool {
   const void *k;  /* K region */
   const void *v;  /* V region */
@@ -59,6 +67,7 @@ typedef struct orc_pool {
   int num_kv_heads;
   int head_dim_k;
   int head_dim_v;
+  int format;     /* ORC_SPLIT or ORC_FOLDED */
 } orc_pool;
 
 /* Online-softmax state of one query head over a set of keys:
@@ -104,8 +113,9 @@ int orc_attend_partitioned_f32(const float *q, const float *k, const float *v, i
 /* ---- paged pool ------------------------------------------------------- */
 
 /* Gather the keys and values of (row b, kv head g) into dense double arrays
- * k_out[len][dk], v_out[len][dv].  Fails on a page id outside the pool or a
- * length past the table. */
+ * k_out[len][key width], v_out[len][dv]; the key width is head_dim_k for a
+ * split pool and head_dim_v (the assembled key) for a folded one.  Fails on
+ * a page id outside the pool or a length past the table. */
 int orc_gather(const orc_pool *pool, const int32_t *page_tables, int table_stride, int b, int g,
                int len, double *k_out, double *v_out);
 

@@ -33,12 +33,15 @@ def q_f64(case):
 
 def brute_force(case):
     """softmax(scale * q K^T) V on the dense tensors, with scipy's softmax; query
-    head h reads KV head h // (Hq / Hkv)."""
+    head h reads KV head h // (Hq / Hkv).  For a folded pool the key is the
+    stored K columns followed by V's remaining columns."""
     q = q_f64(case)
     G = case.num_q_heads // case.num_kv_heads
     out = np.zeros((case.batch, case.num_q_heads, case.head_dim))
     for b in range(case.batch):
         K, V = dense_f64(case, b)
+        if case.folded:
+            K = np.concatenate([K, V[:, :, K.shape[2]:]], axis=2)
         lo = 0
         if case.window_lo is not None:
             lo = max(0, int(case.window_lo[b]) - int(case.first_pos[b]))
@@ -371,3 +374,54 @@ def test_refuses_empty_rows():
     case = W.make_paged_case(1, [4], num_q_heads=2, num_kv_heads=1, head_dim=8, page_size=8)
     with pytest.raises(oracle.OracleError):
         oracle.decode_direct(case.q, case.k_pool, case.v_pool, case.page_tables, [0], case.scale)
+
+
+# ---- the folded format ----------------------------------------------------------
+
+def split_twin(case):
+    """The split pool a folded pool stands for: K = [stored K, V's remaining columns]."""
+    import dataclasses
+    dk = case.k_pool.shape[3]
+    k_full = np.concatenate([case.k_pool, case.v_pool[..., dk:]], axis=3)
+    return dataclasses.replace(case, k_pool=np.ascontiguousarray(k_full))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_folded_equals_its_split_twin_exactly(dtype):
+    case = W.make_paged_case(31, [1, 70, 257], num_q_heads=8, num_kv_heads=2, head_dim=32,
+                             page_size=16, dtype=dtype, k_dims=8)
+    assert case.folded
+    twin = split_twin(case)
+    assert np.array_equal(run_direct(case), run_direct(twin))
+    for parts in (1, 5):
+        a = oracle.decode_online(case.q, case.k_pool, case.v_pool, case.page_tables,
+                                 case.seq_lens, case.scale, num_splits=parts, chunk_tokens=16)
+        b = oracle.decode_online(twin.q, twin.k_pool, twin.v_pool, twin.page_tables,
+                                 twin.seq_lens, twin.scale, num_splits=parts, chunk_tokens=16)
+        assert np.array_equal(a, b)
+
+
+def test_folded_matches_brute_force():
+    case = W.make_paged_case(32, [3, 90, 140], num_q_heads=4, num_kv_heads=2, head_dim=24,
+                             page_size=8, k_dims=6)
+    np.testing.assert_allclose(run_direct(case), brute_force(case), rtol=0, atol=1e-12)
+    k, v = oracle.gather(case.k_pool, case.v_pool, case.page_tables, 1, 1, 90)
+    K, V = dense_f64(case, 1)
+    assert np.array_equal(k[:, :6], K[:, 1]) and np.array_equal(k[:, 6:], V[:, 1, 6:])
+
+
+def test_folded_stored_columns_reach_the_score():
+    """Changing a stored K column changes the output; changing V's first columns
+    (which a folded key does not use) changes only the value side."""
+    case = W.make_paged_case(33, [20], num_q_heads=2, num_kv_heads=1, head_dim=16, page_size=16,
+                             dtype="f32", k_dims=4)
+    base = run_direct(case)
+    page = case.page_tables[0, 0]
+    k_saved = case.k_pool.copy()
+    case.k_pool[page, 0, 3, 0] += 5.0  # one key's stored column (a shift of all keys would cancel)
+    assert not np.allclose(run_direct(case), base)
+    case.k_pool[:] = k_saved
+    case.v_pool[page, 0, 3, 1] += 5.0  # V column 1 < k_dims: only the value side moves
+    out = run_direct(case)
+    moved = np.abs(out - base).max(axis=(0, 1))
+    assert moved[1] > 0 and np.all(moved[np.arange(16) != 1] == 0)

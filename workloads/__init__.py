@@ -81,7 +81,12 @@ class PagedCase:
 
     @property
     def head_dim(self) -> int:
-        return self.k_pool.shape[3]
+        return self.v_pool.shape[3]
+
+    @property
+    def folded(self) -> bool:
+        """True for a folded pool (the K region narrower than the V region)."""
+        return self.k_pool.shape[3] < self.v_pool.shape[3]
 
     @property
     def page_size(self) -> int:
@@ -94,20 +99,25 @@ class PagedCase:
     def kv_bytes(self) -> int:
         """Bytes of K and V the attended keys occupy."""
         es = 2 if self.dtype == "bf16" else 4
+        row_elems = self.k_pool.shape[3] + self.v_pool.shape[3]
         n = 0
         for b in range(self.batch):
             lo = 0
             if self.window_lo is not None:
                 lo = min(max(int(self.window_lo[b]) - int(self.first_pos[b]), 0), int(self.seq_lens[b]))
             n += int(self.seq_lens[b]) - lo
-        return n * self.num_kv_heads * self.head_dim * 2 * es
+        return n * self.num_kv_heads * row_elems * es
 
 
 def make_paged_case(seed: int, seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
                     page_size: int, dtype: str = "bf16", shuffle: bool = True,
                     extra_pages: int = 0, table_stride: int | None = None,
-                    keep_dense: bool | None = None, scale: float | None = None) -> PagedCase:
-    """Build a paged pool holding random K/V for every row, plus random queries."""
+                    keep_dense: bool | None = None, scale: float | None = None,
+                    k_dims: int | None = None) -> PagedCase:
+    """Build a paged pool holding random K/V for every row, plus random queries.
+
+    ``k_dims`` < head_dim makes a folded pool: the K region keeps k_dims
+    columns per row, the V region head_dim (queries are head_dim wide)."""
     if dtype not in ("bf16", "f32"):
         raise ValueError(dtype)
     # values and page order come from independent streams, so a shuffled and an
@@ -135,31 +145,33 @@ def make_paged_case(seed: int, seq_lens, num_q_heads: int, num_kv_heads: int, he
         tables[b, :n] = ids[cursor:cursor + n]
         cursor += n
 
+    dk = head_dim if k_dims is None else k_dims
     shape = (num_pages, num_kv_heads, page_size, head_dim)
+    kshape = (num_pages, num_kv_heads, page_size, dk)
     if dtype == "bf16":
-        k_pool = np.full(shape, BF16_NAN, np.uint16)
+        k_pool = np.full(kshape, BF16_NAN, np.uint16)
         v_pool = np.full(shape, BF16_NAN, np.uint16)
     else:
-        k_pool = np.full(shape, np.nan, np.float32)
+        k_pool = np.full(kshape, np.nan, np.float32)
         v_pool = np.full(shape, np.nan, np.float32)
 
     dense_k, dense_v = ([], []) if keep_dense else (None, None)
     for b, n in enumerate(seq_lens):
         if keep_dense:
-            dk = _normal(rng, (n, num_kv_heads, head_dim), dtype)
-            dv = _normal(rng, (n, num_kv_heads, head_dim), dtype)
-            dense_k.append(dk)
-            dense_v.append(dv)
+            dkk = _normal(rng, (n, num_kv_heads, dk), dtype)
+            dvv = _normal(rng, (n, num_kv_heads, head_dim), dtype)
+            dense_k.append(dkk)
+            dense_v.append(dvv)
         for j in range(pages_of_row[b]):
             lo, hi = j * page_size, min(n, (j + 1) * page_size)
             if hi <= lo:
                 continue
             page = tables[b, j]
             if keep_dense:
-                kk = dk[lo:hi].transpose(1, 0, 2)
-                vv = dv[lo:hi].transpose(1, 0, 2)
+                kk = dkk[lo:hi].transpose(1, 0, 2)
+                vv = dvv[lo:hi].transpose(1, 0, 2)
             else:
-                kk = _normal(rng, (num_kv_heads, hi - lo, head_dim), dtype)
+                kk = _normal(rng, (num_kv_heads, hi - lo, dk), dtype)
                 vv = _normal(rng, (num_kv_heads, hi - lo, head_dim), dtype)
             k_pool[page, :, :hi - lo, :] = kk
             v_pool[page, :, :hi - lo, :] = vv
@@ -186,6 +198,12 @@ def with_window(case: PagedCase, window: int, first_pos=None) -> PagedCase:
 GLOBAL_SHAPE = dict(num_q_heads=32, num_kv_heads=4, head_dim=512, page_size=256)
 WINDOW_SHAPE = dict(num_q_heads=32, num_kv_heads=16, head_dim=256, page_size=64)
 WINDOW = 1024
+
+
+def folded_case(context: int, seed: int = 0, batch: int = 1) -> PagedCase:
+    """The global-layer shape in the folded format: per token and KV head the
+    K region keeps the rotated quarter (128 columns), V all 512 (640 in all)."""
+    return make_paged_case(seed, [context] * batch, dtype="bf16", k_dims=128, **GLOBAL_SHAPE)
 
 
 def tiny_case(seed: int = 0) -> PagedCase:
