@@ -285,6 +285,12 @@ class Packed:
         self.host_out.copy_(self.dev_out, non_blocking=True)
 
 
+def make_extra_calls(args, dev):
+    """Calls measured one at a time beside the step: the folded format (NEXT row)."""
+    return [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev, ROTATE)
+            for ctx in args.folded_contexts]
+
+
 def make_calls(args, dev):
     calls = []
     for ctx in args.contexts:
@@ -329,6 +335,8 @@ def parse():
     ap.add_argument("--splits", type=int, default=0, help="global-layer split count (0 = auto)")
     ap.add_argument("--window-splits", type=int, default=0)
     ap.add_argument("--no-window", action="store_true")
+    ap.add_argument("--folded-contexts", type=int, nargs="*", default=[40002],
+                    help="contexts of the folded-format decode timed beside the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
@@ -490,8 +498,21 @@ def main():
 
     # per-call µs/call (append + partial + merge), each call timed alone with a cold L2:
     # a 256 MB buffer is READ between calls (reads leave no dirty lines to write back)
+    extra = make_extra_calls(args, dev)
+    for c in extra:
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for it in range(args.warmup):
+            c.run(it)
+        for it in range(args.steps):
+            c.run(it, events=pe[it])
+        torch.cuda.synchronize()
+        part = [b.elapsed_time(e) for b, e in pe]
+        per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
+                            "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9,
+                            "note": "folded format, measured beside the step (not in value)"}
     flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
-    for c in calls:
+    for c in calls + extra:
         times = []
         for it in range(max(5, min(args.steps, 30))):
             flush.sum()

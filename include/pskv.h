@@ -63,7 +63,8 @@ typedef struct CUevent_st *pskv_event_t;
 #define PSKV_DTYPE_BF16 1
 
 #define PSKV_FORMAT_SPLIT 0   /* K and V rows kept whole, one region each */
-#define PSKV_FORMAT_FOLDED 1  /* reserved (pegainfer #1055's 640-column row): refused */
+#define PSKV_FORMAT_FOLDED 1  /* K keeps only its first head_dim_v/4 columns (pegainfer #1055's
+                                 640-column row at head dim 512), V in full; bf16 only */
 
 /* ---- device fault bits, ORed into status[0] of the layout's status word ------ */
 #define PSKV_FAULT_BAD_PAGE 1u      /* a table entry outside [0, num_pages): that tile or row skipped */
@@ -91,15 +92,24 @@ typedef struct CUevent_st *pskv_event_t;
  *
  * status: device int32[4] the caller zeroes; kernels OR PSKV_FAULT_* bits into
  * status[0].  May be NULL (faults are then skipped silently).
- * The format is fixed for the pool's life (pegainfer #1055, Description). */
+ * The format is fixed for the pool's life (pegainfer #1055, Description).
+ *
+ * Folded format (pegainfer #1055, Description: the folded row holds K only
+ * where the rotation touches it, V in full, and the prep folds K's norm
+ * weight into the query): the K region keeps the first head_dim_v/4 columns
+ * of each key (the rotated quarter), the V region all head_dim_v; queries
+ * are head_dim_v wide and the score of key i is
+ *     scale * (q[0:Dr] . k_i[0:Dr] + q[Dr:Dv] . v_i[Dr:Dv]),  Dr = Dv/4,
+ * i.e. the key is taken to equal V outside the rotated quarter once the norm
+ * weight sits in q (this library's reading of the page). */
 typedef struct pskv_layout_desc {
   int64_t num_pages;   /* pages in each region, >= 1 */
   int32_t page_size;   /* keys per page: a multiple of PSKV_KEY_TILE */
   int32_t num_kv_heads;
-  int32_t head_dim_k;  /* 256 or 512 */
-  int32_t head_dim_v;  /* must equal head_dim_k in this build */
+  int32_t head_dim_k;  /* stored K columns: head_dim_v (split) or head_dim_v / 4 (folded) */
+  int32_t head_dim_v;  /* 256 or 512 */
   int32_t kv_dtype;    /* PSKV_DTYPE_F32 or PSKV_DTYPE_BF16 (queries use the same type) */
-  int32_t format;      /* PSKV_FORMAT_SPLIT */
+  int32_t format;      /* PSKV_FORMAT_SPLIT or PSKV_FORMAT_FOLDED */
   void *k_pool;        /* device, 16-byte aligned */
   void *v_pool;        /* device, 16-byte aligned */
   int32_t *status;     /* device int32[4] or NULL */
@@ -117,8 +127,9 @@ typedef struct pskv_decode_opts {
 
 /* Validate `desc` and make a layout handle.  Touches no device.
  * Errors: INVALID_ARG (null pointers, sizes < 1, misaligned pools,
- * page_size not a multiple of PSKV_KEY_TILE), UNSUPPORTED (format FOLDED,
- * head_dim not 256/512, head_dim_k != head_dim_v). */
+ * page_size not a multiple of PSKV_KEY_TILE, unknown format), UNSUPPORTED
+ * (head_dim_v not 256/512; split with head_dim_k != head_dim_v; folded with
+ * head_dim_k != head_dim_v / 4 or an f32 pool). */
 int paged_kv_layout_create(const pskv_layout_desc *desc, pskv_layout **out);
 
 /* Free a handle (NULL is ignored).  The pools are the caller's. */
@@ -126,7 +137,8 @@ void paged_kv_layout_destroy(pskv_layout *layout);
 
 /* Append n new rows into the pool, bit for bit (TensorFold #1619, "Writes":
  * rows copied into the pages keep the linear cache's bits).
- *   k_new, v_new     device [n][num_kv_heads][head_dim], the pool's dtype, 16-byte aligned
+ *   k_new, v_new     device [n][num_kv_heads][head_dim_k] and [n][num_kv_heads][head_dim_v],
+ *                    the pool's dtype, 16-byte aligned
  *   row_of, pos_of   device int32[n]: table row and key position of each new row
  *   page_tables      device int32[batch][table_stride]
  *   pages_of_row     device int32[batch]: pages row b holds (its lease)
@@ -146,7 +158,8 @@ int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_n
                    const int32_t *pages_of_row_host, pskv_stream_t stream);
 
 /* Split-KV decode: one query token per row.
- *   q              device [batch][num_q_heads][head_dim], the pool's dtype
+ *   q              device [batch][num_q_heads][head_dim_v], the pool's dtype (for a
+ *                  folded pool, the folded query: see pskv_layout_desc)
  *   page_tables    device int32[batch][table_stride]; entries past a row's
  *                  pages are never read
  *   seq_lens_host  host int32[batch]: keys per row, each in [1, table_stride * page_size];
@@ -167,8 +180,10 @@ int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_n
  *   out            device [batch][num_q_heads][head_dim] of out_dtype
  *                  (PSKV_DTYPE_BF16, round to nearest even, or PSKV_DTYPE_F32)
  * The result is run-to-run deterministic for a fixed split count.
- * Errors: INVALID_ARG, UNSUPPORTED (num_q_heads % num_kv_heads != 0 or a
- * query-group size this build has no kernel for), WORKSPACE_TOO_SMALL, CUDA. */
+ * Errors: INVALID_ARG, UNSUPPORTED (num_q_heads % num_kv_heads != 0, or a
+ * query-group size this build has no kernel for: bf16 takes 1/2/4/8 query heads
+ * per KV head (and 16 at head dim 256, split only), f32 takes 1/2/4/8 (16 at
+ * head dim 256)), WORKSPACE_TOO_SMALL, CUDA. */
 int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t *page_tables,
                         int32_t table_stride, const int32_t *seq_lens_host,
                         const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,

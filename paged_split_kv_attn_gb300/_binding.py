@@ -217,12 +217,14 @@ class Layout:
 
 
 def paged_kv_layout_create(k_pool: torch.Tensor, v_pool: torch.Tensor,
-                           status: torch.Tensor | None = None,
-                           fmt: int = PSKV_FORMAT_SPLIT) -> Layout:
-    """Wrap pools shaped [num_pages, num_kv_heads, page_size, head_dim]."""
+                           status: torch.Tensor | None = None, fmt: int | None = None) -> Layout:
+    """Wrap pools shaped [num_pages, num_kv_heads, page_size, head_dim]; a K pool
+    narrower than the V pool is a folded pool unless ``fmt`` says otherwise."""
     lib = load_library()
     if k_pool.dim() != 4 or v_pool.dim() != 4 or k_pool.shape[:3] != v_pool.shape[:3]:
         raise ValueError("pools must be [num_pages, num_kv_heads, page_size, head_dim]")
+    if fmt is None:
+        fmt = PSKV_FORMAT_FOLDED if k_pool.shape[3] < v_pool.shape[3] else PSKV_FORMAT_SPLIT
     if k_pool.dtype != v_pool.dtype:
         raise TypeError("k_pool and v_pool must share a dtype")
     desc = LayoutDesc(k_pool.shape[0], k_pool.shape[2], k_pool.shape[1], k_pool.shape[3],

@@ -14,6 +14,7 @@ namespace pskv {
 constexpr int kAppendWarps = 4;
 
 // Longest row handled: 2048 bytes (head dim 512 in f32) = 4 vectors of 16 bytes per lane.
+// (K rows of a folded pool are a quarter of that.)
 constexpr int kMaxVecsPerLane = 4;
 
 __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const AppendArgs a) {
@@ -25,19 +26,17 @@ __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const Appe
   const int r = (int)(item / a.num_kv_heads), h = (int)(item % a.num_kv_heads);
   const size_t src_row = (size_t)r * a.num_kv_heads + h;
   const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.k_new) +
-                                                    src_row * a.row_bytes);
+                                                    src_row * a.k_row_bytes);
   const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.v_new) +
-                                                    src_row * a.row_bytes);
-  const int vecs = a.row_bytes / 16;
+                                                    src_row * a.v_row_bytes);
+  const int kvecs = a.k_row_bytes / 16, vvecs = a.v_row_bytes / 16;
   // the row's bytes and its indices are independent: load them all before any check
   uint4 kb[kMaxVecsPerLane], vb[kMaxVecsPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxVecsPerLane; ++i) {
     const int v = lane + 32 * i;
-    if (v < vecs) {
-      kb[i] = ks[v];
-      vb[i] = vs[v];
-    }
+    if (v < kvecs) kb[i] = ks[v];
+    if (v < vvecs) vb[i] = vs[v];
   }
   const int b = a.row_of[r], pos = a.pos_of[r];
   if (b < 0 || b >= a.batch || pos < 0) {
@@ -56,15 +55,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) pskv_append_rows(const Appe
     return;
   }
   const size_t dst_row = ((size_t)page * a.num_kv_heads + h) * a.page_size + pos % a.page_size;
-  uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(a.k_pool) + dst_row * a.row_bytes);
-  uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(a.v_pool) + dst_row * a.row_bytes);
+  uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(a.k_pool) + dst_row * a.k_row_bytes);
+  uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(a.v_pool) + dst_row * a.v_row_bytes);
 #pragma unroll
   for (int i = 0; i < kMaxVecsPerLane; ++i) {
     const int v = lane + 32 * i;
-    if (v < vecs) {
-      kd[v] = kb[i];
-      vd[v] = vb[i];
-    }
+    if (v < kvecs) kd[v] = kb[i];
+    if (v < vvecs) vd[v] = vb[i];
   }
 }
 

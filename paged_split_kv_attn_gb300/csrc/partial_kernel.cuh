@@ -49,21 +49,26 @@ namespace pskv {
 // (the stage count is a multiple of kWarps), so every stage is always consumed
 // by the same warp, in order: a consumer never waits on a phase more than one
 // ahead of its barrier's current phase.  Rows are copied in groups of kRows.
-template <int kRowBytes, int kRows, int kWarps>
+template <int kRowBytesK, int kRowBytesV, int kRows, int kWarps>
 struct RingGeom {
   static constexpr int kRowsPerCopy = kRows;
-  static constexpr int kGroupStride = kRows * kRowBytes + 16;
-  static constexpr int kTileBytes = (kKeyTile / kRows) * kGroupStride;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+  static constexpr int kGroupStrideK = kRows * kRowBytesK + 16;
+  static constexpr int kGroupStrideV = kRows * kRowBytesV + 16;
+  static constexpr int kTileBytesK = (kKeyTile / kRows) * kGroupStrideK;
+  static constexpr int kTileBytesV = (kKeyTile / kRows) * kGroupStrideV;
+  static constexpr int kStageBytes = kTileBytesK + kTileBytesV;  // K tile then V tile
   static constexpr int kPerWarpFit = PSKV_STAGE_BUDGET / (kWarps * kStageBytes);
   static constexpr int kPerWarpMax = 8 / kWarps > 0 ? 8 / kWarps : 1;
   static constexpr int kPerWarp =
       kPerWarpFit < 1 ? 1 : (kPerWarpFit > kPerWarpMax ? kPerWarpMax : kPerWarpFit);
   static constexpr int kStages = kWarps * kPerWarp;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  // byte offset of key row t (0..15) of a tile
-  static __device__ __forceinline__ int row_off(int t) {
-    return (t / kRows) * kGroupStride + (t % kRows) * kRowBytes;
+  // byte offset of key row t (0..15) in a K tile and in a V tile
+  static __device__ __forceinline__ int row_off_k(int t) {
+    return (t / kRows) * kGroupStrideK + (t % kRows) * kRowBytesK;
+  }
+  static __device__ __forceinline__ int row_off_v(int t) {
+    return (t / kRows) * kGroupStrideV + (t % kRows) * kRowBytesV;
   }
   static_assert(kKeyTile % kRows == 0, "row groups must divide the tile");
 };
@@ -108,7 +113,13 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
 
 // G < 8 query heads per KV head run on the same 8-column products with the
 // unused columns' queries set to zero (their results are never written).
-template <int kD, int kG = 8>
+// kFolded: the pool keeps only the first D/4 columns of K (the rotated quarter)
+// and the folded query's other columns meet V's (pegainfer #1055, Description:
+// the folded row holds K only where the rotation touches it, V in full, with
+// K's norm weight folded into the query).  Warp 0's quarter of D is exactly the
+// stored K columns, so warp 0 reads its score operands from the K tile and
+// warps 1..3 read theirs from the V tile.
+template <int kD, int kG = 8, bool kFolded = false>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
@@ -119,10 +130,14 @@ struct MmaConsumer {
   static constexpr int DW = D / kWarps;        // head-dim columns per warp
   static constexpr int KS = DW / 16;           // k-steps of QK = m-tiles of PV per warp
   static constexpr int kExtraSmem = 2 * kWarps * 32 * 16;  // double-buffered score exchange
-  using Geom = RingGeom<D * 2, 2, 1>;
-  static constexpr int RB = D * 2;               // bytes of one key row
-  static constexpr int GS = Geom::kGroupStride;  // bytes of a padded pair of rows
+  static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;  // bytes of one stored K row
+  static constexpr int kRowBytesV = D * 2;
+  using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1>;
+  static constexpr int RBK = kRowBytesK, RBV = kRowBytesV;
+  static constexpr int GSK = Geom::kGroupStrideK;  // bytes of a padded pair of K rows
+  static constexpr int GSV = Geom::kGroupStrideV;  // bytes of a padded pair of V rows
   static_assert(KS >= 2 && KS % 2 == 0, "two QK accumulator chains");
+  static_assert(!kFolded || DW == D / 4, "warp 0 must own exactly the stored K columns");
 
   uint32_t qf[KS][2];  // Q^T B-fragments: (d = dw0 + 16k + 2c + {0,1} [+8], head r)
   float o[KS][4];      // O^T accumulators: (d = dw0 + 16j + r [+8], heads 2c, 2c+1)
@@ -159,8 +174,11 @@ struct MmaConsumer {
     // ---- partial scores over this warp's d range, two accumulator chains for latency
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
     // A rows m = (mi&1)*8 + rr hold key 2*rr + (mi&1): pair rr, row (mi&1) of the pair
+    const bool from_v = kFolded && warp > 0;  // a folded key's columns past D/4 live in V
     const uint32_t kaddr =
-        smem_u32(ks) + rr * GS + (mi & 1) * RB + (mi >> 1) * 16 + warp * DW * 2;
+        from_v ? smem_u32(vs) + rr * GSV + (mi & 1) * RBV + (mi >> 1) * 16 + warp * DW * 2
+               : smem_u32(ks) + rr * GSK + (mi & 1) * RBK + (mi >> 1) * 16 +
+                     (kFolded ? 0 : warp * DW * 2);
 #pragma unroll
     for (int k = 0; k < KS; k += 2) {
       uint32_t a0, a1, a2, a3;
@@ -237,7 +255,7 @@ struct MmaConsumer {
     }
     // V^T A-fragment: source row k = rr + 8*(mi>>1) holds key 2*rr + (mi>>1)
     const uint32_t vaddr =
-        smem_u32(vs) + rr * GS + (mi >> 1) * RB + (mi & 1) * 16 + warp * DW * 2;
+        smem_u32(vs) + rr * GSV + (mi >> 1) * RBV + (mi & 1) * 16 + warp * DW * 2;
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
       uint32_t a0, a1, a2, a3;
@@ -311,7 +329,8 @@ struct SimtConsumer {
   // four consumer warps, two when a stage is too big for four of them
   static constexpr int kWarps = (D * (int)sizeof(T) > 1024) ? 2 : 4;
   static constexpr bool kCooperative = false;  // warp w takes tiles w, w + kWarps, ...
-  using Geom = RingGeom<D * (int)sizeof(T), kKeyTile, kWarps>;  // one copy per tile
+  static constexpr int kRowBytesK = D * (int)sizeof(T), kRowBytesV = D * (int)sizeof(T);
+  using Geom = RingGeom<kRowBytesK, kRowBytesV, kKeyTile, kWarps>;  // one copy per tile
 
   float q[kQInRegs ? G : 1][kQInRegs ? E : 1];
   float o[G][E];
@@ -396,7 +415,7 @@ struct SimtConsumer {
         for (int g = 0; g < G; ++g) s[u][g] = -CUDART_INF_F;
         if (valid[u]) {
           float kf[E];
-          load_row(reinterpret_cast<const T *>(ks + Geom::row_off(t0 + u)), lane, kf);
+          load_row(reinterpret_cast<const T *>(ks + Geom::row_off_k(t0 + u)), lane, kf);
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             float acc = 0.f;
@@ -437,7 +456,7 @@ struct SimtConsumer {
       for (int u = 0; u < 4; ++u) {
         if (!valid[u]) continue;
         float vf[E];
-        load_row(reinterpret_cast<const T *>(vs + Geom::row_off(t0 + u)), lane, vf);
+        load_row(reinterpret_cast<const T *>(vs + Geom::row_off_v(t0 + u)), lane, vf);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -528,8 +547,8 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   using Geom = typename C::Geom;
   using S = PartialSmem<C>;
   constexpr int D = C::D, G = C::G, NS = Geom::kStages;
-  constexpr int RB = D * (int)sizeof(typename C::Elem);
-  constexpr int TB = Geom::kTileBytes;
+  constexpr int RBK = C::kRowBytesK, RBV = C::kRowBytesV;  // bytes of a K row, a V row
+  constexpr int TBK = Geom::kTileBytesK;
   constexpr int R = Geom::kRowsPerCopy;
   constexpr int CW = C::kWarps;  // consumer warps; warp CW is the producer
 
@@ -631,11 +650,11 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
       const int r_lo = i0 > key0 ? i0 - key0 : 0;
       const int r_hi = len - key0 < kKeyTile ? len - key0 : kKeyTile;
       unsigned char *kdst = ring + s * Geom::kStageBytes;
-      unsigned char *vdst = kdst + TB;
+      unsigned char *vdst = kdst + TBK;
       if (lane == 0) {
         stage_skip[s] = ok ? 0 : 1;
         if (!ok) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
-        mbar_arrive_expect_tx(&full_bar[s], ok ? (uint32_t)(2 * (r_hi - r_lo) * RB) : 0u);
+        mbar_arrive_expect_tx(&full_bar[s], ok ? (uint32_t)((r_hi - r_lo) * (RBK + RBV)) : 0u);
       }
       __syncwarp();
       // one copy per group of R rows (clipped to the valid rows); lane i copies
@@ -645,10 +664,12 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
       if (ok && grp < kKeyTile / R && g_lo < g_hi) {
         const size_t grow = ((size_t)page * a.num_kv_heads + g) * a.page_size +
                             (size_t)(key0 % a.page_size) + g_lo;
+        const bool is_k = lane < 16;
+        const int rb = is_k ? RBK : RBV;
         const unsigned char *src =
-            static_cast<const unsigned char *>(lane < 16 ? a.k_pool : a.v_pool) + grow * RB;
-        bulk_g2s((lane < 16 ? kdst : vdst) + Geom::row_off(g_lo), src,
-                 (uint32_t)((g_hi - g_lo) * RB), &full_bar[s]);
+            static_cast<const unsigned char *>(is_k ? a.k_pool : a.v_pool) + grow * rb;
+        bulk_g2s(is_k ? kdst + Geom::row_off_k(g_lo) : vdst + Geom::row_off_v(g_lo), src,
+                 (uint32_t)((g_hi - g_lo) * rb), &full_bar[s]);
       }
       issued = j + 1;
     }
@@ -679,7 +700,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
         break;
       }
       const unsigned char *kst = ring + s * Geom::kStageBytes;
-      cons.tile(kst, kst + TB, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane, j);
+      cons.tile(kst, kst + TBK, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane, j);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }

@@ -47,15 +47,15 @@ int sm_count(int *out) {
   return PSKV_OK;
 }
 
-// CTA slots of the partial kernel serving (dtype, head_dim, group): SMs x CTAs per SM.
-int partial_slots(int kv_dtype, int head_dim, int group, int *slots) {
+// CTA slots of the partial kernel serving (dtype, head_dim, group, format): SMs x CTAs per SM.
+int partial_slots(int kv_dtype, int head_dim, int group, int format, int *slots) {
   int n_sm = 0, rc = sm_count(&n_sm);
   if (rc) return rc;
-  const int kernel = pick_kernel(kv_dtype, head_dim, group);
+  const int kernel = pick_kernel(kv_dtype, head_dim, group, format);
   int per = 0;
   cudaError_t e;
   if (kernel == kKernelMma)
-    e = occupancy_partial_mma(head_dim, group, &per);
+    e = occupancy_partial_mma(head_dim, group, format == PSKV_FORMAT_FOLDED, &per);
   else if (kernel == kKernelSimt && kv_dtype == PSKV_DTYPE_F32)
     e = occupancy_partial_simt_f32(head_dim, group, &per);
   else if (kernel == kKernelSimt)
@@ -95,8 +95,9 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   if (num_q_heads % d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
   if (d.num_kv_heads > 65535) return PSKV_ERR_UNSUPPORTED;
   const int group = num_q_heads / d.num_kv_heads;
-  const int kernel = pick_kernel(d.kv_dtype, d.head_dim_k, group);
+  const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
   if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
+  const bool folded = d.format == PSKV_FORMAT_FOLDED;
   int rc = check_lengths(layout, batch, table_stride, seq_lens_host);
   if (rc) return rc;
   int mgroup = 0;
@@ -105,7 +106,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int P = num_splits;
   if (P == 0) {
     int slots = 0;
-    if ((rc = partial_slots(d.kv_dtype, d.head_dim_k, group, &slots))) return rc;
+    if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, &slots))) return rc;
     P = plan_splits(slots, batch, d.num_kv_heads, seq_lens_host);
   }
   WorkspacePlan w;
@@ -143,11 +144,11 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (kernel == kKernelMma)
-    e = launch_partial_mma(a, d.head_dim_k, group, grid, s);
+    e = launch_partial_mma(a, d.head_dim_v, group, folded, grid, s);
   else if (d.kv_dtype == PSKV_DTYPE_F32)
-    e = launch_partial_simt_f32(a, d.head_dim_k, group, grid, s);
+    e = launch_partial_simt_f32(a, d.head_dim_v, group, grid, s);
   else
-    e = launch_partial_simt_bf16(a, d.head_dim_k, group, grid, s);
+    e = launch_partial_simt_bf16(a, d.head_dim_v, group, grid, s);
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (opts && opts->partial_end) {
@@ -190,7 +191,8 @@ int paged_kv_layout_create(const pskv_layout_desc *desc, pskv_layout **out) {
   if (!l) return PSKV_ERR_INVALID_ARG;
   l->d = *desc;
   l->elem_size = desc->kv_dtype == PSKV_DTYPE_BF16 ? 2 : 4;
-  l->row_bytes = desc->head_dim_k * l->elem_size;
+  l->k_row_bytes = desc->head_dim_k * l->elem_size;
+  l->v_row_bytes = desc->head_dim_v * l->elem_size;
   *out = l;
   return PSKV_OK;
 }
@@ -231,7 +233,8 @@ int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_n
   a.num_pages = layout->d.num_pages;
   a.page_size = layout->d.page_size;
   a.num_kv_heads = layout->d.num_kv_heads;
-  a.row_bytes = layout->row_bytes;
+  a.k_row_bytes = layout->k_row_bytes;
+  a.v_row_bytes = layout->v_row_bytes;
   a.status = layout->d.status;
   const cudaError_t e = launch_append(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -359,8 +362,8 @@ int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_hea
     return PSKV_ERR_INVALID_ARG;
   if (num_q_heads % layout->d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
   int slots = 0;
-  const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_k,
-                               num_q_heads / layout->d.num_kv_heads, &slots);
+  const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_v,
+                               num_q_heads / layout->d.num_kv_heads, layout->d.format, &slots);
   if (rc) return rc;
   *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host);
   return PSKV_OK;

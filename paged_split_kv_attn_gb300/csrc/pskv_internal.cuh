@@ -79,18 +79,19 @@ struct AppendArgs {
   long long num_pages;
   int page_size;
   int num_kv_heads;
-  int row_bytes;  // head_dim * element size, a multiple of 16
+  int k_row_bytes;  // head_dim_k * element size, a multiple of 16
+  int v_row_bytes;  // head_dim_v * element size, a multiple of 16
   int32_t *status;
 };
 
 // Host-side launchers (one per kernel family).  They return a CUDA error code.
-cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, dim3 grid,
-                               cudaStream_t s);
+cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, bool folded,
+                               dim3 grid, cudaStream_t s);
 cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                     cudaStream_t s);
 cudaError_t launch_partial_simt_bf16(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                      cudaStream_t s);
-cudaError_t occupancy_partial_mma(int head_dim, int group, int *ctas);
+cudaError_t occupancy_partial_mma(int head_dim, int group, bool folded, int *ctas);
 cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas);
 cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);

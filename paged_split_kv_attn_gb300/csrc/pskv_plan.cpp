@@ -14,17 +14,19 @@ int check_layout_desc(const pskv_layout_desc *d) {
     return PSKV_ERR_INVALID_ARG;
   if (d->page_size % PSKV_KEY_TILE != 0) return PSKV_ERR_INVALID_ARG;
   if (d->kv_dtype != PSKV_DTYPE_F32 && d->kv_dtype != PSKV_DTYPE_BF16) return PSKV_ERR_INVALID_ARG;
-  if (d->format == PSKV_FORMAT_FOLDED) return PSKV_ERR_UNSUPPORTED;
-  if (d->format != PSKV_FORMAT_SPLIT) return PSKV_ERR_INVALID_ARG;
-  if (d->head_dim_k != d->head_dim_v) return PSKV_ERR_UNSUPPORTED;
-  if (d->head_dim_k != 256 && d->head_dim_k != 512) return PSKV_ERR_UNSUPPORTED;
+  if (d->format != PSKV_FORMAT_SPLIT && d->format != PSKV_FORMAT_FOLDED) return PSKV_ERR_INVALID_ARG;
+  if (d->head_dim_v != 256 && d->head_dim_v != 512) return PSKV_ERR_UNSUPPORTED;
+  if (d->format == PSKV_FORMAT_SPLIT && d->head_dim_k != d->head_dim_v) return PSKV_ERR_UNSUPPORTED;
+  if (d->format == PSKV_FORMAT_FOLDED &&
+      (d->head_dim_k * 4 != d->head_dim_v || d->kv_dtype != PSKV_DTYPE_BF16))
+    return PSKV_ERR_UNSUPPORTED;
   if (!aligned16(d->k_pool) || !aligned16(d->v_pool)) return PSKV_ERR_INVALID_ARG;
   if (d->status && (reinterpret_cast<uintptr_t>(d->status) & 3u)) return PSKV_ERR_INVALID_ARG;
   // every element index of a region must fit in size_t and every row index in int64
   size_t rows, elems;
   if (__builtin_mul_overflow((size_t)d->num_pages, (size_t)d->num_kv_heads, &rows) ||
       __builtin_mul_overflow(rows, (size_t)d->page_size, &rows) ||
-      __builtin_mul_overflow(rows, (size_t)d->head_dim_k * 4, &elems))
+      __builtin_mul_overflow(rows, (size_t)d->head_dim_v * 4, &elems))
     return PSKV_ERR_OVERFLOW;
   if (d->num_pages > 0x7fffffffLL) return PSKV_ERR_UNSUPPORTED;  // page ids are int32
   return PSKV_OK;
@@ -103,10 +105,11 @@ int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride
   return PSKV_OK;
 }
 
-int pick_kernel(int kv_dtype, int head_dim, int group) {
+int pick_kernel(int kv_dtype, int head_dim, int group, int format) {
   const bool mma_group = group == 1 || group == 2 || group == 4 || group == 8;
   if (kv_dtype == PSKV_DTYPE_BF16 && mma_group && (head_dim == 256 || head_dim == 512))
     return kKernelMma;
+  if (format == PSKV_FORMAT_FOLDED) return -1;  // folded pools run on the tensor-core consumer only
   const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8 ||
                     (group == 16 && head_dim == 256);
   if ((head_dim == 256 || head_dim == 512) && g_ok) return kKernelSimt;

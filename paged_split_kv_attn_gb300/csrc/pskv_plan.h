@@ -11,8 +11,9 @@
 
 struct pskv_layout {
   pskv_layout_desc d;
-  int elem_size;  // bytes per element
-  int row_bytes;  // bytes of one key (or value) row of one head
+  int elem_size;    // bytes per element
+  int k_row_bytes;  // bytes of one stored key row of one head
+  int v_row_bytes;  // bytes of one value row of one head
 };
 
 namespace pskv {
@@ -43,8 +44,8 @@ int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *s
 int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride, int32_t batch,
                       const int32_t *row_of, const int32_t *pos_of, const int32_t *pages_of_row);
 
-// Which partial kernel family serves (dtype, head_dim, group); -1 if none.
+// Which partial kernel family serves (dtype, head_dim_v, group, format); -1 if none.
 enum { kKernelMma = 0, kKernelSimt = 1 };
-int pick_kernel(int kv_dtype, int head_dim, int group);
+int pick_kernel(int kv_dtype, int head_dim, int group, int format = PSKV_FORMAT_SPLIT);
 
 }  // namespace pskv

@@ -37,7 +37,7 @@ class DevCase:
         self.tables = i32(case.page_tables)
         self.lens = i32(case.seq_lens)
         self.status = torch.zeros(4, dtype=torch.int32, device="cuda")
-        self.layout = pskv.paged_kv_layout_create(self.k_pool, self.v_pool, self.status)
+        self.layout = pskv.paged_kv_layout_create(self.k_pool, self.v_pool, self.status)  # folded if K is narrower
         self.first_pos = None if case.first_pos is None else i32(case.first_pos)
         self.window_lo = None if case.window_lo is None else i32(case.window_lo)
 

@@ -38,6 +38,13 @@ int main() {
   e.k_pool = fake_k + 4;
   CHECK(check_layout_desc(&e) == PSKV_ERR_INVALID_ARG);
   CHECK(check_layout_desc(nullptr) == PSKV_ERR_INVALID_ARG);
+  e = d;
+  e.format = PSKV_FORMAT_FOLDED;
+  CHECK(check_layout_desc(&e) == PSKV_ERR_UNSUPPORTED);  // folded needs head_dim_k = head_dim_v / 4
+  e.head_dim_k = 128;
+  CHECK(check_layout_desc(&e) == PSKV_OK);
+  e.kv_dtype = PSKV_DTYPE_F32;
+  CHECK(check_layout_desc(&e) == PSKV_ERR_UNSUPPORTED);
 
   WorkspacePlan w;
   CHECK(plan_workspace(1, 32, 512, 32, 16, &w) == PSKV_OK);
@@ -46,7 +53,7 @@ int main() {
   CHECK(plan_workspace((int64_t)1 << 30, (int64_t)1 << 30, 512, 1024, 16, &w) == PSKV_ERR_OVERFLOW);
   CHECK(plan_workspace(0, 32, 512, 32, 16, &w) == PSKV_ERR_INVALID_ARG);
 
-  pskv_layout lay{d, 2, 1024};
+  pskv_layout lay{d, 2, 1024, 1024};
   std::vector<int32_t> lens = {1, 256 * 4, 7};
   CHECK(check_lengths(&lay, 3, 4, lens.data()) == PSKV_OK);
   lens[1] = 256 * 4 + 1;
@@ -81,6 +88,8 @@ int main() {
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 16) == kKernelSimt);
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 512, 16) == -1);
   CHECK(pick_kernel(PSKV_DTYPE_BF16, 128, 8) == -1);
+  CHECK(pick_kernel(PSKV_DTYPE_BF16, 512, 8, PSKV_FORMAT_FOLDED) == kKernelMma);
+  CHECK(pick_kernel(PSKV_DTYPE_BF16, 256, 16, PSKV_FORMAT_FOLDED) == -1);
   std::puts("plan driver ok");
   return 0;
 }

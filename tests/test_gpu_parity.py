@@ -305,3 +305,64 @@ def test_bad_page_id_is_flagged_not_read():
     torch.cuda.synchronize()
     assert dc.faults() & pskv.PSKV_FAULT_BAD_PAGE
     assert torch.all(torch.isfinite(out))
+
+
+# ---- the folded format (K keeps the rotated quarter, V in full) ------------------------
+
+def _split_twin_dev(case):
+    """The split pool a folded pool stands for: K = [stored K, V's remaining columns]."""
+    import dataclasses
+    dk = case.k_pool.shape[3]
+    k_full = np.ascontiguousarray(np.concatenate([case.k_pool, case.v_pool[..., dk:]], axis=3))
+    return dataclasses.replace(case, k_pool=k_full)
+
+
+@pytest.mark.parametrize("context", [10602, 40002])
+def test_folded_decode(context):
+    case = W.folded_case(context, seed=51)
+    dc = DevCase(case)
+    ref = ref_direct(case)
+    for splits in (0, 8, 64):
+        check_decode(dc, ref, num_splits=splits)
+
+
+def test_folded_equals_its_split_twin_bit_for_bit():
+    case = W.make_paged_case(52, [5000, 333, 1], k_dims=128, **W.GLOBAL_SHAPE)
+    twin = _split_twin_dev(case)
+    a, b = DevCase(case), DevCase(twin)
+    for splits in (0, 7):
+        oa = a.decode(num_splits=splits)
+        ob = b.decode(num_splits=splits)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(256, 32, 16), (256, 32, 4), (512, 16, 4)])
+def test_folded_other_shapes_and_window(d, hq, hkv):
+    base = W.make_paged_case(53, [700, 64, 1, 300], num_q_heads=hq, num_kv_heads=hkv,
+                             head_dim=d, page_size=64, k_dims=d // 4)
+    for case in (base, W.with_window(base, 256, first_pos=[0, 10, 3, 1000])):
+        dc = DevCase(case)
+        ref = ref_direct(case)
+        for splits in (0, 3):
+            check_decode(dc, ref, num_splits=splits)
+
+
+def test_folded_append_is_bit_exact():
+    case = W.make_paged_case(54, [40, 300], num_q_heads=8, num_kv_heads=2, head_dim=512,
+                             page_size=256, k_dims=128, keep_dense=True)
+    exp_k, exp_v = np.zeros_like(case.k_pool), np.zeros_like(case.v_pool)
+    rows = [(b, i) for b in range(case.batch) for i in range(int(case.seq_lens[b]))]
+    kn = np.stack([case.dense_k[b][i] for b, i in rows])
+    vn = np.stack([case.dense_v[b][i] for b, i in rows])
+    row_of, pos_of = [r[0] for r in rows], [r[1] for r in rows]
+    oracle.append_rows(exp_k, exp_v, kn, vn, row_of, pos_of, case.page_tables, case.pages_of_row)
+    k_pool = torch.zeros_like(to_dev(case.k_pool, "bf16"))
+    v_pool = torch.zeros_like(to_dev(case.v_pool, "bf16"))
+    layout = pskv.paged_kv_layout_create(k_pool, v_pool)
+    assert layout.desc.format == pskv.PSKV_FORMAT_FOLDED
+    pskv.kv_append_rows(layout, to_dev(kn, "bf16"), to_dev(vn, "bf16"), i32(row_of), i32(pos_of),
+                        i32(case.page_tables), i32(case.pages_of_row))
+    torch.cuda.synchronize()
+    assert k_pool.cpu().view(torch.int16).numpy().tobytes() == exp_k.view(np.int16).tobytes()
+    assert v_pool.cpu().view(torch.int16).numpy().tobytes() == exp_v.view(np.int16).tobytes()
