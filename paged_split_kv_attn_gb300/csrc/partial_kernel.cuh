@@ -49,7 +49,8 @@ namespace pskv {
 // (the stage count is a multiple of kWarps), so every stage is always consumed
 // by the same warp, in order: a consumer never waits on a phase more than one
 // ahead of its barrier's current phase.  Rows are copied in groups of kRows.
-template <int kRowBytesK, int kRowBytesV, int kRows, int kWarps>
+// kFixedStages > 0 sets the stage count directly (the budget then does not apply).
+template <int kRowBytesK, int kRowBytesV, int kRows, int kWarps, int kFixedStages = 0>
 struct RingGeom {
   static constexpr int kRowsPerCopy = kRows;
   static constexpr int kGroupStrideK = kRows * kRowBytesK + 16;
@@ -61,7 +62,7 @@ struct RingGeom {
   static constexpr int kPerWarpMax = 8 / kWarps > 0 ? 8 / kWarps : 1;
   static constexpr int kPerWarp =
       kPerWarpFit < 1 ? 1 : (kPerWarpFit > kPerWarpMax ? kPerWarpMax : kPerWarpFit);
-  static constexpr int kStages = kWarps * kPerWarp;
+  static constexpr int kStages = kFixedStages > 0 ? kFixedStages : kWarps * kPerWarp;
   static constexpr int kRingBytes = kStages * kStageBytes;
   // byte offset of key row t (0..15) in a K tile and in a V tile
   static __device__ __forceinline__ int row_off_k(int t) {
@@ -92,6 +93,14 @@ struct RingGeom {
 // -------------------------------------------------------------------------------------------
 #ifndef PSKV_MMA_WARPS
 #define PSKV_MMA_WARPS 4
+#endif
+
+// Stages per CTA of the tensor-core consumer.  Three stages per CTA, with as
+// many CTAs per SM as shared memory allows (2 for split hd512 rows, 3 for
+// folded ones), measured best on GB300: more stages per CTA left fewer CTAs
+// to overlap their start-up and tail, fewer left too few bytes in flight.
+#ifndef PSKV_MMA_STAGES
+#define PSKV_MMA_STAGES 3
 #endif
 
 // bar.sync on a named barrier shared by the `n` threads of the consumer warps.
@@ -132,7 +141,7 @@ struct MmaConsumer {
   static constexpr int kExtraSmem = 2 * kWarps * 32 * 16;  // double-buffered score exchange
   static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;  // bytes of one stored K row
   static constexpr int kRowBytesV = D * 2;
-  using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1>;
+  using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1, PSKV_MMA_STAGES>;
   static constexpr int RBK = kRowBytesK, RBV = kRowBytesV;
   static constexpr int GSK = Geom::kGroupStrideK;  // bytes of a padded pair of K rows
   static constexpr int GSV = Geom::kGroupStrideV;  // bytes of a padded pair of V rows
@@ -171,8 +180,9 @@ struct MmaConsumer {
   __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
                        bool skip, int lane, int j_tile) {
     const int mi = lane >> 3, rr = lane & 7;
-    // ---- partial scores over this warp's d range, two accumulator chains for latency
+    // ---- partial scores over this warp's d range, several accumulator chains for latency
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
     // A rows m = (mi&1)*8 + rr hold key 2*rr + (mi&1): pair rr, row (mi&1) of the pair
     const bool from_v = kFolded && warp > 0;  // a folded key's columns past D/4 live in V
     const uint32_t kaddr =
@@ -180,16 +190,25 @@ struct MmaConsumer {
                : smem_u32(ks) + rr * GSK + (mi & 1) * RBK + (mi >> 1) * 16 +
                      (kFolded ? 0 : warp * DW * 2);
 #pragma unroll
-    for (int k = 0; k < KS; k += 2) {
+    for (int k = 0; k < KS; k += 4) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4(kaddr + k * 32, a0, a1, a2, a3);
       mma_bf16(sa, a0, a1, a2, a3, qf[k][0], qf[k][1]);
       ldsm_x4(kaddr + (k + 1) * 32, a0, a1, a2, a3);
       mma_bf16(sb, a0, a1, a2, a3, qf[k + 1][0], qf[k + 1][1]);
+      if (k + 2 < KS) {
+        ldsm_x4(kaddr + (k + 2) * 32, a0, a1, a2, a3);
+        mma_bf16(sc, a0, a1, a2, a3, qf[k + 2][0], qf[k + 2][1]);
+        ldsm_x4(kaddr + (k + 3) * 32, a0, a1, a2, a3);
+        mma_bf16(sd, a0, a1, a2, a3, qf[k + 3][0], qf[k + 3][1]);
+      }
     }
     // ---- sum the four warps' partials (fixed order: every warp gets the same bits)
     float4 *slot = xchg + (j_tile & 1) * kWarps * 32;
-    slot[warp * 32 + lane] = make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
+    slot[warp * 32 + lane] = make_float4((sa[0] + sb[0]) + (sc[0] + sd[0]),
+                                         (sa[1] + sb[1]) + (sc[1] + sd[1]),
+                                         (sa[2] + sb[2]) + (sc[2] + sd[2]),
+                                         (sa[3] + sb[3]) + (sc[3] + sd[3]));
     consumers_sync(kWarps * 32);
     float4 st = slot[lane];
 #pragma unroll
@@ -209,24 +228,25 @@ struct MmaConsumer {
     const float s10 = vB ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, head 2c
     const float s11 = vB ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, head 2c+1
 
-    // ---- online softmax update (max over the 16 keys: lanes sharing c)
+    // ---- online softmax update.  The reference max m only moves when some score
+    // exceeds it by more than kSlack (log2 units): below that, exp2(s - m) <= 2^8
+    // is exact in float and in the hi+lo weights, and (m, l, o) stays an exact
+    // state for any reference m, so most tiles skip the cross-lane max and the
+    // rescale.  The decision depends only on the scores, which every warp holds
+    // identically, so all warps take the same branch.
+    constexpr float kSlack = 8.f;
     float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+    if (__any_sync(0xffffffffu, x0 > m0 + kSlack || x1 > m1 + kSlack)) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float u0 = (n0 == -CUDART_INF_F) ? 0.f : n0;  // nothing attended yet: all weights 0
-    const float u1 = (n1 == -CUDART_INF_F) ? 0.f : n1;
-    const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
-    const float p00 = exp2f(s00 - u0), p01 = exp2f(s01 - u1);
-    const float p10 = exp2f(s10 - u0), p11 = exp2f(s11 - u1);
-    l0 = l0 * al0 + (p00 + p10);
-    l1 = l1 * al1 + (p01 + p11);
-    m0 = n0;
-    m1 = n1;
-    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+      for (int off = 4; off < 32; off <<= 1) {  // max over the 16 keys: lanes sharing c
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float al0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - n0);
+      const float al1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - n1);
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int j = 0; j < KS; ++j) {
         o[j][0] *= al0;
@@ -234,7 +254,15 @@ struct MmaConsumer {
         o[j][2] *= al0;
         o[j][3] *= al1;
       }
+      m0 = n0;
+      m1 = n1;
     }
+    const float u0 = (m0 == -CUDART_INF_F) ? 0.f : m0;  // nothing attended yet: all weights 0
+    const float u1 = (m1 == -CUDART_INF_F) ? 0.f : m1;
+    const float p00 = exp2f(s00 - u0), p01 = exp2f(s01 - u1);
+    const float p10 = exp2f(s10 - u0), p11 = exp2f(s11 - u1);
+    l0 += p00 + p10;
+    l1 += p01 + p11;
 
     // ---- P^T fragments (hi + lo bf16 pairs), transposed in registers
     const uint32_t hA = pack_bf16x2(p00, p01), hB = pack_bf16x2(p10, p11);
