@@ -74,6 +74,7 @@ def _load():
         lib.orc_append_rows.argtypes = [P, P, P, P, P, P, P, I, P, I, P, I]
         lib.orc_decode_direct.argtypes = [P, P, P, I, P, P, P, I, I, D, P]
         lib.orc_decode_online.argtypes = [P, P, P, I, P, P, P, I, I, D, I, I, I, P]
+        lib.orc_decode_multirow_direct.argtypes = [P, P, P, I, P, I, I, I, D, P]
         lib.orc_partial_scratch_bytes.argtypes = [I64, I64, I64, I64, P, P, P, P]
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -218,6 +219,20 @@ def decode_direct(q, k_pool, v_pool, page_tables, seq_lens, scale, first_pos=Non
     _check(_load().orc_decode_direct(ctypes.byref(pool), _ptr(q), _ptr(tables), tables.shape[1],
                                      _ptr(lens), _ptr(fp), _ptr(wl), q.shape[0], q.shape[1],
                                      scale, _ptr(out)), "decode_direct")
+    return out
+
+
+def decode_multirow_direct(q, k_pool, v_pool, page_tables, seq_lens, scale):
+    """q [batch, tokens, num_q_heads, key width] -> out [batch, tokens, num_q_heads, dv]:
+    token t of row b sits at key position len - tokens + t and attends causally."""
+    pool, keep = _pool(k_pool, v_pool)
+    q, _ = _data(q)
+    tables, lens = _c(page_tables, np.int32), _c(seq_lens, np.int32)
+    out = np.zeros((q.shape[0], q.shape[1], q.shape[2], pool.head_dim_v), np.float64)
+    _check(_load().orc_decode_multirow_direct(ctypes.byref(pool), _ptr(q), _ptr(tables),
+                                              tables.shape[1], _ptr(lens), q.shape[0], q.shape[1],
+                                              q.shape[2], scale, _ptr(out)),
+           "decode_multirow_direct")
     return out
 
 

@@ -378,29 +378,37 @@ static int decode_args_ok(const orc_pool *pool, const void *q, const int32_t *pa
   return ORC_OK;
 }
 
-int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
-                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
-                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
-                      double *out) {
+/* Direct decode of T query tokens per row: token t of row b (query row
+ * (b*T + t)) sits at key position len - T + t and attends the keys up to and
+ * including its own position, from the window bound if any. */
+static int decode_direct_tokens(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                                int table_stride, const int32_t *seq_lens,
+                                const int32_t *first_pos, const int32_t *window_lo, int batch,
+                                int num_tokens, int num_q_heads, double scale, double *out) {
   int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo,
                           batch, num_q_heads, out);
   if (rc) return rc;
+  if (num_tokens < 1) return ORC_ERR_INVALID;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < num_tokens) return ORC_ERR_INVALID;
   const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
   const int G = num_q_heads / pool->num_kv_heads; /* head h reads kv head h / G */
   int rc_all = ORC_OK;
-  const int jobs = batch * num_q_heads;
+  const int T = num_tokens;
+  const int jobs = batch * T * num_q_heads;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int job = 0; job < jobs; ++job) {
-    const int b = job / num_q_heads, h = job % num_q_heads, g = h / G, len = seq_lens[b];
+    const int h = job % num_q_heads, bt = job / num_q_heads, b = bt / T, t = bt % T, g = h / G;
+    const int len = seq_lens[b] - T + t + 1; /* keys this token sees */
     const int i0 = first_key(first_pos, window_lo, b, len);
     double *qd = (double *)malloc(sizeof(double) * (size_t)kw);
     double *s = (double *)malloc(sizeof(double) * (size_t)(len - i0));
-    double *dst = out + ((size_t)b * num_q_heads + h) * dv;
+    double *dst = out + ((size_t)bt * num_q_heads + h) * dv;
     if (!qd || !s) {
 #pragma omp critical
       rc_all = ORC_ERR_INVALID;
     } else {
-      for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)b * num_q_heads + h) * kw + d);
+      for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)bt * num_q_heads + h) * kw + d);
       /* s_i = scale * q . k_i over the attended keys */
       double mx = -INFINITY;
       for (int i = i0; i < len; ++i) {
@@ -428,6 +436,21 @@ int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_t
     free(s);
   }
   return rc_all;
+}
+
+int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                      int table_stride, const int32_t *seq_lens, const int32_t *first_pos,
+                      const int32_t *window_lo, int batch, int num_q_heads, double scale,
+                      double *out) {
+  return decode_direct_tokens(pool, q, page_tables, table_stride, seq_lens, first_pos, window_lo,
+                              batch, 1, num_q_heads, scale, out);
+}
+
+int orc_decode_multirow_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                               int table_stride, const int32_t *seq_lens, int batch,
+                               int num_tokens, int num_q_heads, double scale, double *out) {
+  return decode_direct_tokens(pool, q, page_tables, table_stride, seq_lens, NULL, NULL, batch,
+                              num_tokens, num_q_heads, scale, out);
 }
 
 int orc_decode_online(const orc_pool *pool, const void *q, const int32_t *page_tables,

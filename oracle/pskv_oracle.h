@@ -136,6 +136,17 @@ int orc_decode_direct(const orc_pool *pool, const void *q, const int32_t *page_t
                       const int32_t *window_lo, int batch, int num_q_heads, double scale,
                       double *out);
 
+/* Direct fp64 decode of num_tokens query tokens per row (a verify window:
+ * the row's last num_tokens key positions are its query tokens; TensorFold
+ * #1619 reads such windows and tree-attention rows through the page table).
+ * q is [batch][num_tokens][num_q_heads][key width], out the same with head_dim_v;
+ * token t of row b sits at key position seq_lens[b] - num_tokens + t and
+ * attends keys [0, seq_lens[b] - num_tokens + t] (causal).  num_tokens = 1 is
+ * orc_decode_direct without a window. */
+int orc_decode_multirow_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                               int table_stride, const int32_t *seq_lens, int batch,
+                               int num_tokens, int num_q_heads, double scale, double *out);
+
 /* Online fp64 decode: the attended keys of a row are cut into chunks of
  * chunk_tokens (aligned to key index 0), the chunks into num_splits
  * contiguous partitions of ceil(n_chunks / num_splits) chunks (trailing

@@ -425,3 +425,50 @@ def test_folded_stored_columns_reach_the_score():
     out = run_direct(case)
     moved = np.abs(out - base).max(axis=(0, 1))
     assert moved[1] > 0 and np.all(moved[np.arange(16) != 1] == 0)
+
+
+# ---- multi-row decode (verify windows) ----------------------------------------------
+
+@pytest.mark.parametrize("tokens", [1, 2, 3, 8])
+def test_multirow_token_equals_single_decode_of_the_truncated_row(tokens):
+    """Token t of a T-token window is the single-token decode of the row cut at
+    its own position (the same keys, the same order: bit for bit)."""
+    import dataclasses
+    case = W.make_paged_case(61, [40, 9, 300], num_q_heads=4, num_kv_heads=2, head_dim=16,
+                             page_size=16, dtype="f32")
+    rng = np.random.default_rng(tokens)
+    q = rng.standard_normal((case.batch, tokens, 4, 16)).astype(np.float32)
+    out = oracle.decode_multirow_direct(q, case.k_pool, case.v_pool, case.page_tables,
+                                        case.seq_lens, case.scale)
+    for t in range(tokens):
+        lens = case.seq_lens - tokens + t + 1
+        single = dataclasses.replace(case, q=np.ascontiguousarray(q[:, t]), seq_lens=lens)
+        assert np.array_equal(out[:, t], run_direct(single))
+
+
+def test_multirow_matches_causal_brute_force():
+    case = W.make_paged_case(62, [33, 70], num_q_heads=4, num_kv_heads=1, head_dim=8, page_size=8,
+                             dtype="bf16")
+    T = 4
+    rng = np.random.default_rng(0)
+    q = W.bf16_bits(rng.standard_normal((case.batch, T, 4, 8)).astype(np.float32))
+    out = oracle.decode_multirow_direct(q, case.k_pool, case.v_pool, case.page_tables,
+                                        case.seq_lens, case.scale)
+    qf = W.bf16_to_f32(q).astype(np.float64)
+    for b in range(case.batch):
+        K, V = dense_f64(case, b)
+        L = int(case.seq_lens[b])
+        for t in range(T):
+            for h in range(4):
+                s_ = case.scale * (K[:, 0, :] @ qf[b, t, h])
+                s_[L - T + t + 1:] = -np.inf  # causal: keys after the token's own position
+                ref = softmax(s_) @ V[:, 0, :]
+                np.testing.assert_allclose(out[b, t, h], ref, rtol=0, atol=1e-12)
+
+
+def test_multirow_refuses_rows_shorter_than_the_window():
+    case = W.make_paged_case(63, [2], num_q_heads=2, num_kv_heads=1, head_dim=8, page_size=8)
+    q = np.zeros((1, 3, 2, 8), np.uint16)
+    with pytest.raises(oracle.OracleError):
+        oracle.decode_multirow_direct(q, case.k_pool, case.v_pool, case.page_tables,
+                                      case.seq_lens, case.scale)
