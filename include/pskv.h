@@ -69,7 +69,7 @@ typedef struct CUevent_st *pskv_event_t;
 /* ---- device fault bits, ORed into status[0] of the layout's status word ------ */
 #define PSKV_FAULT_BAD_PAGE 1u      /* a table entry outside [0, num_pages): that tile or row skipped */
 #define PSKV_FAULT_PAST_PAGES 2u    /* an append past its row's pages: that row skipped */
-#define PSKV_FAULT_BAD_LENGTH 4u    /* a device length outside [1, table_stride * page_size]: clamped */
+#define PSKV_FAULT_BAD_LENGTH 4u    /* a device length outside [tokens, table_stride * page_size]: clamped */
 #define PSKV_FAULT_WAIT_TIMEOUT 8u  /* a bounded wait on a copy expired: the partition was dropped */
 #define PSKV_FAULT_EMPTY_ROW 16u    /* a row had no attended key: its output was written as zeros */
 #define PSKV_FAULT_BAD_STATE 32u    /* merge input with m = -inf but l != 0, or a NaN m: treated as empty */
@@ -79,6 +79,7 @@ typedef struct CUevent_st *pskv_event_t;
 #define PSKV_AUTO_MAX_SPLITS 256   /* most partitions the automatic plan picks */
 #define PSKV_MERGE_GROUP 16        /* partials folded per level-1 group of the merge */
 #define PSKV_KEY_TILE 16           /* keys per kernel tile; partitions are whole tiles */
+#define PSKV_MAX_WINDOW_TOKENS 64  /* query tokens per row of decode_attn_multirow */
 
 /* Description of one paged KV pool.
  *
@@ -203,6 +204,33 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
                          const int32_t *seq_lens, const int32_t *first_pos,
                          const int32_t *window_lo, int32_t batch, int32_t num_q_heads,
                          float scale, int32_t num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, int32_t out_dtype,
+                         const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Multi-row split-KV decode: num_tokens query tokens per row, the row's last
+ * num_tokens keys (a verify window; TensorFold #1619, description "Reads" and
+ * the review thread: drafted verify windows and tree-attention rows read
+ * their keys through the page table).  Token t of row b sits at key
+ * seq_lens[b] - num_tokens + t and attends keys [0, seq_lens[b] - num_tokens + t]
+ * (causal inside the window).  As decode_attn_splitkv, except:
+ *   q           device [batch][num_tokens][num_q_heads][head_dim_v]
+ *   out         device [batch][num_tokens][num_q_heads][head_dim_v] of out_dtype
+ *   num_tokens  1..PSKV_MAX_WINDOW_TOKENS.  The window's query columns per KV
+ *               head (query heads per KV head x num_tokens) are served 8 per
+ *               CTA when they fit in 8, else 16 per CTA, the CTAs of one
+ *               partition reading the same keys (the later ones mostly from L2)
+ *   seq_lens    every length at least num_tokens
+ *   workspace   decode_attn_workspace_bytes(batch * num_tokens, num_q_heads, ...)
+ *               bytes; its partials are laid out as for batch * num_tokens rows
+ *               (row b * num_tokens + t)
+ * bf16 pools with 1/2/4/8 query heads per KV head only; no
+ * key window.  num_tokens = 1 gives decode_attn_splitkv's bits.
+ * Errors: INVALID_ARG (also a host length below num_tokens), UNSUPPORTED,
+ * WORKSPACE_TOO_SMALL, CUDA. */
+int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                         int32_t table_stride, const int32_t *seq_lens_host,
+                         const int32_t *seq_lens, int32_t batch, int32_t num_tokens,
+                         int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream);
 

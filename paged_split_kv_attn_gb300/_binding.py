@@ -39,11 +39,12 @@ PSKV_MAX_SPLITS = 1024
 PSKV_AUTO_MAX_SPLITS = 256
 PSKV_MERGE_GROUP = 16
 PSKV_KEY_TILE = 16
+PSKV_MAX_WINDOW_TOKENS = 64
 PSKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 # Every function the header declares, in the header's order.
 EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows",
-           "decode_attn_splitkv", "decode_attn_windowed", "merge_partials",
+           "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
            "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches", "pskv_version")
@@ -93,6 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.decode_attn_splitkv.argtypes = [P, P, P, I32, P, P, I32, I32, F, I32, P, SZ, P, I32, P, P]
     lib.decode_attn_windowed.argtypes = [P, P, P, I32, P, P, P, P, I32, I32, F, I32, P, SZ, P,
                                          I32, P, P]
+    lib.decode_attn_multirow.argtypes = [P, P, P, I32, P, P, I32, I32, I32, F, I32, P, SZ, P, I32,
+                                         P, P]
     lib.merge_partials.argtypes = [P, P, P, I32, I32, I32, P, I32, P, SZ, P, P, P]
     lib.decode_attn_workspace_bytes.argtypes = [I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.merge_partials_workspace_bytes.argtypes = [I32, I32, I32, ctypes.POINTER(SZ)]
@@ -299,6 +302,9 @@ def workspace(batch: int, num_q_heads: int, head_dim_v: int, num_splits: int = 0
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+_alloc_workspace = workspace
+
+
 def _decode(windowed: bool, layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,
             num_splits, workspace_t, out, out_dtype, merge_group, events, stream,
             first_pos=None, window_lo=None):
@@ -345,6 +351,35 @@ def decode_attn_windowed(layout: Layout, q, page_tables, seq_lens, seq_lens_host
     """Windowed split-KV decode; keys at positions below ``window_lo`` are masked."""
     return _decode(True, layout, q, page_tables, seq_lens, seq_lens_host, scale, num_splits,
                    workspace, out, out_dtype, merge_group, events, stream, first_pos, window_lo)
+
+
+def decode_attn_multirow(layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,
+                         num_splits: int = 0, workspace=None, out=None, out_dtype=None,
+                         merge_group: int = 0, events=None, stream=None) -> torch.Tensor:
+    """Multi-row decode of a verify window: ``q`` is [batch, tokens, num_q_heads,
+    head_dim]; token t of row b sits at key ``seq_lens[b] - tokens + t`` and
+    attends keys up to itself.  Returns ``out`` [batch, tokens, num_q_heads, head_dim]."""
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, tokens, num_q_heads, head_dim]")
+    batch, tokens, hq = q.shape[0], q.shape[1], q.shape[2]
+    dv = layout.desc.head_dim_v
+    if out is None:
+        out = torch.empty((batch, tokens, hq, dv), device=q.device,
+                          dtype=out_dtype or torch.bfloat16)
+    if workspace is None:
+        workspace = _alloc_workspace(batch * tokens, hq, dv, num_splits, q.device)
+    lens_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if len(lens_h) != batch:
+        raise ValueError("seq_lens_host must have one entry per row")
+    opts = _opts(merge_group, events)
+    _check(lib.decode_attn_multirow(
+        layout.handle, _dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
+        page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32), batch, tokens, hq,
+        float(scale), num_splits, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev(out, "out"), _dtype_code(out.dtype),
+        None if opts is None else ctypes.byref(opts), _stream(stream)), "decode_attn_multirow")
+    return out
 
 
 def decode_attn_splitkv_static(layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,

@@ -128,61 +128,85 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
 // K's norm weight folded into the query).  Warp 0's quarter of D is exactly the
 // stored K columns, so warp 0 reads its score operands from the K tile and
 // warps 1..3 read theirs from the V tile.
-template <int kD, int kG = 8, bool kFolded = false>
+template <int kD, int kG = 8, bool kFolded = false, int kNT = 1>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
   static constexpr int G = kG;
   static_assert(kG == 1 || kG == 2 || kG == 4 || kG == 8, "query heads per KV head");
+  // Query columns: kNT n-tiles of 8 per CTA.  Window column j (of tokens x G)
+  // serves query token j / G, head j % G of the KV group; CTA column block cb
+  // takes columns [cb * kCols, (cb + 1) * kCols).  Columns past tokens x G have
+  // zero queries and are never written.
+  static constexpr int NT = kNT;
+  static constexpr int kCols = 8 * kNT;
   static constexpr int kWarps = PSKV_MMA_WARPS;
   static constexpr bool kCooperative = true;   // every warp takes part in every tile
   static constexpr int DW = D / kWarps;        // head-dim columns per warp
   static constexpr int KS = DW / 16;           // k-steps of QK = m-tiles of PV per warp
-  static constexpr int kExtraSmem = 2 * kWarps * 32 * 16;  // double-buffered score exchange
+  static constexpr int CH = NT == 1 ? 4 : 2;   // score accumulator chains per n-tile
+  static constexpr int kExtraSmem = 2 * kWarps * NT * 32 * 16;  // double-buffered score exchange
   static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;  // bytes of one stored K row
   static constexpr int kRowBytesV = D * 2;
   using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1, PSKV_MMA_STAGES>;
   static constexpr int RBK = kRowBytesK, RBV = kRowBytesV;
   static constexpr int GSK = Geom::kGroupStrideK;  // bytes of a padded pair of K rows
   static constexpr int GSV = Geom::kGroupStrideV;  // bytes of a padded pair of V rows
-  static_assert(KS >= 2 && KS % 2 == 0, "two QK accumulator chains");
+  static_assert(KS % CH == 0, "k-steps divide among the accumulator chains");
   static_assert(!kFolded || DW == D / 4, "warp 0 must own exactly the stored K columns");
 
-  uint32_t qf[KS][2];  // Q^T B-fragments: (d = dw0 + 16k + 2c + {0,1} [+8], head r)
-  float o[KS][4];      // O^T accumulators: (d = dw0 + 16j + r [+8], heads 2c, 2c+1)
-  float m0, m1;        // running max (log2 units) of heads 2c, 2c+1, the same in every warp
-  float l0, l1;        // this lane's share of the running sums of heads 2c, 2c+1
+  uint32_t qf[NT][KS][2];  // Q^T B-fragments: (d = dw0 + 16k + 2c + {0,1} [+8], column 8nt + r)
+  float o[NT][KS][4];      // O^T accumulators: (d = dw0 + 16j + r [+8], columns 8nt + 2c, +1)
+  float m0[NT], m1[NT];    // reference max (log2 units) of columns 8nt + 2c, +1: the same in every warp
+  float l0[NT], l1[NT];    // this lane's share of the sums of those columns
+  int lim0[NT], lim1[NT];  // keys below lim are visible to those columns (causal in a window)
   float scale_log2;
-  float4 *xchg;        // [2][kWarps][32] partial scores
-  int r, c, warp;
+  float4 *xchg;            // [2][kWarps][NT][32] partial scores
+  int r, c, warp, tokens, cbase;
 
   static __device__ void prologue(const PartialArgs &, int, int, unsigned char *) {}
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra) {
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra,
+                       int len, int cb) {
     r = lane >> 2;
     c = lane & 3;
     warp = threadIdx.x >> 5;
+    tokens = a.num_tokens;
+    cbase = cb * kCols;
     scale_log2 = a.scale_log2;
     xchg = reinterpret_cast<float4 *>(extra);
-    const uint16_t *q = static_cast<const uint16_t *>(a.q) +
-                        ((size_t)b * a.num_q_heads + h0 + (r < G ? r : 0)) * D + warp * DW;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      qf[k][0] = r < G ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
-      qf[k][1] = r < G ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c) : 0u;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int jq = cbase + 8 * nt + r, tq = jq / G;  // the column this lane feeds as B operand
+      const bool real = tq < tokens;
+      const uint16_t *q =
+          static_cast<const uint16_t *>(a.q) +
+          (((size_t)b * tokens + (real ? tq : 0)) * a.num_q_heads + h0 + jq % G) * D + warp * DW;
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        qf[nt][k][0] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
+        qf[nt][k][1] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c) : 0u;
+      }
+      // token t of the row sits at key len - tokens + t and sees keys up to itself
+      const int j0 = cbase + 8 * nt + 2 * c, t0 = j0 / G, t1 = (j0 + 1) / G;
+      lim0[nt] = t0 < tokens ? len - tokens + t0 + 1 : 0;
+      lim1[nt] = t1 < tokens ? len - tokens + t1 + 1 : 0;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) o[nt][j][0] = o[nt][j][1] = o[nt][j][2] = o[nt][j][3] = 0.f;
+      m0[nt] = m1[nt] = -CUDART_INF_F;
+      l0[nt] = l1[nt] = 0.f;
     }
-#pragma unroll
-    for (int j = 0; j < KS; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    m0 = m1 = -CUDART_INF_F;
-    l0 = l1 = 0.f;
   }
 
   __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
                        bool skip, int lane, int j_tile) {
     const int mi = lane >> 3, rr = lane & 7;
-    // ---- partial scores over this warp's d range, several accumulator chains for latency
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- partial scores over this warp's d range; each K fragment feeds every n-tile
+    float acc[NT][CH][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) acc[nt][ch][0] = acc[nt][ch][1] = acc[nt][ch][2] = acc[nt][ch][3] = 0.f;
     // A rows m = (mi&1)*8 + rr hold key 2*rr + (mi&1): pair rr, row (mi&1) of the pair
     const bool from_v = kFolded && warp > 0;  // a folded key's columns past D/4 live in V
     const uint32_t kaddr =
@@ -190,88 +214,104 @@ struct MmaConsumer {
                : smem_u32(ks) + rr * GSK + (mi & 1) * RBK + (mi >> 1) * 16 +
                      (kFolded ? 0 : warp * DW * 2);
 #pragma unroll
-    for (int k = 0; k < KS; k += 4) {
+    for (int k = 0; k < KS; ++k) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4(kaddr + k * 32, a0, a1, a2, a3);
-      mma_bf16(sa, a0, a1, a2, a3, qf[k][0], qf[k][1]);
-      ldsm_x4(kaddr + (k + 1) * 32, a0, a1, a2, a3);
-      mma_bf16(sb, a0, a1, a2, a3, qf[k + 1][0], qf[k + 1][1]);
-      if (k + 2 < KS) {
-        ldsm_x4(kaddr + (k + 2) * 32, a0, a1, a2, a3);
-        mma_bf16(sc, a0, a1, a2, a3, qf[k + 2][0], qf[k + 2][1]);
-        ldsm_x4(kaddr + (k + 3) * 32, a0, a1, a2, a3);
-        mma_bf16(sd, a0, a1, a2, a3, qf[k + 3][0], qf[k + 3][1]);
-      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_bf16(acc[nt][k % CH], a0, a1, a2, a3, qf[nt][k][0], qf[nt][k][1]);
     }
     // ---- sum the four warps' partials (fixed order: every warp gets the same bits)
-    float4 *slot = xchg + (j_tile & 1) * kWarps * 32;
-    slot[warp * 32 + lane] = make_float4((sa[0] + sb[0]) + (sc[0] + sd[0]),
-                                         (sa[1] + sb[1]) + (sc[1] + sd[1]),
-                                         (sa[2] + sb[2]) + (sc[2] + sd[2]),
-                                         (sa[3] + sb[3]) + (sc[3] + sd[3]));
+    float4 *slot = xchg + (j_tile & 1) * kWarps * NT * 32;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) {
+        part.x += acc[nt][ch][0];
+        part.y += acc[nt][ch][1];
+        part.z += acc[nt][ch][2];
+        part.w += acc[nt][ch][3];
+      }
+      slot[(warp * NT + nt) * 32 + lane] = part;
+    }
     consumers_sync(kWarps * 32);
-    float4 st = slot[lane];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-      const float4 x = slot[w * 32 + lane];
-      st.x += x.x;
-      st.y += x.y;
-      st.z += x.z;
-      st.w += x.w;
-    }
-
+    float s00[NT], s01[NT], s10[NT], s11[NT];
     const int tA = key0 + 2 * r, tB = tA + 1;  // keys of MMA rows r and r + 8
-    const bool vA = !skip && tA >= i0 && tA < len;
-    const bool vB = !skip && tB >= i0 && tB < len;
-    const float s00 = vA ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, head 2c
-    const float s01 = vA ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, head 2c+1
-    const float s10 = vB ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, head 2c
-    const float s11 = vB ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, head 2c+1
-
-    // ---- online softmax update.  The reference max m only moves when some score
-    // exceeds it by more than kSlack (log2 units): below that, exp2(s - m) <= 2^8
-    // is exact in float and in the hi+lo weights, and (m, l, o) stays an exact
-    // state for any reference m, so most tiles skip the cross-lane max and the
-    // rescale.  The decision depends only on the scores, which every warp holds
-    // identically, so all warps take the same branch.
+    bool need = false;
+    // The reference max only moves when some score exceeds it by more than
+    // kSlack (log2 units): below that, exp2(s - m) <= 2^8 is exact in float and
+    // in the hi+lo weights, and (m, l, o) stays an exact state for any reference
+    // m, so most tiles skip the cross-lane max and the rescale.  The decision
+    // depends only on the scores, which every warp holds identically.
     constexpr float kSlack = 8.f;
-    float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
-    if (__any_sync(0xffffffffu, x0 > m0 + kSlack || x1 > m1 + kSlack)) {
+    float x0[NT], x1[NT];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {  // max over the 16 keys: lanes sharing c
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-      }
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float al0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - n0);
-      const float al1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - n1);
-      l0 *= al0;
-      l1 *= al1;
+    for (int nt = 0; nt < NT; ++nt) {
+      float4 st = slot[nt * 32 + lane];
 #pragma unroll
-      for (int j = 0; j < KS; ++j) {
-        o[j][0] *= al0;
-        o[j][1] *= al1;
-        o[j][2] *= al0;
-        o[j][3] *= al1;
+      for (int w = 1; w < kWarps; ++w) {
+        const float4 x = slot[(w * NT + nt) * 32 + lane];
+        st.x += x.x;
+        st.y += x.y;
+        st.z += x.z;
+        st.w += x.w;
       }
-      m0 = n0;
-      m1 = n1;
+      auto vis = [&](int t, int lim) { return !skip && t >= i0 && t < lim; };
+      s00[nt] = vis(tA, lim0[nt]) ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, column 8nt+2c
+      s01[nt] = vis(tA, lim1[nt]) ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, column 8nt+2c+1
+      s10[nt] = vis(tB, lim0[nt]) ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, column 8nt+2c
+      s11[nt] = vis(tB, lim1[nt]) ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, column 8nt+2c+1
+      x0[nt] = fmaxf(s00[nt], s10[nt]);
+      x1[nt] = fmaxf(s01[nt], s11[nt]);
+      need |= x0[nt] > m0[nt] + kSlack || x1[nt] > m1[nt] + kSlack;
     }
-    const float u0 = (m0 == -CUDART_INF_F) ? 0.f : m0;  // nothing attended yet: all weights 0
-    const float u1 = (m1 == -CUDART_INF_F) ? 0.f : m1;
-    const float p00 = exp2f(s00 - u0), p01 = exp2f(s01 - u1);
-    const float p10 = exp2f(s10 - u0), p11 = exp2f(s11 - u1);
-    l0 += p00 + p10;
-    l1 += p01 + p11;
 
-    // ---- P^T fragments (hi + lo bf16 pairs), transposed in registers
-    const uint32_t hA = pack_bf16x2(p00, p01), hB = pack_bf16x2(p10, p11);
-    const uint32_t lA = pack_bf16x2(p00 - bf16_lo(hA), p01 - bf16_hi(hA));
-    const uint32_t lB = pack_bf16x2(p10 - bf16_lo(hB), p11 - bf16_hi(hB));
-    const uint32_t bh0 = movmatrix_t(hA), bh1 = movmatrix_t(hB);
-    const uint32_t bl0 = movmatrix_t(lA), bl1 = movmatrix_t(lB);
+    // ---- online softmax update
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {  // max over the 16 keys: lanes sharing c
+          x0[nt] = fmaxf(x0[nt], __shfl_xor_sync(0xffffffffu, x0[nt], off));
+          x1[nt] = fmaxf(x1[nt], __shfl_xor_sync(0xffffffffu, x1[nt], off));
+        }
+        const float n0 = fmaxf(m0[nt], x0[nt]), n1 = fmaxf(m1[nt], x1[nt]);
+        const float al0 = (m0[nt] == -CUDART_INF_F) ? 0.f : exp2f(m0[nt] - n0);
+        const float al1 = (m1[nt] == -CUDART_INF_F) ? 0.f : exp2f(m1[nt] - n1);
+        l0[nt] *= al0;
+        l1[nt] *= al1;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          o[nt][j][0] *= al0;
+          o[nt][j][1] *= al1;
+          o[nt][j][2] *= al0;
+          o[nt][j][3] *= al1;
+        }
+        m0[nt] = n0;
+        m1[nt] = n1;
+      }
+    }
+    uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float u0 = (m0[nt] == -CUDART_INF_F) ? 0.f : m0[nt];  // nothing visible yet: weights 0
+      const float u1 = (m1[nt] == -CUDART_INF_F) ? 0.f : m1[nt];
+      const float p00 = exp2f(s00[nt] - u0), p01 = exp2f(s01[nt] - u1);
+      const float p10 = exp2f(s10[nt] - u0), p11 = exp2f(s11[nt] - u1);
+      l0[nt] += p00 + p10;
+      l1[nt] += p01 + p11;
+      // P^T fragments (hi + lo bf16 pairs), transposed in registers
+      const uint32_t hA = pack_bf16x2(p00, p01), hB = pack_bf16x2(p10, p11);
+      const uint32_t lA = pack_bf16x2(p00 - bf16_lo(hA), p01 - bf16_hi(hA));
+      const uint32_t lB = pack_bf16x2(p10 - bf16_lo(hB), p11 - bf16_hi(hB));
+      bh0[nt] = movmatrix_t(hA);
+      bh1[nt] = movmatrix_t(hB);
+      bl0[nt] = movmatrix_t(lA);
+      bl1[nt] = movmatrix_t(lB);
+    }
 
-    // ---- O^T += V^T P^T over this warp's d range; values of keys not attended masked to zero
+    // ---- O^T += V^T P^T over this warp's d range; values of keys outside [i0, len) masked to zero
     const bool full = !skip && key0 >= i0 && key0 + kKeyTile <= len;
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (!full) {
@@ -292,45 +332,48 @@ struct MmaConsumer {
       a1 &= mlo;
       a2 &= mhi;
       a3 &= mhi;
-      mma_bf16(o[j], a0, a1, a2, a3, bh0, bh1);
-      mma_bf16(o[j], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16(o[nt][j], a0, a1, a2, a3, bh0[nt], bh1[nt]);
+        mma_bf16(o[nt][j], a0, a1, a2, a3, bl0[nt], bl1[nt]);
+      }
     }
   }
 
-  // Sum this warp's per-lane l over the 8 lanes that share a head pair.
+  // Sum this warp's per-lane l over the 8 lanes that share a column pair.
   __device__ void finish() {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0[nt] += __shfl_xor_sync(0xffffffffu, l0[nt], off);
+        l1[nt] += __shfl_xor_sync(0xffffffffu, l1[nt], off);
+      }
   }
 
-  // Write this partition's (m, l, o): every warp writes its d range; warp 0 the scalars.
-  __device__ void write_partial(const PartialArgs &a, size_t row0, int P) const {
-    const int d0 = warp * DW;
-    const bool h0_real = 2 * c < G, h1_real = 2 * c + 1 < G;  // columns holding real heads
+  // Write this partition's (m, l, o) of every real column: every warp writes
+  // its d range; warp 0 the scalars.  Column j -> workspace row (b, j / G, h0 + j % G).
+  __device__ void write_partial(const PartialArgs &a, int b, int h0, int p) const {
+    const int P = a.num_splits, d0 = warp * DW;
 #pragma unroll
-    for (int j = 0; j < KS; ++j) {
-      float *o_h0 = a.ws_o + (row0 + (size_t)(2 * c) * P) * D + d0 + 16 * j + r;
-      float *o_h1 = a.ws_o + (row0 + (size_t)(2 * c + 1) * P) * D + d0 + 16 * j + r;
-      if (h0_real) {
-        o_h0[0] = o[j][0];
-        o_h0[8] = o[j][2];
-      }
-      if (h1_real) {
-        o_h1[0] = o[j][1];
-        o_h1[8] = o[j][3];
-      }
-    }
-    if (warp == 0 && r == 0) {
-      if (h0_real) {
-        a.ws_m[row0 + (size_t)(2 * c) * P] = m0 == -CUDART_INF_F ? -CUDART_INF_F : m0 * kLn2;
-        a.ws_l[row0 + (size_t)(2 * c) * P] = l0;
-      }
-      if (h1_real) {
-        a.ws_m[row0 + (size_t)(2 * c + 1) * P] = m1 == -CUDART_INF_F ? -CUDART_INF_F : m1 * kLn2;
-        a.ws_l[row0 + (size_t)(2 * c + 1) * P] = l1;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int jc = cbase + 8 * nt + 2 * c + e, t = jc / G;
+        if (t >= tokens) continue;
+        const size_t row =
+            (((size_t)b * tokens + t) * a.num_q_heads + h0 + jc % G) * P + p;
+        float *dst = a.ws_o + row * D + d0 + r;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          dst[16 * j] = o[nt][j][e];
+          dst[16 * j + 8] = o[nt][j][2 + e];
+        }
+        if (warp == 0 && r == 0) {
+          const float mm = e ? m1[nt] : m0[nt];
+          a.ws_m[row] = mm == -CUDART_INF_F ? -CUDART_INF_F : mm * kLn2;
+          a.ws_l[row] = e ? l1[nt] : l0[nt];
+        }
       }
     }
   }
@@ -349,6 +392,7 @@ struct SimtConsumer {
   using Elem = T;
   static constexpr int D = kD;
   static constexpr int G = kG;
+  static constexpr int kCols = kG;  // one query token: a column per head of the group
   static constexpr int E = D / 32;
   static constexpr int VE = 16 / (int)sizeof(T);
   static constexpr int NC = E / VE;
@@ -400,7 +444,8 @@ struct SimtConsumer {
     }
   }
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra) {
+  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra,
+                       int, int) {
     lane_ = lane;
     scale_log2 = a.scale_log2;
     q_s = reinterpret_cast<const float *>(extra);
@@ -591,7 +636,10 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // x = partition x column block (the blocks of one partition launch together
+  // and share its keys in L2), y = KV head, z = row
+  const int cb = (int)(blockIdx.x % (unsigned)a.col_blocks);
+  const int p = (int)(blockIdx.x / (unsigned)a.col_blocks), g = blockIdx.y, b = blockIdx.z;
   const int P = a.num_splits;
   const int h0 = g * G;
 
@@ -612,7 +660,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   // ---- this partition's tiles
   const long long cap = (long long)a.table_stride * a.page_size;
   long long len_ll = a.seq_lens[b];
-  if (len_ll < 1 || len_ll > cap) {
+  if (len_ll < a.num_tokens || len_ll > cap) {  // a row holds at least its query tokens
     if (threadIdx.x == 0 && p == 0 && g == 0) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
     len_ll = len_ll < 0 ? 0 : (len_ll > cap ? cap : len_ll);
   }
@@ -631,15 +679,18 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   const int t_begin = t_lo + (int)lo_ll;
   const int n_my = (int)(hi_ll - lo_ll);
 
-  const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0
-  // the merge that follows counts finished groups per (row, head): start it at zero
-  if (a.merge_counters != nullptr && p == 0 && g == 0)
-    for (int h = threadIdx.x; h < a.num_q_heads; h += blockDim.x)
-      a.merge_counters[(size_t)b * a.num_q_heads + h] = 0u;
+  const int T = a.num_tokens;
+  const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0 (T = 1)
+  // the merge that follows counts finished groups per (row, token, head): start it at zero
+  if (a.merge_counters != nullptr && p == 0 && g == 0 && cb == 0)
+    for (int h = threadIdx.x; h < T * a.num_q_heads; h += blockDim.x)
+      a.merge_counters[(size_t)b * T * a.num_q_heads + h] = 0u;
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
-    if (threadIdx.x < G) {
-      a.ws_m[row0 + (size_t)threadIdx.x * P] = -CUDART_INF_F;
-      a.ws_l[row0 + (size_t)threadIdx.x * P] = 0.f;
+    const int c0 = cb * C::kCols, c1 = min(c0 + C::kCols, T * G);  // this block's columns
+    for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+      const size_t row = (((size_t)b * T + i / G) * a.num_q_heads + h0 + i % G) * P + p;
+      a.ws_m[row] = -CUDART_INF_F;
+      a.ws_l[row] = 0.f;
     }
     return;
   }
@@ -709,7 +760,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   } else {
     // ---------------- consumer warps
     // cooperative consumers all take every tile; the others take every CW-th
-    cons.init(a, b, h0, lane, extra);
+    cons.init(a, b, h0, lane, extra, len, cb);
     const int j0 = C::kCooperative ? 0 : warp, dj = C::kCooperative ? 1 : CW;
     for (int j = j0; j < n_my; j += dj) {
       const int s = j % NS;
@@ -738,7 +789,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(c
   if (*abort_flag) return;
 
   if constexpr (C::kCooperative) {
-    if (warp < CW) cons.write_partial(a, row0, P);
+    if (warp < CW) cons.write_partial(a, b, h0, p);
     return;
   } else {
     merge_warp_states<C>(cons, a, ring, red_m, red_l, weight, row0, P, warp);

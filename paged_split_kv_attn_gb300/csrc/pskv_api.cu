@@ -47,15 +47,15 @@ int sm_count(int *out) {
   return PSKV_OK;
 }
 
-// CTA slots of the partial kernel serving (dtype, head_dim, group, format): SMs x CTAs per SM.
-int partial_slots(int kv_dtype, int head_dim, int group, int format, int *slots) {
+// CTA slots of the partial kernel serving (dtype, head_dim, group, format, n-tiles): SMs x CTAs per SM.
+int partial_slots(int kv_dtype, int head_dim, int group, int format, int nt, int *slots) {
   int n_sm = 0, rc = sm_count(&n_sm);
   if (rc) return rc;
   const int kernel = pick_kernel(kv_dtype, head_dim, group, format);
   int per = 0;
   cudaError_t e;
   if (kernel == kKernelMma)
-    e = occupancy_partial_mma(head_dim, group, format == PSKV_FORMAT_FOLDED, &per);
+    e = occupancy_partial_mma(head_dim, group, format == PSKV_FORMAT_FOLDED, nt, &per);
   else if (kernel == kKernelSimt && kv_dtype == PSKV_DTYPE_F32)
     e = occupancy_partial_simt_f32(head_dim, group, &per);
   else if (kernel == kKernelSimt)
@@ -80,7 +80,8 @@ constexpr int kMaxGroups = 64;
 int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_tables,
                   int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
                   const int32_t *first_pos, const int32_t *window_lo, bool windowed,
-                  int32_t batch, int32_t num_q_heads, float scale, int32_t num_splits,
+                  int32_t batch, int32_t num_tokens, int32_t num_q_heads, float scale,
+                  int32_t num_splits,
                   void *workspace, size_t workspace_bytes, void *out, int32_t out_dtype,
                   const pskv_decode_opts *opts, pskv_stream_t stream) {
   if (!layout || !q || !page_tables || !seq_lens_host || !seq_lens || !workspace || !out)
@@ -98,7 +99,16 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
   if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
   const bool folded = d.format == PSKV_FORMAT_FOLDED;
-  int rc = check_lengths(layout, batch, table_stride, seq_lens_host);
+  // Query columns per KV head (heads x tokens): one n-tile of 8 when they fit,
+  // else blocks of two n-tiles, one CTA per block (several tokens only on the
+  // tensor-core family).
+  if (num_tokens < 1 || num_tokens > PSKV_MAX_WINDOW_TOKENS) return PSKV_ERR_INVALID_ARG;
+  if (num_tokens > 1 && (kernel != kKernelMma || windowed)) return PSKV_ERR_UNSUPPORTED;
+  const int columns = group * num_tokens;
+  const int nt = columns > 8 ? 2 : 1;
+  const int col_blocks = (columns + 8 * nt - 1) / (8 * nt);
+  if ((int64_t)batch * num_tokens * num_q_heads > INT32_MAX) return PSKV_ERR_INVALID_ARG;
+  int rc = check_lengths(layout, batch, table_stride, seq_lens_host, num_tokens);
   if (rc) return rc;
   int mgroup = 0;
   if ((rc = merge_group_of(opts, &mgroup))) return rc;
@@ -106,11 +116,13 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int P = num_splits;
   if (P == 0) {
     int slots = 0;
-    if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, &slots))) return rc;
-    P = plan_splits(slots, batch, d.num_kv_heads, seq_lens_host);
+    if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
+    // every partition launches col_blocks CTAs
+    P = plan_splits(slots / col_blocks, batch, d.num_kv_heads, seq_lens_host);
   }
   WorkspacePlan w;
-  if ((rc = plan_workspace(batch, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
+  const int64_t rows = (int64_t)batch * num_tokens;  // workspace and output rows: (row, token)
+  if ((rc = plan_workspace(rows, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
   if (workspace_bytes < w.total) return PSKV_ERR_WORKSPACE_TOO_SMALL;
 
@@ -134,17 +146,19 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.num_kv_heads = d.num_kv_heads;
   a.num_q_heads = num_q_heads;
   a.num_splits = P;
+  a.num_tokens = num_tokens;
+  a.col_blocks = col_blocks;
   a.scale_log2 = scale * kLog2e;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(P, d.num_kv_heads, batch);
+  const dim3 grid(P * col_blocks, d.num_kv_heads, batch);
   cudaError_t e;
   if (opts && opts->partial_begin) {
     e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (kernel == kKernelMma)
-    e = launch_partial_mma(a, d.head_dim_v, group, folded, grid, s);
+    e = launch_partial_mma(a, d.head_dim_v, group, folded, nt, grid, s);
   else if (d.kv_dtype == PSKV_DTYPE_F32)
     e = launch_partial_simt_f32(a, d.head_dim_v, group, grid, s);
   else
@@ -160,7 +174,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   m.m = a.ws_m;
   m.l = a.ws_l;
   m.o = a.ws_o;
-  m.rows = batch * num_q_heads;
+  m.rows = (int)(rows * num_q_heads);
   m.count = P;
   m.dv = d.head_dim_v;
   m.group = mgroup;
@@ -248,7 +262,7 @@ int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t 
                         int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
                         int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream) {
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
-                       nullptr, false, batch, num_q_heads, scale, num_splits, workspace,
+                       nullptr, false, batch, 1, num_q_heads, scale, num_splits, workspace,
                        workspace_bytes, out, out_dtype, opts, stream);
 }
 
@@ -260,8 +274,19 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream) {
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, first_pos,
-                       window_lo, true, batch, num_q_heads, scale, num_splits, workspace,
+                       window_lo, true, batch, 1, num_q_heads, scale, num_splits, workspace,
                        workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                         int32_t table_stride, const int32_t *seq_lens_host,
+                         const int32_t *seq_lens, int32_t batch, int32_t num_tokens,
+                         int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, int32_t out_dtype,
+                         const pskv_decode_opts *opts, pskv_stream_t stream) {
+  return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
+                       nullptr, false, batch, num_tokens, num_q_heads, scale, num_splits,
+                       workspace, workspace_bytes, out, out_dtype, opts, stream);
 }
 
 int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
@@ -363,7 +388,7 @@ int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_hea
   if (num_q_heads % layout->d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
   int slots = 0;
   const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_v,
-                               num_q_heads / layout->d.num_kv_heads, layout->d.format, &slots);
+                               num_q_heads / layout->d.num_kv_heads, layout->d.format, 1, &slots);
   if (rc) return rc;
   *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host);
   return PSKV_OK;

@@ -41,6 +41,8 @@ struct PartialArgs {
   int num_kv_heads;
   int num_q_heads;
   int num_splits;
+  int num_tokens;    // query tokens per row: 1, or a verify window's length
+  int col_blocks;    // CTAs per (row, KV head, partition): query columns in blocks
   float scale_log2;  // scale * log2(e)
 };
 
@@ -85,13 +87,14 @@ struct AppendArgs {
 };
 
 // Host-side launchers (one per kernel family).  They return a CUDA error code.
-cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, bool folded,
+// The tensor-core family takes `nt` n-tiles of 8 query columns (group x tokens <= 8 nt).
+cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, bool folded, int nt,
                                dim3 grid, cudaStream_t s);
 cudaError_t launch_partial_simt_f32(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                     cudaStream_t s);
 cudaError_t launch_partial_simt_bf16(const PartialArgs &a, int head_dim, int group, dim3 grid,
                                      cudaStream_t s);
-cudaError_t occupancy_partial_mma(int head_dim, int group, bool folded, int *ctas);
+cudaError_t occupancy_partial_mma(int head_dim, int group, bool folded, int nt, int *ctas);
 cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas);
 cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);

@@ -63,11 +63,12 @@ int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64
 }
 
 int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride,
-                  const int32_t *seq_lens_host) {
-  if (!layout || !seq_lens_host || batch < 1 || table_stride < 1) return PSKV_ERR_INVALID_ARG;
+                  const int32_t *seq_lens_host, int32_t min_len) {
+  if (!layout || !seq_lens_host || batch < 1 || table_stride < 1 || min_len < 1)
+    return PSKV_ERR_INVALID_ARG;
   const int64_t cap = (int64_t)table_stride * layout->d.page_size;
   for (int32_t b = 0; b < batch; ++b)
-    if (seq_lens_host[b] < 1 || (int64_t)seq_lens_host[b] > cap) return PSKV_ERR_INVALID_ARG;
+    if (seq_lens_host[b] < min_len || (int64_t)seq_lens_host[b] > cap) return PSKV_ERR_INVALID_ARG;
   return PSKV_OK;
 }
 

@@ -33,9 +33,9 @@ int check_layout_desc(const pskv_layout_desc *d);
 int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64_t splits,
                    int64_t group, WorkspacePlan *out);
 
-// Checks the host lengths: each in [1, table_stride * page_size].
+// Checks the host lengths: each in [min_len, table_stride * page_size].
 int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride,
-                  const int32_t *seq_lens_host);
+                  const int32_t *seq_lens_host, int32_t min_len = 1);
 
 // Automatic split count for `slots` CTA slots (SMs x CTAs per SM).
 int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host);

@@ -155,6 +155,34 @@ def test_decode_refusals_happen_before_any_launch(lib):
         lib.paged_kv_layout_destroy(h)
 
 
+def _multirow_rc(lib, layout, lens, tokens, **kw):
+    args = dict(q=0x30000, tables=0x40000, stride=4, lens_dev=0x50000, batch=len(lens), hq=32,
+                scale=0.04, splits=8, ws=0x60000, ws_bytes=1 << 30, out=0x70000,
+                out_dtype=B.PSKV_DTYPE_BF16)
+    args.update(kw)
+    lh = (ctypes.c_int32 * len(lens))(*lens)
+    return lib.decode_attn_multirow(layout, args["q"], args["tables"], args["stride"], lh,
+                                    args["lens_dev"], args["batch"], tokens, args["hq"],
+                                    args["scale"], args["splits"], args["ws"], args["ws_bytes"],
+                                    args["out"], args["out_dtype"], None, None)
+
+
+def test_multirow_refusals_happen_before_any_launch(lib):
+    h = _layout(lib)
+    f32 = _layout(lib, kv_dtype=B.PSKV_DTYPE_F32)
+    try:
+        assert _multirow_rc(lib, h, [100], 0) == B.PSKV_ERR_INVALID_ARG
+        assert _multirow_rc(lib, h, [100], B.PSKV_MAX_WINDOW_TOKENS + 1) == B.PSKV_ERR_INVALID_ARG
+        assert _multirow_rc(lib, h, [3], 4) == B.PSKV_ERR_INVALID_ARG   # row shorter than the window
+        assert _multirow_rc(lib, f32, [100], 2) == B.PSKV_ERR_UNSUPPORTED  # tensor-core family only
+        # the workspace holds batch x tokens rows of partials
+        need = pskv.decode_attn_workspace_bytes(2, 32, 512, 8)
+        assert _multirow_rc(lib, h, [100, 100], 3, ws_bytes=need) == B.PSKV_ERR_WORKSPACE_TOO_SMALL
+    finally:
+        lib.paged_kv_layout_destroy(h)
+        lib.paged_kv_layout_destroy(f32)
+
+
 def test_append_past_pages_refused_on_host(lib):
     h = _layout(lib)
     try:

@@ -184,6 +184,13 @@ def make_paged_case(seed: int, seq_lens, num_q_heads: int, num_kv_heads: int, he
                      dense_k=dense_k, dense_v=dense_v)
 
 
+def window_queries(case: PagedCase, tokens: int, seed: int = 0) -> np.ndarray:
+    """Random queries for a verify window of ``tokens`` per row:
+    [batch, tokens, num_q_heads, head_dim] in the case's dtype."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tokens])))
+    return _normal(rng, (case.batch, tokens, case.num_q_heads, case.head_dim), case.dtype)
+
+
 def with_window(case: PagedCase, window: int, first_pos=None) -> PagedCase:
     """Give every row a window lower bound so that the query (at position
     first_pos + len - 1) sees the last ``window`` positions, itself included."""
