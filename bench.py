@@ -48,6 +48,7 @@ DEFAULT_CONTEXTS = (10602, 40002)
 WINDOW_RESIDENCY = W.WINDOW + 64
 ROTATE = 3
 PARTIAL_SOURCES = ("paged_split_kv_attn_gb300/csrc/partial_kernel.cuh",
+                   "paged_split_kv_attn_gb300/csrc/partial_mma.cuh",
                    "paged_split_kv_attn_gb300/csrc/partial_mma.cu",
                    "paged_split_kv_attn_gb300/csrc/pskv_internal.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_mma_d512_ctx40002.md")
@@ -188,10 +189,11 @@ class ClockSampler:
 class Call:
     """One decode call of the step: a pool (and rotating copies), its inputs and outputs."""
 
-    def __init__(self, name, case, windowed, splits, dev, rotate):
+    def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1):
         import torch
         import paged_split_kv_attn_gb300 as pskv
         self.name, self.case, self.windowed = name, case, windowed
+        self.tokens = tokens  # query tokens per row: > 1 is a verify window (multi-row decode)
         self.splits = splits
         bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
             torch.bfloat16).to(dev)
@@ -201,7 +203,7 @@ class Call:
         self.status = torch.zeros(4, dtype=torch.int32, device=dev)
         self.layouts = [pskv.paged_kv_layout_create(k, v, self.status)
                         for k, v in zip(self.k, self.v)]
-        self.q = bf(case.q)
+        self.q = bf(case.q if tokens == 1 else W.window_queries(case, tokens))
         self.tables = torch.from_numpy(case.page_tables).to(dev)
         self.lens = torch.from_numpy(case.seq_lens).to(dev)
         self.lens_host = case.seq_lens.copy()
@@ -220,8 +222,8 @@ class Call:
                                   for r, p in zip(self.rows, self.pos)]).contiguous()
         self.v_new = torch.stack([v0[int(case.page_tables[r, p // ps]), :, p % ps]
                                   for r, p in zip(self.rows, self.pos)]).contiguous()
-        self.out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=dev)
-        self.ws = pskv.workspace(b, hq, d, splits, dev)
+        self.out = torch.empty(tuple(self.q.shape[:-1]) + (d,), dtype=torch.bfloat16, device=dev)
+        self.ws = pskv.workspace(b * tokens, hq, d, splits, dev)
         self.bytes = case.kv_bytes()
         self.partial_bytes_per_launch = self.bytes
         self.hkv = hkv
@@ -235,7 +237,11 @@ class Call:
         layout = self.layouts[it % len(self.layouts)]
         pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of, self.tables,
                             self.pages_of_row)
-        if self.windowed:
+        if self.tokens > 1:
+            pskv.decode_attn_multirow(layout, self.q, self.tables, self.lens, self.lens_host,
+                                      self.case.scale, num_splits=self.splits, workspace=self.ws,
+                                      out=self.out, events=events)
+        elif self.windowed:
             pskv.decode_attn_windowed(layout, self.q, self.tables, self.lens, self.lens_host,
                                       self.first_pos, self.window_lo, self.case.scale,
                                       num_splits=self.splits, workspace=self.ws, out=self.out,
@@ -286,9 +292,15 @@ class Packed:
 
 
 def make_extra_calls(args, dev):
-    """Calls measured one at a time beside the step: the folded format (NEXT row)."""
-    return [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev, ROTATE)
-            for ctx in args.folded_contexts]
+    """Calls measured one at a time beside the step: the folded format and
+    verify windows of the global shape (multi-row decode)."""
+    calls = [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev,
+                  ROTATE) for ctx in args.folded_contexts]
+    for t in args.verify_tokens:
+        ctx = args.verify_context
+        calls.append(Call(f"verify_{ctx}x{t}", W.global_case(ctx, seed=ctx + 2), False,
+                          args.splits, dev, ROTATE, tokens=t))
+    return calls
 
 
 def make_calls(args, dev):
@@ -337,6 +349,10 @@ def parse():
     ap.add_argument("--no-window", action="store_true")
     ap.add_argument("--folded-contexts", type=int, nargs="*", default=[40002],
                     help="contexts of the folded-format decode timed beside the step")
+    ap.add_argument("--verify-tokens", type=int, nargs="*", default=[2, 4],
+                    help="verify-window lengths of the multi-row decode timed beside the step")
+    ap.add_argument("--verify-context", type=int, default=40002,
+                    help="context of those verify windows (global-layer shape)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
@@ -510,7 +526,9 @@ def main():
         part = [b.elapsed_time(e) for b, e in pe]
         per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
                             "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9,
-                            "note": "folded format, measured beside the step (not in value)"}
+                            "note": ("folded format" if c.tokens == 1 else
+                                     f"verify window of {c.tokens} tokens")
+                            + ", measured beside the step (not in value)"}
     flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
     for c in calls + extra:
         times = []
@@ -524,7 +542,9 @@ def main():
             times.append(b.elapsed_time(e) * 1e3)
         per_call[c.name]["us_per_call_median"] = statistics.median(times)
         per_call[c.name]["GBps_per_call"] = c.bytes / (statistics.median(times) * 1e-6) / 1e9
-        per_call[c.name]["splits"] = c.splits or pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads, c.lens_host)
+        per_call[c.name]["splits"] = c.splits or (
+            pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads, c.lens_host)
+            if c.tokens == 1 else "auto")
 
     # optional split sweep of the global contexts (each call alone, cold L2)
     sweep = None
