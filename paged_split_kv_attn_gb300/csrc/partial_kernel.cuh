@@ -75,25 +75,30 @@ struct RingGeom {
 };
 
 // -------------------------------------------------------------------------------------------
-// Tensor-core consumer: bf16 K/V, 8 query heads per KV head.
-// The four consumer warps work on every tile together, each on one quarter of
-// the head dimension (so each SM sub-partition's tensor unit takes a quarter
-// of the products; one warp alone issues mma.sync too slowly to keep up with
-// HBM):
-//  1. warp w forms the partial scores S_w^T[16 keys x 8 heads] = K[:, dw] Q^T[dw, :]
-//     over its d range dw (mma m16n8k16, keys as M so no row is wasted);
-//  2. the four partials are summed through shared memory in a fixed order,
-//     so every warp holds the same S^T and runs the same online-softmax update;
-//  3. warp w accumulates O^T[dw x 8] += V^T[dw x 16] P^T[16 x 8], with P^T
-//     obtained from the S^T accumulator by movmatrix.trans.  P is applied as a
-//     bf16 hi+lo pair (p = hi + lo to ~2^-17 relative), so the weights keep
-//     nearly fp32 accuracy while V stays bf16.
+// Tensor-core consumer: bf16 K/V, query columns in n-tiles of 8.
+// A column is one (query token, query head of the KV group): 8 heads of one
+// token per n-tile in single-token decode, up to 16 columns per CTA for verify
+// windows.  The consumer warps work on every tile together (one warp alone
+// issues mma.sync too slowly to keep up with HBM):
+//  1. scores: the head dimension is cut into four quarters; warp w forms the
+//     partial scores S^T[16 keys x 8 columns] = K[:, dq] Q^T[dq, :] of n-tile
+//     w % NT over quarter dq = w / NT (mma m16n8k16, keys as M so no row is
+//     wasted);
+//  2. the four quarters' partials of each n-tile are summed through shared
+//     memory in a fixed order, so every warp holds the same S^T of every
+//     column and runs the same online-softmax update;
+//  3. warp w accumulates O^T[dw x cols] += V^T[dw x 16] P^T[16 x cols] over its
+//     own slice dw of the head dimension (D / warps wide), with P^T obtained
+//     from the S^T accumulator by movmatrix.trans.  P is applied as a bf16
+//     hi+lo pair (p = hi + lo to ~2^-17 relative), so the weights keep nearly
+//     fp32 accuracy while V stays bf16.
+// With one n-tile that is four warps, each on a quarter of D for both steps;
+// with two, eight warps: each warp's products, accumulators and dependency
+// chain per tile stay as short as with one n-tile, and the score exchange
+// grows only with the number of n-tiles.
 // MMA row m holds key 2m (m < 8) or key 2(m-8)+1 (m >= 8): with rows stored in
 // padded pairs, each 8x8 ldmatrix phase then reads 8 distinct bank groups.
 // -------------------------------------------------------------------------------------------
-#ifndef PSKV_MMA_WARPS
-#define PSKV_MMA_WARPS 4
-#endif
 
 // Stages per CTA of the tensor-core consumer.  Three stages per CTA, with as
 // many CTAs per SM as shared memory allows (2 for split hd512 rows, 3 for
@@ -120,49 +125,54 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
   return out != 0;
 }
 
-// G < 8 query heads per KV head run on the same 8-column products with the
-// unused columns' queries set to zero (their results are never written).
+// Columns past the window's tokens x G (G < 8 query heads per KV head, or a
+// window that does not fill its last n-tile) have zero queries and are never
+// written back.
 // kFolded: the pool keeps only the first D/4 columns of K (the rotated quarter)
 // and the folded query's other columns meet V's (pegainfer #1055, Description:
 // the folded row holds K only where the rotation touches it, V in full, with
-// K's norm weight folded into the query).  Warp 0's quarter of D is exactly the
-// stored K columns, so warp 0 reads its score operands from the K tile and
-// warps 1..3 read theirs from the V tile.
+// K's norm weight folded into the query).  The warps scoring quarter 0 read
+// their operands from the K tile, the others from the V tile.
 template <int kD, int kG = 8, bool kFolded = false, int kNT = 1>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
   static constexpr int G = kG;
   static_assert(kG == 1 || kG == 2 || kG == 4 || kG == 8, "query heads per KV head");
-  // Query columns: kNT n-tiles of 8 per CTA.  Window column j (of tokens x G)
-  // serves query token j / G, head j % G of the KV group; CTA column block cb
-  // takes columns [cb * kCols, (cb + 1) * kCols).  Columns past tokens x G have
-  // zero queries and are never written.
+  // Window column j (of tokens x G) serves query token j / G, head j % G of the
+  // KV group; CTA column block cb takes columns [cb * kCols, (cb + 1) * kCols).
   static constexpr int NT = kNT;
   static constexpr int kCols = 8 * kNT;
-  static constexpr int kWarps = PSKV_MMA_WARPS;
-  static constexpr bool kCooperative = true;   // every warp takes part in every tile
-  static constexpr int DW = D / kWarps;        // head-dim columns per warp
-  static constexpr int KS = DW / 16;           // k-steps of QK = m-tiles of PV per warp
-  static constexpr int CH = NT == 1 ? 4 : 2;   // score accumulator chains per n-tile
-  static constexpr int kExtraSmem = 2 * kWarps * NT * 32 * 16;  // double-buffered score exchange
-  static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;  // bytes of one stored K row
+  static constexpr int kQuarters = 4;              // score partials per n-tile
+  static constexpr int kWarps = kQuarters * kNT;
+  static constexpr int kMinBlocks = 2;             // registers sized for two CTAs per SM
+  static constexpr bool kCooperative = true;       // every warp takes part in every tile
+  static constexpr int DQ = D / kQuarters;         // score columns per warp
+  static constexpr int KSQ = DQ / 16;              // k-steps of a warp's score product
+  static constexpr int DW = D / kWarps;            // output columns per warp
+  static constexpr int KSP = DW / 16;              // m-tiles of a warp's PV product
+  static constexpr int CH = KSQ % 4 == 0 ? 4 : 2;  // score accumulator chains
+  static constexpr int kExtraSmem = 2 * kQuarters * NT * 32 * 16;  // double-buffered exchange
+  static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;     // bytes of one stored K row
   static constexpr int kRowBytesV = D * 2;
   using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1, PSKV_MMA_STAGES>;
   static constexpr int RBK = kRowBytesK, RBV = kRowBytesV;
   static constexpr int GSK = Geom::kGroupStrideK;  // bytes of a padded pair of K rows
   static constexpr int GSV = Geom::kGroupStrideV;  // bytes of a padded pair of V rows
-  static_assert(KS % CH == 0, "k-steps divide among the accumulator chains");
-  static_assert(!kFolded || DW == D / 4, "warp 0 must own exactly the stored K columns");
+  static_assert(KSQ % CH == 0 && KSP >= 1, "warp shares of the head dimension");
 
-  uint32_t qf[NT][KS][2];  // Q^T B-fragments: (d = dw0 + 16k + 2c + {0,1} [+8], column 8nt + r)
-  float o[NT][KS][4];      // O^T accumulators: (d = dw0 + 16j + r [+8], columns 8nt + 2c, +1)
+  uint32_t qf[KSQ][2];     // Q^T B-fragments of this warp's n-tile and quarter:
+                           //   (d = dq0 + 16k + 2c + {0,1} [+8], column 8 nts + r)
+  float o[NT][KSP][4];     // O^T accumulators: (d = dw0 + 16j + r [+8], columns 8nt + 2c, +1)
   float m0[NT], m1[NT];    // reference max (log2 units) of columns 8nt + 2c, +1: the same in every warp
   float l0[NT], l1[NT];    // this lane's share of the sums of those columns
   int lim0[NT], lim1[NT];  // keys below lim are visible to those columns (causal in a window)
   float scale_log2;
-  float4 *xchg;            // [2][kWarps][NT][32] partial scores
+  float4 *xchg;            // [2][kQuarters][NT][32] partial scores
   int r, c, warp, tokens, cbase;
+
+  __device__ int nt_scored() const { return warp % NT; }  // the n-tile this warp scores
+  __device__ int quarter() const { return warp / NT; }     // the quarter of D it scores over
 
   static __device__ void prologue(const PartialArgs &, int, int, unsigned char *) {}
 
@@ -175,24 +185,27 @@ struct MmaConsumer {
     cbase = cb * kCols;
     scale_log2 = a.scale_log2;
     xchg = reinterpret_cast<float4 *>(extra);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int jq = cbase + 8 * nt + r, tq = jq / G;  // the column this lane feeds as B operand
+    {
+      const int jq = cbase + 8 * nt_scored() + r, tq = jq / G;  // the column this lane feeds
       const bool real = tq < tokens;
       const uint16_t *q =
           static_cast<const uint16_t *>(a.q) +
-          (((size_t)b * tokens + (real ? tq : 0)) * a.num_q_heads + h0 + jq % G) * D + warp * DW;
+          (((size_t)b * tokens + (real ? tq : 0)) * a.num_q_heads + h0 + jq % G) * D +
+          quarter() * DQ;
 #pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        qf[nt][k][0] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
-        qf[nt][k][1] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c) : 0u;
+      for (int k = 0; k < KSQ; ++k) {
+        qf[k][0] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
+        qf[k][1] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 8 + 2 * c) : 0u;
       }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
       // token t of the row sits at key len - tokens + t and sees keys up to itself
       const int j0 = cbase + 8 * nt + 2 * c, t0 = j0 / G, t1 = (j0 + 1) / G;
       lim0[nt] = t0 < tokens ? len - tokens + t0 + 1 : 0;
       lim1[nt] = t1 < tokens ? len - tokens + t1 + 1 : 0;
 #pragma unroll
-      for (int j = 0; j < KS; ++j) o[nt][j][0] = o[nt][j][1] = o[nt][j][2] = o[nt][j][3] = 0.f;
+      for (int j = 0; j < KSP; ++j) o[nt][j][0] = o[nt][j][1] = o[nt][j][2] = o[nt][j][3] = 0.f;
       m0[nt] = m1[nt] = -CUDART_INF_F;
       l0[nt] = l1[nt] = 0.f;
     }
@@ -201,39 +214,35 @@ struct MmaConsumer {
   __device__ void tile(const unsigned char *ks, const unsigned char *vs, int key0, int i0, int len,
                        bool skip, int lane, int j_tile) {
     const int mi = lane >> 3, rr = lane & 7;
-    // ---- partial scores over this warp's d range; each K fragment feeds every n-tile
-    float acc[NT][CH][4];
+    // ---- partial scores of this warp's n-tile over its quarter of D
+    float acc[CH][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int ch = 0; ch < CH; ++ch) acc[nt][ch][0] = acc[nt][ch][1] = acc[nt][ch][2] = acc[nt][ch][3] = 0.f;
+    for (int ch = 0; ch < CH; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
     // A rows m = (mi&1)*8 + rr hold key 2*rr + (mi&1): pair rr, row (mi&1) of the pair
-    const bool from_v = kFolded && warp > 0;  // a folded key's columns past D/4 live in V
+    const int dq = quarter();
+    const bool from_v = kFolded && dq > 0;  // a folded key's columns past D/4 live in V
     const uint32_t kaddr =
-        from_v ? smem_u32(vs) + rr * GSV + (mi & 1) * RBV + (mi >> 1) * 16 + warp * DW * 2
+        from_v ? smem_u32(vs) + rr * GSV + (mi & 1) * RBV + (mi >> 1) * 16 + dq * DQ * 2
                : smem_u32(ks) + rr * GSK + (mi & 1) * RBK + (mi >> 1) * 16 +
-                     (kFolded ? 0 : warp * DW * 2);
+                     (kFolded ? 0 : dq * DQ * 2);
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
+    for (int k = 0; k < KSQ; ++k) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4(kaddr + k * 32, a0, a1, a2, a3);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_bf16(acc[nt][k % CH], a0, a1, a2, a3, qf[nt][k][0], qf[nt][k][1]);
+      mma_bf16(acc[k % CH], a0, a1, a2, a3, qf[k][0], qf[k][1]);
     }
-    // ---- sum the four warps' partials (fixed order: every warp gets the same bits)
-    float4 *slot = xchg + (j_tile & 1) * kWarps * NT * 32;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    // ---- sum the four quarters' partials of each n-tile (fixed order: every warp gets the same bits)
+    float4 *slot = xchg + (j_tile & 1) * kQuarters * NT * 32;
+    {
       float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int ch = 0; ch < CH; ++ch) {
-        part.x += acc[nt][ch][0];
-        part.y += acc[nt][ch][1];
-        part.z += acc[nt][ch][2];
-        part.w += acc[nt][ch][3];
+        part.x += acc[ch][0];
+        part.y += acc[ch][1];
+        part.z += acc[ch][2];
+        part.w += acc[ch][3];
       }
-      slot[(warp * NT + nt) * 32 + lane] = part;
+      slot[(dq * NT + nt_scored()) * 32 + lane] = part;
     }
     consumers_sync(kWarps * 32);
     float s00[NT], s01[NT], s10[NT], s11[NT];
@@ -250,8 +259,8 @@ struct MmaConsumer {
     for (int nt = 0; nt < NT; ++nt) {
       float4 st = slot[nt * 32 + lane];
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) {
-        const float4 x = slot[(w * NT + nt) * 32 + lane];
+      for (int q = 1; q < kQuarters; ++q) {
+        const float4 x = slot[(q * NT + nt) * 32 + lane];
         st.x += x.x;
         st.y += x.y;
         st.z += x.z;
@@ -282,7 +291,7 @@ struct MmaConsumer {
         l0[nt] *= al0;
         l1[nt] *= al1;
 #pragma unroll
-        for (int j = 0; j < KS; ++j) {
+        for (int j = 0; j < KSP; ++j) {
           o[nt][j][0] *= al0;
           o[nt][j][1] *= al1;
           o[nt][j][2] *= al0;
@@ -311,7 +320,7 @@ struct MmaConsumer {
       bl1[nt] = movmatrix_t(lB);
     }
 
-    // ---- O^T += V^T P^T over this warp's d range; values of keys outside [i0, len) masked to zero
+    // ---- O^T += V^T P^T over this warp's d slice; values of keys outside [i0, len) masked to zero
     const bool full = !skip && key0 >= i0 && key0 + kKeyTile <= len;
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (!full) {
@@ -325,7 +334,7 @@ struct MmaConsumer {
     const uint32_t vaddr =
         smem_u32(vs) + rr * GSV + (mi >> 1) * RBV + (mi & 1) * 16 + warp * DW * 2;
 #pragma unroll
-    for (int j = 0; j < KS; ++j) {
+    for (int j = 0; j < KSP; ++j) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(vaddr + j * 32, a0, a1, a2, a3);
       a0 &= mlo;
@@ -352,7 +361,7 @@ struct MmaConsumer {
   }
 
   // Write this partition's (m, l, o) of every real column: every warp writes
-  // its d range; warp 0 the scalars.  Column j -> workspace row (b, j / G, h0 + j % G).
+  // its d slice; warp 0 the scalars.  Column j -> workspace row (b, j / G, h0 + j % G).
   __device__ void write_partial(const PartialArgs &a, int b, int h0, int p) const {
     const int P = a.num_splits, d0 = warp * DW;
 #pragma unroll
@@ -365,7 +374,7 @@ struct MmaConsumer {
             (((size_t)b * tokens + t) * a.num_q_heads + h0 + jc % G) * P + p;
         float *dst = a.ws_o + row * D + d0 + r;
 #pragma unroll
-        for (int j = 0; j < KS; ++j) {
+        for (int j = 0; j < KSP; ++j) {
           dst[16 * j] = o[nt][j][e];
           dst[16 * j + 8] = o[nt][j][2 + e];
         }
@@ -401,6 +410,7 @@ struct SimtConsumer {
   // four consumer warps, two when a stage is too big for four of them
   static constexpr int kWarps = (D * (int)sizeof(T) > 1024) ? 2 : 4;
   static constexpr bool kCooperative = false;  // warp w takes tiles w, w + kWarps, ...
+  static constexpr int kMinBlocks = 1;
   static constexpr int kRowBytesK = D * (int)sizeof(T), kRowBytesV = D * (int)sizeof(T);
   using Geom = RingGeom<kRowBytesK, kRowBytesV, kKeyTile, kWarps>;  // one copy per tile
 
@@ -615,11 +625,12 @@ __device__ __forceinline__ void merge_warp_states(const C &cons, const PartialAr
 }
 
 template <class C>
-__global__ void __launch_bounds__((C::kWarps + 1) * 32, 1) pskv_partial_kernel(const PartialArgs a) {
+__global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
+    pskv_partial_kernel(const PartialArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using Geom = typename C::Geom;
   using S = PartialSmem<C>;
-  constexpr int D = C::D, G = C::G, NS = Geom::kStages;
+  constexpr int G = C::G, NS = Geom::kStages;
   constexpr int RBK = C::kRowBytesK, RBV = C::kRowBytesV;  // bytes of a K row, a V row
   constexpr int TBK = Geom::kTileBytesK;
   constexpr int R = Geom::kRowsPerCopy;
