@@ -77,6 +77,9 @@ def _load():
         lib.orc_decode_multirow_direct.argtypes = [P, P, P, I, P, I, I, I, D, P]
         lib.orc_partial_scratch_bytes.argtypes = [I64, I64, I64, I64, P, P, P, P]
         lib.orc_num_threads.argtypes = []
+        lib.orc_prep_head.argtypes = [P, I, D, P, I, P, P, P]
+        lib.orc_prep_tokens.argtypes = [P, I, I64, I, I, I, I, I, I, I, I, D, P, P, P, P, I, P, I,
+                                        P, P, P]
         _lib = lib
     return _lib
 
@@ -258,3 +261,39 @@ def partial_scratch_bytes(batch, num_q_heads, head_dim_v, num_splits):
                                              *[ctypes.byref(x) for x in vals]),
            "partial_scratch_bytes")
     return tuple(int(x.value) for x in vals)
+
+
+# ---- K/V prep ------------------------------------------------------------------
+
+def prep_head(x, eps, w=None, cos=None, sin=None):
+    """One head row: RMS-normalise, multiply by w, rotate the first 2*len(cos)
+    columns as pairs (i, i + len(cos))."""
+    x = _c(x, np.float64)
+    w = _c(w, np.float64)
+    cos, sin = _c(cos, np.float64), _c(sin, np.float64)
+    rot = 0 if cos is None else 2 * cos.shape[0]
+    out = np.zeros(x.shape[0], np.float64)
+    _check(_load().orc_prep_head(_ptr(x), x.shape[0], eps, _ptr(w), rot, _ptr(cos), _ptr(sin),
+                                 _ptr(out)), "prep_head")
+    return out
+
+
+def prep_tokens(x, q_col, k_col, v_col, num_q_heads, num_kv_heads, head_dim, eps, w_q, w_k,
+                rope_cos, rope_sin, rope_pos, folded=False):
+    """Prep n tokens from projection rows x [n, stride] (uint16 bf16 bits or
+    float32).  rope_cos / rope_sin are float32 [max_pos, rot/2].  Returns fp64
+    (q [n, Hq, D], k [n, Hkv, D], v [n, Hkv, D])."""
+    x, xd = _data(x)
+    n = x.shape[0]
+    rope_cos, rope_sin = _c(rope_cos, np.float32), _c(rope_sin, np.float32)
+    w_q, w_k = _c(w_q, np.float32), _c(w_k, np.float32)
+    pos = _c(rope_pos, np.int32)
+    rot = 2 * rope_cos.shape[1]
+    q = np.zeros((n, num_q_heads, head_dim), np.float64)
+    k = np.zeros((n, num_kv_heads, head_dim), np.float64)
+    v = np.zeros((n, num_kv_heads, head_dim), np.float64)
+    _check(_load().orc_prep_tokens(_ptr(x), xd, x.shape[1], q_col, k_col, v_col, n, num_q_heads,
+                                   num_kv_heads, head_dim, rot, eps, _ptr(w_q), _ptr(w_k),
+                                   _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(pos),
+                                   int(folded), _ptr(q), _ptr(k), _ptr(v)), "prep_tokens")
+    return q, k, v

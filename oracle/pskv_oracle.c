@@ -526,3 +526,88 @@ int orc_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_d
   if (total) *total = all;
   return ORC_OK;
 }
+
+/* ---- K/V prep (the rows a forward writes into the pages) ------------------
+ * pegainfer #1055, Description: the hd512 prep writes the split or the folded
+ * row and folds K's norm weight into the query; pegainfer #1057, Description:
+ * the preps are elementwise with one RMS reduction per head row.  Reading
+ * (the pages give no formula): each head row x of D columns is normalised by
+ * its root mean square, x / sqrt(mean(x^2) + eps), multiplied column-wise by
+ * the head's norm multiplier (none for V), and its first R columns are rotated
+ * as R/2 pairs (i, i + R/2) by the angle whose cosine and sine the caller's
+ * tables hold for the token's position.  V is normalised only. */
+
+int orc_prep_head(const double *x, int d, double eps, const double *w, int rot,
+                  const double *cos_row, const double *sin_row, double *out) {
+  if (!x || !out || d <= 0 || rot < 0 || rot > d || (rot & 1) || !(eps >= 0.0) ||
+      (rot > 0 && (!cos_row || !sin_row)))
+    return ORC_ERR_INVALID;
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+  const double inv = 1.0 / sqrt(ss / d + eps);
+  if (!isfinite(inv)) return ORC_ERR_INVALID;
+  for (int i = 0; i < d; ++i) out[i] = x[i] * inv * (w ? w[i] : 1.0);
+  const int half = rot / 2;
+  for (int i = 0; i < half; ++i) {
+    const double a = out[i], b = out[i + half];
+    out[i] = a * cos_row[i] - b * sin_row[i];
+    out[i + half] = b * cos_row[i] + a * sin_row[i];
+  }
+  return ORC_OK;
+}
+
+int orc_prep_tokens(const void *x, int x_dtype, int64_t x_stride, int q_col, int k_col, int v_col,
+                    int n, int num_q_heads, int num_kv_heads, int d, int rot, double eps,
+                    const float *w_q, const float *w_k, const float *rope_cos,
+                    const float *rope_sin, int max_pos, const int32_t *rope_pos, int folded,
+                    double *q_out, double *k_out, double *v_out) {
+  if (!x || (x_dtype != ORC_F32 && x_dtype != ORC_BF16) || n < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || d <= 0 || rot < 0 || rot > d || (rot & 1) || max_pos <= 0 ||
+      !rope_pos || !q_out || !k_out || !v_out || (rot > 0 && (!rope_cos || !rope_sin)) ||
+      q_col < 0 || k_col < 0 || v_col < 0 ||
+      (int64_t)q_col + (int64_t)num_q_heads * d > x_stride ||
+      (int64_t)k_col + (int64_t)num_kv_heads * d > x_stride ||
+      (int64_t)v_col + (int64_t)num_kv_heads * d > x_stride)
+    return ORC_ERR_INVALID;
+  /* the folded query meets V's columns past R: K's multiplier moves into q
+   * there, which presumes K and V come from one projection row */
+  if (folded && (k_col != v_col || !w_k)) return ORC_ERR_INVALID;
+  double *xin = (double *)malloc(sizeof(double) * (size_t)d);
+  double *wd = (double *)malloc(sizeof(double) * (size_t)d);
+  double *cs = (double *)malloc(sizeof(double) * (size_t)(rot / 2 + 1));
+  double *sn = (double *)malloc(sizeof(double) * (size_t)(rot / 2 + 1));
+  int rc = (xin && wd && cs && sn) ? ORC_OK : ORC_ERR_INVALID;
+  for (int t = 0; t < n && !rc; ++t) {
+    const int pos = rope_pos[t];
+    if (pos < 0 || pos >= max_pos) {
+      rc = ORC_ERR_INVALID;
+      break;
+    }
+    for (int i = 0; i < rot / 2; ++i) {
+      cs[i] = rope_cos[(size_t)pos * (rot / 2) + i];
+      sn[i] = rope_sin[(size_t)pos * (rot / 2) + i];
+    }
+    const size_t base = (size_t)t * (size_t)x_stride;
+    for (int h = 0; h < num_q_heads && !rc; ++h) {
+      for (int i = 0; i < d; ++i) xin[i] = load_elem(x, x_dtype, base + q_col + (size_t)h * d + i);
+      for (int i = 0; i < d; ++i) wd[i] = w_q ? (double)w_q[i] : 1.0;
+      double *o = q_out + ((size_t)t * num_q_heads + h) * d;
+      rc = orc_prep_head(xin, d, eps, wd, rot, cs, sn, o);
+      if (!rc && folded)
+        for (int i = rot; i < d; ++i) o[i] *= (double)w_k[i];
+    }
+    for (int h = 0; h < num_kv_heads && !rc; ++h) {
+      for (int i = 0; i < d; ++i) xin[i] = load_elem(x, x_dtype, base + k_col + (size_t)h * d + i);
+      for (int i = 0; i < d; ++i) wd[i] = w_k ? (double)w_k[i] : 1.0;
+      rc = orc_prep_head(xin, d, eps, wd, rot, cs, sn, k_out + ((size_t)t * num_kv_heads + h) * d);
+      if (rc) break;
+      for (int i = 0; i < d; ++i) xin[i] = load_elem(x, x_dtype, base + v_col + (size_t)h * d + i);
+      rc = orc_prep_head(xin, d, eps, NULL, 0, NULL, NULL, v_out + ((size_t)t * num_kv_heads + h) * d);
+    }
+  }
+  free(xin);
+  free(wd);
+  free(cs);
+  free(sn);
+  return rc;
+}

@@ -163,6 +163,29 @@ int orc_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_d
                               int64_t num_splits, size_t *maxima, size_t *denominators,
                               size_t *numerators, size_t *total);
 
+/* K/V prep of one head row (pegainfer #1055 and #1057, Description: the
+ * elementwise preps with one RMS reduction per head row write the rows the
+ * pages hold).  out = x / sqrt(mean(x^2) + eps) * w (w NULL: 1), then the
+ * first rot columns rotated as pairs (i, i + rot/2):
+ *   out[i] = a cos_i - b sin_i,  out[i + rot/2] = b cos_i + a sin_i
+ * with (a, b) the normalised pair. */
+int orc_prep_head(const double *x, int d, double eps, const double *w, int rot,
+                  const double *cos_row, const double *sin_row, double *out);
+
+/* Prep of n tokens from projection rows x ([n][x_stride], bf16 or f32):
+ * the q band at column q_col (num_q_heads heads of d), the K band at k_col
+ * and the V band at v_col (num_kv_heads heads each).  Token t uses row
+ * rope_pos[t] of the cos/sin tables ([max_pos][rot/2]).  Outputs in fp64:
+ * q_out [n][Hq][d] (normalised with w_q, rotated), k_out [n][Hkv][d]
+ * (w_k, rotated), v_out [n][Hkv][d] (normalised only).  folded: q_out's
+ * columns past rot are further multiplied by w_k (K's norm multiplier folded
+ * into the query; needs k_col == v_col and w_k). */
+int orc_prep_tokens(const void *x, int x_dtype, int64_t x_stride, int q_col, int k_col, int v_col,
+                    int n, int num_q_heads, int num_kv_heads, int d, int rot, double eps,
+                    const float *w_q, const float *w_k, const float *rope_cos,
+                    const float *rope_sin, int max_pos, const int32_t *rope_pos, int folded,
+                    double *q_out, double *k_out, double *v_out);
+
 /* Number of OpenMP threads the oracle's parallel loops use (1 without OpenMP). */
 int orc_num_threads(void);
 

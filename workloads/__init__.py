@@ -237,3 +237,53 @@ def ragged_case(seed: int = 0, n: int = 16, hi: int = 131072) -> PagedCase:
     """16 rows, lengths log-uniform in [1, 131,072], global-layer shape, one
     shared shuffled pool of pages of 256."""
     return make_paged_case(seed, ragged_lengths(seed, n, hi), dtype="bf16", **GLOBAL_SHAPE)
+
+
+# ---- K/V prep inputs -----------------------------------------------------------
+
+@dataclasses.dataclass
+class PrepInputs:
+    """Projection rows of n new tokens and the prep's parameters."""
+    x: np.ndarray            # bf16 bits [n, stride]: q band | K band | V band
+    q_col: int
+    k_col: int
+    v_col: int               # == k_col when K and V share one projection
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    rot: int                 # leading columns rotated
+    eps: float
+    w_q: np.ndarray          # float32 [head_dim]
+    w_k: np.ndarray          # float32 [head_dim]
+    rope_cos: np.ndarray     # float32 [max_pos, rot / 2]
+    rope_sin: np.ndarray
+
+
+def rope_tables(max_pos: int, rot: int, theta: float = 10000.0):
+    """cos / sin tables [max_pos, rot/2] (float32) of angles pos * theta^(-2i/rot)."""
+    i = np.arange(rot // 2, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * theta ** (-2.0 * i / rot)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def make_prep_inputs(seed: int, n: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     rot: int, max_pos: int, shared_kv: bool = False, eps: float = 1e-6,
+                     theta: float = 10000.0) -> PrepInputs:
+    """Random projection rows (each head row N(0,1) times a log-uniform scale in
+    [0.1, 10]), norm multipliers 1 + 0.25 N(0,1), and rotation tables."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 77])))
+    q_w = num_q_heads * head_dim
+    kv_w = num_kv_heads * head_dim
+    q_col, k_col = 0, q_w
+    v_col = k_col if shared_kv else k_col + kv_w
+    stride = v_col + kv_w
+    heads = stride // head_dim
+    x = rng.standard_normal((n, heads, head_dim), dtype=np.float32)
+    x *= np.exp(rng.uniform(math.log(0.1), math.log(10.0), size=(n, heads, 1))).astype(np.float32)
+    cos, sin = rope_tables(max_pos, rot, theta)
+    return PrepInputs(x=bf16_bits(x.reshape(n, stride)), q_col=q_col, k_col=k_col, v_col=v_col,
+                      num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                      rot=rot, eps=eps,
+                      w_q=(1 + 0.25 * rng.standard_normal(head_dim)).astype(np.float32),
+                      w_k=(1 + 0.25 * rng.standard_normal(head_dim)).astype(np.float32),
+                      rope_cos=cos, rope_sin=sin)
