@@ -187,16 +187,23 @@ class ClockSampler:
 # ---- the workload ----------------------------------------------------------------
 
 class Call:
-    """One decode call of the step: a pool (and rotating copies), its inputs and outputs."""
+    """One decode call of the step: a pool (and rotating copies), its inputs and outputs.
 
-    def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1):
+    With ``prep`` the step's new tokens arrive as projection rows: the fused
+    K/V prep normalises and rotates them, writes K and V into their pages and
+    the prepared queries into ``q`` (one launch); without it the K/V rows are
+    copied into the pages as they are (kv_append_rows) and ``q`` is given."""
+
+    def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1, prep=False):
         import torch
         import paged_split_kv_attn_gb300 as pskv
         self.name, self.case, self.windowed = name, case, windowed
         self.tokens = tokens  # query tokens per row: > 1 is a verify window (multi-row decode)
         self.splits = splits
+        self.prep = prep
         bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
             torch.bfloat16).to(dev)
+        f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
         k0, v0 = bf(case.k_pool), bf(case.v_pool)
         self.k = [k0] + [k0.clone() for _ in range(rotate - 1)]
         self.v = [v0] + [v0.clone() for _ in range(rotate - 1)]
@@ -212,9 +219,9 @@ class Call:
         self.window_lo = None if case.window_lo is None else torch.from_numpy(case.window_lo).to(dev)
         b, hq, d = case.q.shape
         hkv = case.num_kv_heads
-        # the step's new token: its K/V row goes to the last position of each row
-        self.pos = [int(n) - 1 for n in case.seq_lens]
-        self.rows = list(range(b))
+        # the step's new tokens: the last `tokens` positions of each row
+        self.rows = [r for r in range(b) for _ in range(tokens)]
+        self.pos = [int(case.seq_lens[r]) - tokens + t for r in range(b) for t in range(tokens)]
         self.row_of = torch.tensor(self.rows, dtype=torch.int32, device=dev)
         self.pos_of = torch.tensor(self.pos, dtype=torch.int32, device=dev)
         ps = case.page_size
@@ -222,6 +229,18 @@ class Call:
                                   for r, p in zip(self.rows, self.pos)]).contiguous()
         self.v_new = torch.stack([v0[int(case.page_tables[r, p // ps]), :, p % ps]
                                   for r, p in zip(self.rows, self.pos)]).contiguous()
+        if prep:
+            # global layers: K and V from one projection row, the first quarter
+            # rotated; sliding layers: separate bands, the whole head rotated
+            fp = 0 if case.first_pos is None else int(case.first_pos.max())
+            rot = d if windowed else case.k_pool.shape[3] if case.folded else d // 4
+            self.prep_in = W.make_prep_inputs(len(self.rows) + hq, len(self.rows), hq, hkv, d, rot,
+                                              fp + int(case.seq_lens.max()),
+                                              shared_kv=not windowed)
+            pi = self.prep_in
+            self.x = bf(pi.x)
+            self.w_q, self.w_k = f32(pi.w_q), f32(pi.w_k)
+            self.rope_cos, self.rope_sin = f32(pi.rope_cos), f32(pi.rope_sin)
         self.out = torch.empty(tuple(self.q.shape[:-1]) + (d,), dtype=torch.bfloat16, device=dev)
         self.ws = pskv.workspace(b * tokens, hq, d, splits, dev)
         self.bytes = case.kv_bytes()
@@ -230,13 +249,24 @@ class Call:
 
     def step_inputs(self) -> dict:
         """The tensors a decode step brings from the host (rebound by pack())."""
+        if self.prep:
+            return {"x": self.x, "pos_of": self.pos_of}
         return {"q": self.q, "k_new": self.k_new, "v_new": self.v_new, "pos_of": self.pos_of}
 
     def run(self, it: int, events=None):
         import paged_split_kv_attn_gb300 as pskv
         layout = self.layouts[it % len(self.layouts)]
-        pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of, self.tables,
-                            self.pages_of_row)
+        if self.prep:
+            pi = self.prep_in
+            n, hq, d = len(self.rows), self.q.shape[-2], self.q.shape[-1]
+            pskv.kv_prep_append(layout, self.x, pi.q_col, pi.k_col, pi.v_col, hq, self.row_of,
+                                self.pos_of, self.tables, self.pages_of_row, pi.rot, pi.eps,
+                                w_q=self.w_q, w_k=self.w_k, rope_cos=self.rope_cos,
+                                rope_sin=self.rope_sin, first_pos=self.first_pos,
+                                q_out=self.q.view(n, hq, d))
+        else:
+            pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of,
+                                self.tables, self.pages_of_row)
         if self.tokens > 1:
             pskv.decode_attn_multirow(layout, self.q, self.tables, self.lens, self.lens_host,
                                       self.case.scale, num_splits=self.splits, workspace=self.ws,
@@ -294,23 +324,24 @@ class Packed:
 def make_extra_calls(args, dev):
     """Calls measured one at a time beside the step: the folded format and
     verify windows of the global shape (multi-row decode)."""
+    prep = args.append == "prep"
     calls = [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev,
-                  ROTATE) for ctx in args.folded_contexts]
+                  ROTATE, prep=prep) for ctx in args.folded_contexts]
     for t in args.verify_tokens:
         ctx = args.verify_context
         calls.append(Call(f"verify_{ctx}x{t}", W.global_case(ctx, seed=ctx + 2), False,
-                          args.splits, dev, ROTATE, tokens=t))
+                          args.splits, dev, ROTATE, tokens=t, prep=prep))
     return calls
 
 
 def make_calls(args, dev):
-    calls = []
+    calls, prep = [], args.append == "prep"
     for ctx in args.contexts:
         calls.append(Call(f"global_{ctx}", W.global_case(ctx, seed=ctx), False, args.splits, dev,
-                          ROTATE))
+                          ROTATE, prep=prep))
     if not args.no_window:
         calls.append(Call(f"window_{WINDOW_RESIDENCY}", W.window_case(WINDOW_RESIDENCY, seed=7),
-                          True, args.window_splits, dev, ROTATE))
+                          True, args.window_splits, dev, ROTATE, prep=prep))
     return calls
 
 
@@ -347,6 +378,11 @@ def parse():
     ap.add_argument("--splits", type=int, default=0, help="global-layer split count (0 = auto)")
     ap.add_argument("--window-splits", type=int, default=0)
     ap.add_argument("--no-window", action="store_true")
+    ap.add_argument("--append", choices=["prep", "copy"], default="copy",
+                    help="new tokens of the step: K/V rows copied into the pages, or projection "
+                         "rows through the fused K/V prep")
+    ap.add_argument("--no-prep-step", action="store_true",
+                    help="skip timing the step with the fused K/V prep beside the headline step")
     ap.add_argument("--folded-contexts", type=int, nargs="*", default=[40002],
                     help="contexts of the folded-format decode timed beside the step")
     ap.add_argument("--verify-tokens", type=int, nargs="*", default=[2, 4],
@@ -407,6 +443,9 @@ def config_dict(args):
             {"batch": 1, "num_q_heads": 32, "num_kv_heads": 16, "head_dim": 256,
              "page_size": 64, "window": W.WINDOW, "residency": WINDOW_RESIDENCY,
              "splits": args.window_splits or "auto"},
+            "new_tokens": ("projection rows through the fused K/V prep (RMS norm, rotation, "
+                           "page write, prepared query) in one launch" if args.append == "prep"
+                           else "K/V rows copied into the pages (kv_append_rows)"),
             "kv_dtype": "bf16", "accumulate": "f32", "out_dtype": "bf16",
             "l2": f"inputs larger than L2: {ROTATE} rotating pool copies, >400 MB of K/V per step",
             "parallelism": "replicas"}
@@ -446,28 +485,34 @@ def main():
         if c.status[0].item() != 0:
             raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
 
-    # ---- the step as CUDA graphs: one graph per pool copy, captured once
-    graphs = None
-    if not args.eager:
-        graphs = []
+    def capture(step_calls):
+        """One CUDA graph per pool copy of the given calls, captured once; returns
+        (graphs, library launches per replay)."""
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            for c in calls:  # warm the capture path (plans, attributes) outside capture
+            for c in step_calls:  # warm the capture path (plans, attributes) outside capture
                 c.run(0)
         stream.wait_stream(side)
         torch.cuda.synchronize()
         n0 = pskv.pskv_kernel_launches()
+        gs = []
         for r in range(ROTATE):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                for c in calls:
+                for c in step_calls:
                     c.run(r)
-            graphs.append(g)
-        launches_per_step = (pskv.pskv_kernel_launches() - n0) / ROTATE
-        for r in range(ROTATE):
-            graphs[r].replay()
+            gs.append(g)
+        per = (pskv.pskv_kernel_launches() - n0) / ROTATE
+        for g in gs:
+            g.replay()
         torch.cuda.synchronize()
+        return gs, per
+
+    # ---- the step as CUDA graphs: one graph per pool copy, captured once
+    graphs = None
+    if not args.eager:
+        graphs, launches_per_step = capture(calls)
 
     def timed(run_step):
         """K steps between events on the stream, barrier and synchronize on both sides."""
@@ -529,17 +574,20 @@ def main():
                             "note": ("folded format" if c.tokens == 1 else
                                      f"verify window of {c.tokens} tokens")
                             + ", measured beside the step (not in value)"}
+    # each call replayed from its own graphs, so host launch overhead stays out
     flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
     for c in calls + extra:
+        cg, _ = capture([c])
         times = []
         for it in range(max(5, min(args.steps, 30))):
             flush.sum()
             b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b.record(stream)
-            c.run(it)
+            cg[it % ROTATE].replay()
             e.record(stream)
             torch.cuda.synchronize()
             times.append(b.elapsed_time(e) * 1e3)
+        del cg
         per_call[c.name]["us_per_call_median"] = statistics.median(times)
         per_call[c.name]["GBps_per_call"] = c.bytes / (statistics.median(times) * 1e-6) / 1e9
         per_call[c.name]["splits"] = c.splits or (
@@ -571,6 +619,27 @@ def main():
             c.splits = args.splits
             c.ws = pskv.workspace(1, 32, 512, args.splits, dev)
     del flush
+
+    # the same step with the fused K/V prep in place of the row copy (projection
+    # rows in, normalised and rotated K/V written into the pages, queries out)
+    prep_step = None
+    if args.append == "copy" and not args.no_prep_step and graphs is not None:
+        pargs = argparse.Namespace(**{**vars(args), "append": "prep"})
+        pcalls = make_calls(pargs, dev)
+        for it in range(args.warmup):
+            for c in pcalls:
+                c.run(it)
+        pgraphs, plaunch = capture(pcalls)
+        pms = timed(lambda it: pgraphs[it % ROTATE].replay())
+        for c in pcalls:
+            if c.status[0].item() != 0:
+                raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
+        prep_step = {"ms_per_step": pms, "unit": "GB/s",
+                     "value": whole_job_gbps(step_bytes, dist.world, pms),
+                     "launches_per_step": plaunch,
+                     "note": "the step with kv_prep_append (projection rows: RMS norm, rotation, "
+                             "page write, prepared queries) in place of kv_append_rows"}
+        del pgraphs, pcalls
 
     # end-to-end through the public calls: each step copies its inputs in from
     # pinned host memory (one copy) and its outputs back (one copy)
@@ -608,6 +677,8 @@ def main():
             "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
     if sweep is not None:
         line["split_sweep_us"] = sweep
+    if prep_step is not None:
+        line["prep_step"] = prep_step
     line["step_launch"] = ("CUDA graph replay (one graph per pool copy, captured once)"
                            if graphs is not None else "eager stream launches")
     line["eager"] = {"ms_per_step": eager_ms, "unit": "GB/s",

@@ -73,6 +73,7 @@ typedef struct CUevent_st *pskv_event_t;
 #define PSKV_FAULT_WAIT_TIMEOUT 8u  /* a bounded wait on a copy expired: the partition was dropped */
 #define PSKV_FAULT_EMPTY_ROW 16u    /* a row had no attended key: its output was written as zeros */
 #define PSKV_FAULT_BAD_STATE 32u    /* merge input with m = -inf but l != 0, or a NaN m: treated as empty */
+#define PSKV_FAULT_BAD_POSITION 64u /* a prep token whose rotation position is outside the table: skipped */
 
 /* ---- limits ---------------------------------------------------------------- */
 #define PSKV_MAX_SPLITS 1024       /* most partitions one decode call may use */
@@ -157,6 +158,54 @@ int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_n
                    const int32_t *pages_of_row, int32_t batch,
                    const int32_t *row_of_host, const int32_t *pos_of_host,
                    const int32_t *pages_of_row_host, pskv_stream_t stream);
+
+/* Rotation and normalisation parameters of kv_prep_append. */
+typedef struct pskv_prep_desc {
+  int32_t rot_dims;       /* leading columns of each head row rotated: even, 0..head_dim */
+  float eps;              /* added to the mean square before the square root */
+  const float *w_q;       /* device float[head_dim], 16-byte aligned: query norm
+                             multiplier, or NULL (1) */
+  const float *w_k;       /* device float[head_dim], 16-byte aligned: key norm
+                             multiplier, or NULL (1); required for a folded pool */
+  const float *rope_cos;  /* device float[max_pos][rot_dims / 2] */
+  const float *rope_sin;  /* device float[max_pos][rot_dims / 2] */
+  int32_t max_pos;        /* rows of the tables */
+} pskv_prep_desc;
+
+/* K/V prep with the page write fused in (pegainfer #1055, Description: the
+ * hd512 prep writes the split or the folded row and folds K's norm weight
+ * into the query; pegainfer #1057, Description: elementwise preps with one RMS
+ * reduction per head row; TensorFold #1619, "Writes" and "Leasing").  For
+ * each new token t (n of them) it takes the projection row
+ *   x          device bf16 [n][x_stride], 16-byte aligned, x_stride a multiple of 8;
+ *              the query band starts at column q_col (num_q_heads head rows of
+ *              head_dim), the key band at k_col and the value band at v_col
+ *              (num_kv_heads head rows each); columns multiples of 8
+ * and computes per head row r of head_dim columns
+ *   r' = r / sqrt(mean(r^2) + eps) * w        (w = w_q for q, w_k for K, 1 for V)
+ * then, for q and K, turns the first rot_dims columns as pairs (i, i + rot/2):
+ *   r''[i] = a cos - b sin,  r''[i + rot/2] = b cos + a sin
+ * with (a, b) = (r'[i], r'[i + rot/2]) and cos, sin = table row p, column i,
+ * p = first_pos[row_of[t]] + pos_of[t] (first_pos NULL: 0).  K (its first
+ * head_dim_k columns: all of them in a split pool, the rotated quarter in a
+ * folded one) and V go straight into page slot pos_of[t] of table row
+ * row_of[t], as kv_append_rows would place them; the prepared query goes to
+ *   q_out      device bf16 [n][num_q_heads][head_dim], 16-byte aligned
+ * and, for a folded pool, its columns past rot_dims are further multiplied by
+ * w_k, which makes q_out the folded query decode_attn_* expect.  A folded pool
+ * needs rot_dims == head_dim_k, k_col == v_col (K and V from one projection)
+ * and w_k.  Values are computed in f32 and rounded to nearest even bf16.
+ * Checks, the host copies and the device fault bits are those of
+ * kv_append_rows, plus PSKV_FAULT_BAD_POSITION for a table row p outside
+ * [0, max_pos) (that token is skipped).  bf16 pools only.
+ * Errors: INVALID_ARG, UNSUPPORTED, PAST_PAGES (from the host copies), CUDA. */
+int kv_prep_append(const pskv_layout *layout, const pskv_prep_desc *prep, const void *x,
+                   int64_t x_stride, int32_t q_col, int32_t k_col, int32_t v_col, int32_t n,
+                   int32_t num_q_heads, const int32_t *row_of, const int32_t *pos_of,
+                   const int32_t *first_pos, const int32_t *page_tables, int32_t table_stride,
+                   const int32_t *pages_of_row, int32_t batch, const int32_t *row_of_host,
+                   const int32_t *pos_of_host, const int32_t *pages_of_row_host, void *q_out,
+                   pskv_stream_t stream);
 
 /* Split-KV decode: one query token per row.
  *   q              device [batch][num_q_heads][head_dim_v], the pool's dtype (for a

@@ -34,6 +34,7 @@ PSKV_FAULT_BAD_LENGTH = 4
 PSKV_FAULT_WAIT_TIMEOUT = 8
 PSKV_FAULT_EMPTY_ROW = 16
 PSKV_FAULT_BAD_STATE = 32
+PSKV_FAULT_BAD_POSITION = 64
 
 PSKV_MAX_SPLITS = 1024
 PSKV_AUTO_MAX_SPLITS = 256
@@ -43,7 +44,7 @@ PSKV_MAX_WINDOW_TOKENS = 64
 PSKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 # Every function the header declares, in the header's order.
-EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows",
+EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows", "kv_prep_append",
            "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
@@ -66,6 +67,12 @@ class LayoutDesc(ctypes.Structure):
                 ("head_dim_v", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("format", ctypes.c_int32), ("k_pool", ctypes.c_void_p),
                 ("v_pool", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+class PrepDesc(ctypes.Structure):
+    _fields_ = [("rot_dims", ctypes.c_int32), ("eps", ctypes.c_float), ("w_q", ctypes.c_void_p),
+                ("w_k", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+                ("rope_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32)]
 
 
 class DecodeOpts(ctypes.Structure):
@@ -91,6 +98,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.paged_kv_layout_destroy.argtypes = [P]
     lib.paged_kv_layout_destroy.restype = None
     lib.kv_append_rows.argtypes = [P, P, P, P, P, I32, P, I32, P, I32, P, P, P, P]
+    lib.kv_prep_append.argtypes = [P, ctypes.POINTER(PrepDesc), P, I64, I32, I32, I32, I32, I32,
+                                   P, P, P, P, I32, P, I32, P, P, P, P, P]
     lib.decode_attn_splitkv.argtypes = [P, P, P, I32, P, P, I32, I32, F, I32, P, SZ, P, I32, P, P]
     lib.decode_attn_windowed.argtypes = [P, P, P, I32, P, P, P, P, I32, I32, F, I32, P, SZ, P,
                                          I32, P, P]
@@ -259,6 +268,39 @@ def kv_append_rows(layout: Layout, k_new, v_new, row_of, pos_of, page_tables, pa
                               page_tables.shape[1], _dev(pages_of_row, "pages_of_row", torch.int32),
                               pages_of_row.numel(), hr, hp, hl, _stream(stream)),
            "kv_append_rows")
+
+
+def kv_prep_append(layout: Layout, x, q_col: int, k_col: int, v_col: int, num_q_heads: int,
+                   row_of, pos_of, page_tables, pages_of_row, rot_dims: int, eps: float,
+                   w_q=None, w_k=None, rope_cos=None, rope_sin=None, first_pos=None, q_out=None,
+                   host=None, stream=None) -> torch.Tensor:
+    """K/V prep of n tokens with the page write fused in: ``x`` [n, stride] bf16
+    projection rows; K and V rows go into the pages, the prepared queries into
+    ``q_out`` [n, num_q_heads, head_dim] (returned).  ``host`` = (row_of, pos_of,
+    pages_of_row) host copies for the up-front refusal."""
+    lib = load_library()
+    n = int(row_of.numel())
+    d = layout.desc.head_dim_v
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [n, stride] with unit column stride")
+    if q_out is None:
+        q_out = torch.empty((n, num_q_heads, d), dtype=torch.bfloat16, device=x.device)
+    hr = hp = hl = None
+    if host is not None:
+        hr, hp, hl = (_host_i32(v, name) for v, name in zip(host, ("row_of", "pos_of", "pages")))
+    opt = lambda t, name: None if t is None else _dev(t, name, torch.float32)
+    desc = PrepDesc(rot_dims=rot_dims, eps=eps, w_q=opt(w_q, "w_q"), w_k=opt(w_k, "w_k"),
+                    rope_cos=opt(rope_cos, "rope_cos"), rope_sin=opt(rope_sin, "rope_sin"),
+                    max_pos=0 if rope_cos is None else rope_cos.shape[0])
+    _check(lib.kv_prep_append(
+        layout.handle, ctypes.byref(desc), _dev(x, "x", torch.bfloat16), x.stride(0), q_col, k_col,
+        v_col, n, num_q_heads, _dev(row_of, "row_of", torch.int32),
+        _dev(pos_of, "pos_of", torch.int32),
+        None if first_pos is None else _dev(first_pos, "first_pos", torch.int32),
+        _dev(page_tables, "page_tables", torch.int32), page_tables.shape[1],
+        _dev(pages_of_row, "pages_of_row", torch.int32), pages_of_row.numel(), hr, hp, hl,
+        _dev(q_out, "q_out", torch.bfloat16), _stream(stream)), "kv_prep_append")
+    return q_out
 
 
 def decode_attn_workspace_bytes(batch: int, num_q_heads: int, head_dim_v: int,

@@ -256,6 +256,82 @@ int kv_append_rows(const pskv_layout *layout, const void *k_new, const void *v_n
   return PSKV_OK;
 }
 
+int kv_prep_append(const pskv_layout *layout, const pskv_prep_desc *prep, const void *x,
+                   int64_t x_stride, int32_t q_col, int32_t k_col, int32_t v_col, int32_t n,
+                   int32_t num_q_heads, const int32_t *row_of, const int32_t *pos_of,
+                   const int32_t *first_pos, const int32_t *page_tables, int32_t table_stride,
+                   const int32_t *pages_of_row, int32_t batch, const int32_t *row_of_host,
+                   const int32_t *pos_of_host, const int32_t *pages_of_row_host, void *q_out,
+                   pskv_stream_t stream) {
+  if (!layout || !prep || n < 0 || batch < 1 || table_stride < 1 || num_q_heads < 1)
+    return PSKV_ERR_INVALID_ARG;
+  const pskv_layout_desc &d = layout->d;
+  if (d.kv_dtype != PSKV_DTYPE_BF16) return PSKV_ERR_UNSUPPORTED;
+  if (num_q_heads % d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
+  const int hd = d.head_dim_v, rot = prep->rot_dims;
+  const bool folded = d.format == PSKV_FORMAT_FOLDED;
+  if (rot < 0 || rot > hd || (rot & 1) || !(prep->eps >= 0.f) || !std::isfinite(prep->eps))
+    return PSKV_ERR_INVALID_ARG;
+  if (rot > 0 && (!prep->rope_cos || !prep->rope_sin || prep->max_pos < 1))
+    return PSKV_ERR_INVALID_ARG;
+  if (folded && (rot != d.head_dim_k || k_col != v_col || !prep->w_k)) return PSKV_ERR_UNSUPPORTED;
+  if (x_stride < 8 || x_stride % 8 != 0 || q_col < 0 || k_col < 0 || v_col < 0 || q_col % 8 ||
+      k_col % 8 || v_col % 8 || (int64_t)q_col + (int64_t)num_q_heads * hd > x_stride ||
+      (int64_t)k_col + (int64_t)d.num_kv_heads * hd > x_stride ||
+      (int64_t)v_col + (int64_t)d.num_kv_heads * hd > x_stride)
+    return PSKV_ERR_INVALID_ARG;
+  if (n == 0) return PSKV_OK;
+  if (!x || !row_of || !pos_of || !page_tables || !pages_of_row || !q_out)
+    return PSKV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q_out, 16) || !aligned(prep->w_q, 16) ||
+      !aligned(prep->w_k, 16))
+    return PSKV_ERR_INVALID_ARG;
+  const int hosts = (row_of_host != nullptr) + (pos_of_host != nullptr) +
+                    (pages_of_row_host != nullptr);
+  if (hosts != 0 && hosts != 3) return PSKV_ERR_INVALID_ARG;
+  if (hosts == 3) {
+    const int rc = check_append_host(layout, n, table_stride, batch, row_of_host, pos_of_host,
+                                     pages_of_row_host);
+    if (rc) return rc;
+  }
+  PrepArgs a;
+  a.x = x;
+  a.x_stride = x_stride;
+  a.q_col = q_col;
+  a.k_col = k_col;
+  a.v_col = v_col;
+  a.n = n;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = d.num_kv_heads;
+  a.d = hd;
+  a.rot = rot;
+  a.eps = prep->eps;
+  a.w_q = prep->w_q;
+  a.w_k = prep->w_k;
+  a.rope_cos = prep->rope_cos;
+  a.rope_sin = prep->rope_sin;
+  a.max_pos = rot > 0 ? prep->max_pos : 0x7fffffff;
+  a.row_of = row_of;
+  a.pos_of = pos_of;
+  a.first_pos = first_pos;
+  a.page_tables = page_tables;
+  a.table_stride = table_stride;
+  a.pages_of_row = pages_of_row;
+  a.batch = batch;
+  a.k_pool = d.k_pool;
+  a.v_pool = d.v_pool;
+  a.num_pages = d.num_pages;
+  a.page_size = d.page_size;
+  a.k_cols = d.head_dim_k;
+  a.folded = folded ? 1 : 0;
+  a.q_out = q_out;
+  a.status = d.status;
+  const cudaError_t e = launch_prep(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return PSKV_OK;
+}
+
 int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t *page_tables,
                         int32_t table_stride, const int32_t *seq_lens_host,
                         const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,

@@ -86,6 +86,38 @@ struct AppendArgs {
   int32_t *status;
 };
 
+struct PrepArgs {
+  const void *x;          // bf16 projection rows [n][x_stride]
+  long long x_stride;     // elements per projection row
+  int q_col, k_col, v_col;  // first column of the q, K and V bands
+  int n;                  // tokens
+  int num_q_heads;
+  int num_kv_heads;
+  int d;                  // head dim
+  int rot;                // leading columns rotated (even)
+  float eps;
+  const float *w_q;       // [d] or null (1)
+  const float *w_k;       // [d] or null (1)
+  const float *rope_cos;  // [max_pos][rot / 2]
+  const float *rope_sin;
+  int max_pos;
+  const int32_t *row_of;  // [n] table row of each token
+  const int32_t *pos_of;  // [n] key index of each token in its row
+  const int32_t *first_pos;  // [batch] position of key 0 of each row, or null (0)
+  const int32_t *page_tables;
+  int table_stride;
+  const int32_t *pages_of_row;
+  int batch;
+  void *k_pool;
+  void *v_pool;
+  long long num_pages;
+  int page_size;
+  int k_cols;             // stored K columns: d (split) or rot (folded)
+  int folded;             // fold K's multiplier into q past rot
+  void *q_out;            // bf16 [n][num_q_heads][d]
+  int32_t *status;
+};
+
 // Host-side launchers (one per kernel family).  They return a CUDA error code.
 // The tensor-core family takes `nt` n-tiles of 8 query columns (group x tokens <= 8 nt).
 cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, bool folded, int nt,
@@ -99,6 +131,7 @@ cudaError_t occupancy_partial_simt_f32(int head_dim, int group, int *ctas);
 cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
 
 // Launch `kernel` with programmatic dependent launch allowed: it may start
 // while the previous kernel on the stream is still running, and must execute

@@ -183,6 +183,41 @@ def test_multirow_refusals_happen_before_any_launch(lib):
         lib.paged_kv_layout_destroy(f32)
 
 
+def _prep_rc(lib, layout, rot=128, stride=40 * 512, cols=(0, 32 * 512, 36 * 512), w_k=0x90000,
+             host=None, n=1):
+    desc = B.PrepDesc(rot_dims=rot, eps=1e-6, w_q=0x80000, w_k=w_k, rope_cos=0xa0000,
+                      rope_sin=0xb0000, max_pos=4096)
+    hr = hp = hl = None
+    if host is not None:
+        hr, hp, hl = ((ctypes.c_int32 * len(v))(*v) for v in host)
+    return lib.kv_prep_append(layout, ctypes.byref(desc), 0x10000, stride, cols[0], cols[1],
+                              cols[2], n, 32, 0x20000, 0x30000, None, 0x40000, 4, 0x50000, 1,
+                              hr, hp, hl, 0x60000, None)
+
+
+def test_prep_refusals_happen_before_any_launch(lib):
+    h = _layout(lib)
+    f32 = _layout(lib, kv_dtype=B.PSKV_DTYPE_F32)
+    folded = _layout(lib, format=B.PSKV_FORMAT_FOLDED, head_dim_k=128)
+    try:
+        assert _prep_rc(lib, f32) == B.PSKV_ERR_UNSUPPORTED             # bf16 pools only
+        assert _prep_rc(lib, h, rot=127) == B.PSKV_ERR_INVALID_ARG      # odd rotation
+        assert _prep_rc(lib, h, rot=514) == B.PSKV_ERR_INVALID_ARG      # wider than the head
+        assert _prep_rc(lib, h, stride=39 * 512) == B.PSKV_ERR_INVALID_ARG  # V band past the row
+        assert _prep_rc(lib, h, cols=(4, 32 * 512, 36 * 512)) == B.PSKV_ERR_INVALID_ARG
+        assert _prep_rc(lib, h, host=([0], [4 * 256], [4])) == B.PSKV_ERR_PAST_PAGES
+        # folded: K and V from one band, K's multiplier given, the rotated quarter stored
+        assert _prep_rc(lib, folded) == B.PSKV_ERR_UNSUPPORTED
+        assert _prep_rc(lib, folded, cols=(0, 32 * 512, 32 * 512), w_k=None) == \
+            B.PSKV_ERR_UNSUPPORTED
+        assert _prep_rc(lib, folded, rot=64, cols=(0, 32 * 512, 32 * 512)) == \
+            B.PSKV_ERR_UNSUPPORTED
+        assert _prep_rc(lib, h, n=0) == 0                                # nothing to do
+    finally:
+        for x in (h, f32, folded):
+            lib.paged_kv_layout_destroy(x)
+
+
 def test_append_past_pages_refused_on_host(lib):
     h = _layout(lib)
     try:
