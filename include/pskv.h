@@ -285,17 +285,18 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
 
 /* Merge P partials per row in two levels by the exact rescaling identity and
  * normalise (gem design, "Candidate ownership and storage"; pegainfer #1055,
- * Description).  Out of place: level 1 writes its group results into
- * `workspace`, never into the inputs.
+ * Description).  One launch: level 1 folds each group of merge_group partials
+ * into a group state held in shared memory (never into the inputs), level 2
+ * folds a row's group states; both in index order.
  *   m, l         device float[rows][num_splits]; m in units of the scaled score
  *   o            device float[rows][num_splits][head_dim_v], 16-byte aligned
  *   head_dim_v   a multiple of 4
  *   out          device [rows][head_dim_v] of out_dtype
- *   workspace    device scratch of merge_partials_workspace_bytes(...) bytes
+ *   workspace    not used (the group states stay on chip): NULL and 0 are fine
  *   status       device int32[4] fault word or NULL
  * The empty state is (m = -inf, l = 0); its o is never used (it may be
- * uninitialised); merging an empty state changes nothing.  Groups are folded
- * in index order. */
+ * uninitialised); merging an empty state changes nothing.  At most 64 groups
+ * per row (num_splits <= 64 * merge_group). */
 int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
                    int32_t num_splits, int32_t head_dim_v, void *out, int32_t out_dtype,
                    void *workspace, size_t workspace_bytes, int32_t *status,
@@ -306,7 +307,7 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
 int decode_attn_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v,
                                 int32_t num_splits, size_t *bytes);
 
-/* Scratch bytes merge_partials needs.  Host-only. */
+/* Scratch bytes merge_partials needs: 0 in this build.  Host-only. */
 int merge_partials_workspace_bytes(int32_t rows, int32_t num_splits, int32_t head_dim_v,
                                    size_t *bytes);
 

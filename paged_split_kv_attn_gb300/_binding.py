@@ -454,10 +454,6 @@ def merge_partials(m, l, o, out=None, out_dtype=None, workspace=None, status=Non
     rows, p, dv = o.shape
     if out is None:
         out = torch.empty((rows, dv), device=o.device, dtype=out_dtype or torch.float32)
-    if workspace is None and p > (merge_group or PSKV_MERGE_GROUP):
-        # group results never outnumber the partials: this bound fits any merge group
-        workspace = torch.empty(rows * p * (dv + 2) * 4 + 1024, dtype=torch.uint8,
-                                device=o.device)
     opts = _opts(merge_group, events)
     _check(lib.merge_partials(_dev(m, "m", torch.float32), _dev(l, "l", torch.float32),
                               _dev(o, "o", torch.float32), rows, p, dv, _dev(out, "out"),

@@ -5,14 +5,15 @@
 // D512 fused split-KV decode design", "Candidate ownership and storage"):
 //   M = max_i m_i,  l = sum_i l_i e^(m_i - M),  o = sum_i o_i e^(m_i - M),
 // which is the pairwise identity applied to all states of a set at once.
-// Level 1 folds groups of up to PSKV_MERGE_GROUP partials of a row into a
-// SEPARATE buffer (pegainfer #1055 folded a group into its own first slot and
-// needed a barrier between the group reads and the store; writing elsewhere
-// removes that race by construction).  Level 2 folds the group results of a
-// row and writes out = o / l.  Folding order is fixed (index order), so the
-// result is deterministic.  An empty state (m = -inf) contributes nothing and
-// its o is never used; an empty state that carries l != 0 (or a NaN m) is
-// flagged PSKV_FAULT_BAD_STATE and treated as empty.
+// Level 1 folds groups of up to PSKV_MERGE_GROUP partials of a row into
+// separate group states (pegainfer #1055 folded a group into its own first
+// slot and needed a barrier between the group reads and the store; here the
+// group states live in shared memory apart from the partials, so that race
+// cannot occur).  Level 2 folds the group states of a row and writes
+// out = o / l.  Folding order is fixed (index order), so the result is
+// deterministic.  An empty state (m = -inf) contributes nothing and its o is
+// never used; an empty state that carries l != 0 (or a NaN m) is flagged
+// PSKV_FAULT_BAD_STATE and treated as empty.
 #include <math_constants.h>
 
 #include "pskv_internal.cuh"
@@ -20,51 +21,47 @@
 namespace pskv {
 
 constexpr int kMergeThreads = 128;
-constexpr int kMaxStates = 64;  // states one level-2 block folds (PSKV_MAX_SPLITS / PSKV_MERGE_GROUP)
+constexpr int kMaxStates = 64;  // states one warp weighs: groups of a row, or partials of a group
 constexpr int kChunk = 16;      // states whose o is loaded together (all loads in flight at once)
 
-// Warp 0 reads the n states' (m, l) in parallel and computes the weights
+// One warp reads n <= 64 states' (m, l) in parallel and computes the weights
 // w_i = e^(m_i - M) (-1 marks an empty state, whose o is skipped), M and l.
+// Every lane returns M and L; the weights go to w_s[0..n).
 template <bool kCoherent = false>
-__device__ void state_weights(const float *m, const float *l, int n, float *w_s, float *M_s,
-                              float *L_s, int32_t *status) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float mi[kMaxStates / 32], li[kMaxStates / 32];
-    bool bad = false;
-    float M = -CUDART_INF_F;
+__device__ __forceinline__ void warp_state_weights(const float *m, const float *l, int n,
+                                                   float *w_s, float &M_out, float &L_out,
+                                                   int32_t *status, int lane) {
+  float mi[kMaxStates / 32], li[kMaxStates / 32];
+  bool bad = false;
+  float M = -CUDART_INF_F;
 #pragma unroll
-    for (int k = 0; k < kMaxStates / 32; ++k) {
-      const int i = lane + 32 * k;
-      mi[k] = i < n ? (kCoherent ? __ldcg(m + i) : m[i]) : -CUDART_INF_F;
-      li[k] = i < n ? (kCoherent ? __ldcg(l + i) : l[i]) : 0.f;
-      if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
-        bad = true;
-        mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
-      }
-      M = fmaxf(M, mi[k]);
+  for (int k = 0; k < kMaxStates / 32; ++k) {
+    const int i = lane + 32 * k;
+    mi[k] = i < n ? (kCoherent ? __ldcg(m + i) : m[i]) : -CUDART_INF_F;
+    li[k] = i < n ? (kCoherent ? __ldcg(l + i) : l[i]) : 0.f;
+    if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
+      bad = true;
+      mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxStates / 32; ++k) {
-      const int i = lane + 32 * k;
-      const bool empty = mi[k] == -CUDART_INF_F;
-      const float w = empty ? 0.f : exp2f((mi[k] - M) * kLog2e);
-      if (i < n) w_s[i] = empty ? -1.f : w;
-      // fixed-order sum: lane partials, then a butterfly (same bits every run)
-      if (!empty) L = fmaf(li[k], w, L);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_fault(status, PSKV_FAULT_BAD_STATE);
-    if (lane == 0) {
-      *M_s = M;
-      *L_s = L;
-    }
+    M = fmaxf(M, mi[k]);
   }
-  __syncthreads();
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxStates / 32; ++k) {
+    const int i = lane + 32 * k;
+    const bool empty = mi[k] == -CUDART_INF_F;
+    const float w = empty ? 0.f : exp2f((mi[k] - M) * kLog2e);
+    if (i < n) w_s[i] = empty ? -1.f : w;
+    // fixed-order sum: lane partials, then a butterfly (same bits every run)
+    if (!empty) L = fmaf(li[k], w, L);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) raise_fault(status, PSKV_FAULT_BAD_STATE);
+  M_out = M;
+  L_out = L;
 }
 
 // Load o_i[d4] of states [i0, i0 + kChunk) (those below n), all in flight at once.
@@ -101,56 +98,76 @@ __device__ __forceinline__ void combine_chunk(float4 &acc, const float4 (&v)[kCh
   }
 }
 
-// Fold the n states of one row: (m, l) weights by warp 0, o by every thread,
-// with the first chunk of each thread's first column loaded before the weights.
-// Calls f(d4, acc) for every column d4 of the row.
-template <bool kCoherent, class F>
-__device__ __forceinline__ void fold_states(const float *m, const float *l, const float *o, int n,
-                                            int dv, float *w_s, float *M_s, float *L_s,
-                                            int32_t *status, F &&f) {
-  const int dv4 = dv / 4;
-  float4 v[kChunk];
-  if ((int)threadIdx.x < dv4) load_chunk<kCoherent>(o, n, dv, threadIdx.x, 0, v);
-  state_weights<kCoherent>(m, l, n, w_s, M_s, L_s, status);
-  for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < n; i0 += kChunk) {
-      if (d4 != (int)threadIdx.x || i0 != 0) load_chunk<kCoherent>(o, n, dv, d4, i0, v);
-      combine_chunk(acc, v, n, i0, w_s);
-    }
-    f(d4, acc);
-  }
-}
+// Both levels in one launch, one block per (row, 64 output columns).  Every
+// block computes the row's level-1 weights (warp w takes groups w, w + 4, ...)
+// and the level-2 weights over the group states; its threads fold, for their
+// column, each group of partials in index order into a shared-memory group
+// accumulator (level 1), then one thread per column folds the group results
+// in index order and normalises (level 2).  The group results never leave the
+// chip, and the arithmetic and its order are those of two separate levels.
+// The first group's numerators are loaded before any weight is known.
+constexpr int kColsPerBlock = 16;                              // float4 columns per block
+constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;     // threads per column
 
-// grid (groups, rows): fold partials [grp*group, min(count, (grp+1)*group)) of a row.
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_level1(const MergeArgs a) {
-  __shared__ float w_s[kMaxStates];
+__global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
+  __shared__ float w_s[PSKV_MAX_SPLITS];             // level-1 weights, by partial
+  __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates], wg_s[kMaxStates];  // group states
+  __shared__ float4 o1_s[kMaxStates][kColsPerBlock];  // group numerators of this block's columns
   __shared__ float M_s, L_s;
-  const int grp = blockIdx.x, row = blockIdx.y;
-  const int ng = (a.count + a.group - 1) / a.group;
-  const int p0 = grp * a.group;
-  const int n = min(a.count - p0, a.group);
-  const size_t base = (size_t)row * a.count + p0;
-  const size_t out_state = (size_t)row * ng + grp;
+  const int row = blockIdx.x;
+  const int c = threadIdx.x % kColsPerBlock, j = threadIdx.x / kColsPerBlock;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dv4 = a.dv / 4, d4 = blockIdx.y * kColsPerBlock + c;
+  const int P = a.count, G = a.group, ng = (P + G - 1) / G;
+  const float *m = a.m + (size_t)row * P, *l = a.l + (size_t)row * P;
+  const float *o = a.o + (size_t)row * P * a.dv;
   pdl_wait();
   pdl_launch_dependents();
-  fold_states<false>(a.m + base, a.l + base, a.o + base * a.dv, n, a.dv, w_s, &M_s, &L_s,
-                     a.status, [&](int d4, float4 acc) {
-                       reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] = acc;
-                     });
-  if (threadIdx.x == 0) {
-    a.m1[out_state] = M_s;
-    a.l1[out_state] = L_s;
+  float4 v[kChunk];
+  if (j < ng && d4 < dv4) load_chunk<false>(o, min(P, j * G + G), a.dv, d4, j * G, v);
+  // level-1 weights and group states
+  for (int g = warp; g < ng; g += kMergeThreads / 32) {
+    const int i0 = g * G, n = min(P, i0 + G) - i0;
+    float Mg, Lg;
+    warp_state_weights<false>(m + i0, l + i0, n, w_s + i0, Mg, Lg, a.status, lane);
+    if (lane == 0) {
+      Mg_s[g] = Mg;
+      Lg_s[g] = Lg;
+    }
   }
-}
-
-// Fold all `n` states of `row` and write the normalised output row.
-template <bool kCoherent>
-__device__ void fold_and_finalize(const float *m, const float *l, const float *o, int n, int row,
-                                  const MergeArgs &a, float *w_s, float &M_s, float &L_s) {
-  const size_t base = (size_t)row * n;
-  fold_states<kCoherent>(m + base, l + base, o + base * a.dv, n, a.dv, w_s, &M_s, &L_s, a.status,
-                         [&](int d4, float4 acc) {
+  __syncthreads();
+  // level-2 weights (warp 0) while every thread folds its groups (level 1)
+  if (warp == 0) {
+    float M, L;
+    warp_state_weights<false>(Mg_s, Lg_s, ng, wg_s, M, L, a.status, lane);
+    if (lane == 0) {
+      M_s = M;
+      L_s = L;
+    }
+  }
+  if (d4 < dv4) {
+    for (int g = j; g < ng; g += kGroupLanes) {
+      const int i0 = g * G, end = min(P, i0 + G);
+      if (g != j) load_chunk<false>(o, end, a.dv, d4, i0, v);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      combine_chunk(acc, v, end, i0, w_s);
+      o1_s[g][c] = acc;
+    }
+  }
+  __syncthreads();
+  // level 2 and normalisation, one thread per column
+  if (j == 0 && d4 < dv4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < ng; ++g) {
+      const float w = wg_s[g];
+      if (w >= 0.f) {
+        const float4 x = o1_s[g][c];
+        acc.x = fmaf(x.x, w, acc.x);
+        acc.y = fmaf(x.y, w, acc.y);
+        acc.z = fmaf(x.z, w, acc.z);
+        acc.w = fmaf(x.w, w, acc.w);
+      }
+    }
     const bool empty_row = (M_s == -CUDART_INF_F);
     const float L = L_s;
     const float4 r = empty_row ? make_float4(0.f, 0.f, 0.f, 0.f)
@@ -163,73 +180,17 @@ __device__ void fold_and_finalize(const float *m, const float *l, const float *o
     } else {
       reinterpret_cast<float4 *>(static_cast<char *>(a.out) + (size_t)row * a.dv * 4)[d4] = r;
     }
-  });
-  if (threadIdx.x == 0 && M_s == -CUDART_INF_F) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
-}
-
-// grid (rows): fold all `n` states of a row and normalise.
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_level2(const float *m, const float *l,
-                                                                   const float *o, int n,
-                                                                   const MergeArgs a) {
-  __shared__ float w_s[kMaxStates];
-  __shared__ float M_s, L_s;
-  pdl_wait();
-  pdl_launch_dependents();
-  fold_and_finalize<false>(m, l, o, n, blockIdx.x, a, w_s, M_s, L_s);
-}
-
-// Both levels in one launch, grid (groups, rows): each block folds one group
-// of partials (level 1) into the group buffer; the block that finishes a row's
-// last group (counted on a per-row counter that the partial kernel zeroed)
-// folds that row's group results (level 2).  The level-2 fold reads the group
-// buffer in index order, so which block finishes last does not change a bit.
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_two_level(const MergeArgs a) {
-  __shared__ float w_s[kMaxStates];
-  __shared__ float M_s, L_s;
-  __shared__ bool last_s;
-  const int grp = blockIdx.x, row = blockIdx.y;
-  const int ng = (a.count + a.group - 1) / a.group;
-  const int p0 = grp * a.group;
-  const int n = min(a.count - p0, a.group);
-  const size_t base = (size_t)row * a.count + p0;
-  pdl_wait();
-  pdl_launch_dependents();
-  const size_t out_state = (size_t)row * ng + grp;
-  fold_states<false>(a.m + base, a.l + base, a.o + base * a.dv, n, a.dv, w_s, &M_s, &L_s,
-                     a.status, [&](int d4, float4 acc) {
-                       reinterpret_cast<float4 *>(a.o1 + out_state * a.dv)[d4] = acc;
-                     });
-  if (threadIdx.x == 0) {
-    a.m1[out_state] = M_s;
-    a.l1[out_state] = L_s;
+    if (empty_row && d4 == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   }
-  // publish this group's result, then count it
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last_s = atomicAdd(a.counters + row, 1u) == (unsigned)(ng - 1);
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  fold_and_finalize<true>(a.m1, a.l1, a.o1, ng, row, a, w_s, M_s, L_s);
 }
 
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
   *launches = 0;
-  if (a.count <= a.group) {  // one group: the second level reads the partials directly
-    *launches = 1;
-    return launch_pdl(pskv_merge_level2, dim3(a.rows), dim3(kMergeThreads), 0, s, a.m, a.l, a.o,
-                      a.count, a);
-  }
   const int ng = (a.count + a.group - 1) / a.group;
-  if (a.counters != nullptr) {  // both levels in one launch
-    *launches = 1;
-    return launch_pdl(pskv_merge_two_level, dim3(ng, a.rows), dim3(kMergeThreads), 0, s, a);
-  }
-  cudaError_t e = launch_pdl(pskv_merge_level1, dim3(ng, a.rows), dim3(kMergeThreads), 0, s, a);
-  if (e != cudaSuccess) return e;
-  *launches = 2;
-  return launch_pdl(pskv_merge_level2, dim3(a.rows), dim3(kMergeThreads), 0, s,
-                    (const float *)a.m1, (const float *)a.l1, (const float *)a.o1, ng, a);
+  if (ng > kMaxStates || a.count > PSKV_MAX_SPLITS || a.group > kChunk) return cudaErrorInvalidValue;
+  const int chunks = (a.dv / 4 + kColsPerBlock - 1) / kColsPerBlock;
+  *launches = 1;
+  return launch_pdl(pskv_merge_cols, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
 }
 
 }  // namespace pskv

@@ -692,10 +692,6 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
 
   const int T = a.num_tokens;
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0 (T = 1)
-  // the merge that follows counts finished groups per (row, token, head): start it at zero
-  if (a.merge_counters != nullptr && p == 0 && g == 0 && cb == 0)
-    for (int h = threadIdx.x; h < T * a.num_q_heads; h += blockDim.x)
-      a.merge_counters[(size_t)b * T * a.num_q_heads + h] = 0u;
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
     const int c0 = cb * C::kCols, c1 = min(c0 + C::kCols, T * G);  // this block's columns
     for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {

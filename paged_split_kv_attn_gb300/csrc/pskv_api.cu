@@ -139,7 +139,6 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.ws_m = reinterpret_cast<float *>(ws + w.m_off);
   a.ws_l = reinterpret_cast<float *>(ws + w.l_off);
   a.ws_o = reinterpret_cast<float *>(ws + w.o_off);
-  a.merge_counters = reinterpret_cast<unsigned int *>(ws + w.cnt_off);
   a.num_pages = d.num_pages;
   a.table_stride = table_stride;
   a.page_size = d.page_size;
@@ -178,13 +177,9 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   m.count = P;
   m.dv = d.head_dim_v;
   m.group = mgroup;
-  m.m1 = reinterpret_cast<float *>(ws + w.m1_off);
-  m.l1 = reinterpret_cast<float *>(ws + w.l1_off);
-  m.o1 = reinterpret_cast<float *>(ws + w.o1_off);
   m.out = out;
   m.out_dtype = out_dtype;
   m.status = d.status;
-  m.counters = a.merge_counters;
   int launched = 0;
   e = launch_merge(m, s, &launched);
   g_launches.fetch_add((uint64_t)launched, std::memory_order_relaxed);
@@ -372,7 +367,6 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
   if (!m || !l || !o || !out || rows < 1 || num_splits < 1 || num_splits > PSKV_MAX_SPLITS ||
       head_dim_v < 4 || head_dim_v % 4 != 0)
     return PSKV_ERR_INVALID_ARG;
-  if (rows > 65535) return PSKV_ERR_UNSUPPORTED;
   if (out_dtype != PSKV_DTYPE_F32 && out_dtype != PSKV_DTYPE_BF16) return PSKV_ERR_INVALID_ARG;
   if (!aligned(o, 16) || !aligned(out, 16) || !aligned(m, 4) || !aligned(l, 4))
     return PSKV_ERR_INVALID_ARG;
@@ -381,10 +375,8 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
   WorkspacePlan w;
   if ((rc = plan_workspace(1, rows, head_dim_v, num_splits, group, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
-  const size_t need = w.cnt_off - w.m1_off;  // only the level-1 sections are used
-  if (w.groups > 1 && (!workspace || workspace_bytes < need)) return PSKV_ERR_WORKSPACE_TOO_SMALL;
-  if (workspace && !aligned(workspace, 16)) return PSKV_ERR_INVALID_ARG;
-  char *ws = static_cast<char *>(workspace);
+  (void)workspace;  // the group states stay on chip: no scratch is needed
+  (void)workspace_bytes;
   MergeArgs a;
   a.m = m;
   a.l = l;
@@ -393,13 +385,9 @@ int merge_partials(const float *m, const float *l, const float *o, int32_t rows,
   a.count = num_splits;
   a.dv = head_dim_v;
   a.group = group;
-  a.m1 = ws ? reinterpret_cast<float *>(ws) : nullptr;
-  a.l1 = ws ? reinterpret_cast<float *>(ws + (w.l1_off - w.m1_off)) : nullptr;
-  a.o1 = ws ? reinterpret_cast<float *>(ws + (w.o1_off - w.m1_off)) : nullptr;
   a.out = out;
   a.out_dtype = out_dtype;
   a.status = status;
-  a.counters = nullptr;  // level 1 and level 2 as two launches
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (opts && opts->partial_begin) {
@@ -434,7 +422,7 @@ int merge_partials_workspace_bytes(int32_t rows, int32_t num_splits, int32_t hea
   WorkspacePlan w;
   const int rc = plan_workspace(1, rows, head_dim_v, num_splits, PSKV_MERGE_GROUP, &w);
   if (rc) return rc;
-  *bytes = w.cnt_off - w.m1_off;
+  *bytes = 0;  // the group states stay on chip
   return PSKV_OK;
 }
 

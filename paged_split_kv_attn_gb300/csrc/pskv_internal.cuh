@@ -34,7 +34,6 @@ struct PartialArgs {
   float *ws_m;                 // [B][Hq][P]
   float *ws_l;                 // [B][Hq][P]
   float *ws_o;                 // [B][Hq][P][D]
-  unsigned int *merge_counters;  // [B][Hq]: zeroed here, counted by the merge
   long long num_pages;
   int table_stride;
   int page_size;
@@ -57,13 +56,9 @@ struct MergeArgs {
   int count;
   int dv;
   int group;
-  float *m1;  // [rows][ceil(count / group)]
-  float *l1;
-  float *o1;  // [rows][ceil(count / group)][dv]
   void *out;  // [rows][dv]
   int out_dtype;
   int32_t *status;
-  unsigned int *counters;  // [rows], zero on entry (two-level merge in one launch), or null
 };
 
 struct AppendArgs {

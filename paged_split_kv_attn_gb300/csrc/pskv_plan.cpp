@@ -39,24 +39,18 @@ int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64
   if (!out || batch < 1 || num_q_heads < 1 || head_dim_v < 1 || splits < 1 || group < 1)
     return PSKV_ERR_INVALID_ARG;
   const int64_t ng = (splits + group - 1) / group;
-  size_t rows, states, ostate, states1, ostate1;
+  size_t rows, states, ostate;
   if (__builtin_mul_overflow((size_t)batch, (size_t)num_q_heads, &rows) ||
       __builtin_mul_overflow(rows, (size_t)splits * 4, &states) ||
-      __builtin_mul_overflow(states, (size_t)head_dim_v, &ostate) ||
-      __builtin_mul_overflow(rows, (size_t)ng * 4, &states1) ||
-      __builtin_mul_overflow(states1, (size_t)head_dim_v, &ostate1))
+      __builtin_mul_overflow(states, (size_t)head_dim_v, &ostate))
     return PSKV_ERR_OVERFLOW;
-  if (states > ((size_t)1 << 60) || ostate > ((size_t)1 << 60) || ostate1 > ((size_t)1 << 60))
+  if (states > ((size_t)1 << 60) || ostate > ((size_t)1 << 60))
     return PSKV_ERR_OVERFLOW;  // keeps the additions below from wrapping
   WorkspacePlan w;
   w.m_off = 0;
   w.l_off = align256(w.m_off + states);
   w.o_off = align256(w.l_off + states);
-  w.m1_off = align256(w.o_off + ostate);
-  w.l1_off = align256(w.m1_off + states1);
-  w.o1_off = align256(w.l1_off + states1);
-  w.cnt_off = align256(w.o1_off + ostate1);
-  w.total = align256(w.cnt_off + rows * 4);
+  w.total = align256(w.o_off + ostate);
   w.groups = (int)ng;
   *out = w;
   return PSKV_OK;

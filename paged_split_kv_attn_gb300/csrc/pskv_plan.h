@@ -18,18 +18,17 @@ struct pskv_layout {
 
 namespace pskv {
 
-// Byte offsets of the workspace sections (each 256-byte aligned).
+// Byte offsets of the workspace sections (each 256-byte aligned): the
+// partials only (the merge keeps its group states on chip).
 struct WorkspacePlan {
-  size_t m_off, l_off, o_off;     // partials: m, l [rows][P], o [rows][P][dv]
-  size_t m1_off, l1_off, o1_off;  // level-1 group results: [rows][ng], [rows][ng][dv]
-  size_t cnt_off;                 // per-row counters of finished level-1 groups: uint32 [rows]
+  size_t m_off, l_off, o_off;  // partials: m, l [rows][P], o [rows][P][dv]
   size_t total;
   int groups;  // ng = ceil(P / group)
 };
 
 int check_layout_desc(const pskv_layout_desc *d);
 
-// Sizes of the decode workspace for `splits` partitions folded in groups of `group`.
+// Sizes of the decode workspace for `splits` partitions (merged in groups of `group`).
 int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64_t splits,
                    int64_t group, WorkspacePlan *out);
 

@@ -72,13 +72,15 @@ def test_size_overflow_fails_closed(lib):
 PSKV_MAX = B.PSKV_MAX_SPLITS
 
 
-def test_workspace_holds_partials_and_group_results(lib):
+def test_workspace_holds_the_partials(lib):
+    """The decode workspace is the partial buffer (256-byte aligned sections);
+    the merge keeps its group states on chip."""
     for p in (1, 16, 17, 32, 256, 1024):
         n = pskv.decode_attn_workspace_bytes(2, 32, 512, p)
         partial = pskv.pskv_partial_scratch_bytes(2, 32, 512, p)[3]
-        groups = -(-p // B.PSKV_MERGE_GROUP)
-        assert n >= partial + 2 * 32 * groups * (512 + 2) * 4
+        assert partial <= n <= partial + 3 * 256
         assert n % 256 == 0
+        assert pskv.merge_partials_workspace_bytes(64, p, 512) == 0
     assert pskv.decode_attn_workspace_bytes(1, 32, 512, 0) == \
         pskv.decode_attn_workspace_bytes(1, 32, 512, B.PSKV_AUTO_MAX_SPLITS)
 
@@ -243,8 +245,9 @@ def test_merge_refusals(lib):
                               None) == B.PSKV_ERR_INVALID_ARG
     assert lib.merge_partials(0x10, 0x10, 0x20, 4, 8, 510, 0x30, 0, None, 0, None, None,
                               None) == B.PSKV_ERR_INVALID_ARG  # dv not a multiple of 4
-    assert lib.merge_partials(0x10, 0x10, 0x20, 4, 40, 512, 0x30, 0, None, 0, None, None,
-                              None) == B.PSKV_ERR_WORKSPACE_TOO_SMALL  # two levels need scratch
+    one = B.DecodeOpts(1, None, None)  # groups of one partial: 65 groups are more than 64
+    assert lib.merge_partials(0x10, 0x10, 0x20, 4, 65, 512, 0x30, 0, None, 0, None,
+                              ctypes.byref(one), None) == B.PSKV_ERR_INVALID_ARG
     opts = B.DecodeOpts(17, None, None)
     assert lib.merge_partials(0x10, 0x10, 0x20, 4, 8, 512, 0x30, 0, None, 0, None,
                               ctypes.byref(opts), None) == B.PSKV_ERR_INVALID_ARG
