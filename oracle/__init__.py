@@ -75,6 +75,7 @@ def _load():
         lib.orc_decode_direct.argtypes = [P, P, P, I, P, P, P, I, I, D, P]
         lib.orc_decode_online.argtypes = [P, P, P, I, P, P, P, I, I, D, I, I, I, P]
         lib.orc_decode_multirow_direct.argtypes = [P, P, P, I, P, I, I, I, D, P]
+        lib.orc_prefill_direct.argtypes = [P, P, P, P, I, P, I, I, I, D, P]
         lib.orc_partial_scratch_bytes.argtypes = [I64, I64, I64, I64, P, P, P, P]
         lib.orc_num_threads.argtypes = []
         lib.orc_prep_head.argtypes = [P, I, D, P, I, P, P, P]
@@ -236,6 +237,21 @@ def decode_multirow_direct(q, k_pool, v_pool, page_tables, seq_lens, scale):
                                               tables.shape[1], _ptr(lens), q.shape[0], q.shape[1],
                                               q.shape[2], scale, _ptr(out)),
            "decode_multirow_direct")
+    return out
+
+
+def prefill_direct(q, cu_q, k_pool, v_pool, page_tables, seq_lens, scale, window=0):
+    """q packed [total, num_q_heads, key width] -> out [total, num_q_heads, dv]:
+    row b's last cu_q[b+1]-cu_q[b] keys are its new tokens, each attending
+    causally (and within `window` keys when window > 0)."""
+    pool, keep = _pool(k_pool, v_pool)
+    q, _ = _data(q)
+    cu = _c(cu_q, np.int32)
+    tables, lens = _c(page_tables, np.int32), _c(seq_lens, np.int32)
+    out = np.zeros((q.shape[0], q.shape[1], pool.head_dim_v), np.float64)
+    _check(_load().orc_prefill_direct(ctypes.byref(pool), _ptr(q), _ptr(cu), _ptr(tables),
+                                      tables.shape[1], _ptr(lens), int(window), lens.shape[0],
+                                      q.shape[1], scale, _ptr(out)), "prefill_direct")
     return out
 
 

@@ -381,6 +381,36 @@ static int decode_args_ok(const orc_pool *pool, const void *q, const int32_t *pa
 /* Direct decode of T query tokens per row: token t of row b (query row
  * (b*T + t)) sits at key position len - T + t and attends the keys up to and
  * including its own position, from the window bound if any. */
+/* softmax(scale q.k_i) v_i over keys [i0, i1) of (row b, kv head g), into dst[dv].
+ * s is caller scratch of at least i1 - i0 doubles. */
+static void attend_paged(const orc_pool *pool, const double *qd, const int32_t *page_tables,
+                         int table_stride, int b, int g, int i0, int i1, double scale, double *s,
+                         double *dst) {
+  const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
+  /* s_i = scale * q . k_i over the attended keys */
+  double mx = -INFINITY;
+  for (int i = i0; i < i1; ++i) {
+    const size_t kr = paged_row(pool, dk, page_tables, table_stride, b, g, i);
+    const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
+    double acc = 0.0;
+    for (int d = 0; d < kw; ++d) acc += qd[d] * key_elem(pool, kr, vr, d);
+    s[i - i0] = scale * acc;
+    if (s[i - i0] > mx) mx = s[i - i0];
+  }
+  /* out = sum_i softmax(s)_i v_i */
+  double z = 0.0;
+  for (int i = i0; i < i1; ++i) {
+    s[i - i0] = exp(s[i - i0] - mx);
+    z += s[i - i0];
+  }
+  for (int d = 0; d < dv; ++d) dst[d] = 0.0;
+  for (int i = i0; i < i1; ++i) {
+    const double w = s[i - i0] / z;
+    const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
+    for (int d = 0; d < dv; ++d) dst[d] += w * load_elem(pool->v, pool->dtype, vr + d);
+  }
+}
+
 static int decode_direct_tokens(const orc_pool *pool, const void *q, const int32_t *page_tables,
                                 int table_stride, const int32_t *seq_lens,
                                 const int32_t *first_pos, const int32_t *window_lo, int batch,
@@ -391,7 +421,7 @@ static int decode_direct_tokens(const orc_pool *pool, const void *q, const int32
   if (num_tokens < 1) return ORC_ERR_INVALID;
   for (int b = 0; b < batch; ++b)
     if (seq_lens[b] < num_tokens) return ORC_ERR_INVALID;
-  const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
+  const int dv = pool->head_dim_v, kw = key_width(pool);
   const int G = num_q_heads / pool->num_kv_heads; /* head h reads kv head h / G */
   int rc_all = ORC_OK;
   const int T = num_tokens;
@@ -402,35 +432,54 @@ static int decode_direct_tokens(const orc_pool *pool, const void *q, const int32
     const int len = seq_lens[b] - T + t + 1; /* keys this token sees */
     const int i0 = first_key(first_pos, window_lo, b, len);
     double *qd = (double *)malloc(sizeof(double) * (size_t)kw);
-    double *s = (double *)malloc(sizeof(double) * (size_t)(len - i0));
-    double *dst = out + ((size_t)bt * num_q_heads + h) * dv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(len - i0 + 1));
     if (!qd || !s) {
 #pragma omp critical
       rc_all = ORC_ERR_INVALID;
     } else {
       for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)bt * num_q_heads + h) * kw + d);
-      /* s_i = scale * q . k_i over the attended keys */
-      double mx = -INFINITY;
-      for (int i = i0; i < len; ++i) {
-        const size_t kr = paged_row(pool, dk, page_tables, table_stride, b, g, i);
-        const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
-        double acc = 0.0;
-        for (int d = 0; d < kw; ++d) acc += qd[d] * key_elem(pool, kr, vr, d);
-        s[i - i0] = scale * acc;
-        if (s[i - i0] > mx) mx = s[i - i0];
-      }
-      /* out = sum_i softmax(s)_i v_i */
-      double z = 0.0;
-      for (int i = i0; i < len; ++i) {
-        s[i - i0] = exp(s[i - i0] - mx);
-        z += s[i - i0];
-      }
-      for (int d = 0; d < dv; ++d) dst[d] = 0.0;
-      for (int i = i0; i < len; ++i) {
-        const double w = s[i - i0] / z;
-        const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, i);
-        for (int d = 0; d < dv; ++d) dst[d] += w * load_elem(pool->v, pool->dtype, vr + d);
-      }
+      attend_paged(pool, qd, page_tables, table_stride, b, g, i0, len, scale, s,
+                   out + ((size_t)bt * num_q_heads + h) * dv);
+    }
+    free(qd);
+    free(s);
+  }
+  return rc_all;
+}
+
+int orc_prefill_direct(const orc_pool *pool, const void *q, const int32_t *cu_q,
+                       const int32_t *page_tables, int table_stride, const int32_t *seq_lens,
+                       int window, int batch, int num_q_heads, double scale, double *out) {
+  int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, NULL, NULL, batch,
+                          num_q_heads, out);
+  if (rc) return rc;
+  if (!cu_q || cu_q[0] != 0 || window < 0) return ORC_ERR_INVALID;
+  for (int b = 0; b < batch; ++b) {
+    const int T = cu_q[b + 1] - cu_q[b];
+    if (T < 0 || T > seq_lens[b]) return ORC_ERR_INVALID;
+  }
+  const int dv = pool->head_dim_v, kw = key_width(pool);
+  const int G = num_q_heads / pool->num_kv_heads;
+  const int total = cu_q[batch];
+  int rc_all = ORC_OK;
+  const int jobs = total * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int job = 0; job < jobs; ++job) {
+    const int h = job % num_q_heads, r = job / num_q_heads, g = h / G;
+    int b = 0;
+    while (cu_q[b + 1] <= r) ++b; /* the row token r belongs to */
+    const int T = cu_q[b + 1] - cu_q[b], t = r - cu_q[b];
+    const int own = seq_lens[b] - T + t; /* the token's own key index */
+    const int i0 = (window > 0 && own - window + 1 > 0) ? own - window + 1 : 0;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)kw);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(own - i0 + 2));
+    if (!qd || !s) {
+#pragma omp critical
+      rc_all = ORC_ERR_INVALID;
+    } else {
+      for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)r * num_q_heads + h) * kw + d);
+      attend_paged(pool, qd, page_tables, table_stride, b, g, i0, own + 1, scale, s,
+                   out + ((size_t)r * num_q_heads + h) * dv);
     }
     free(qd);
     free(s);

@@ -147,6 +147,19 @@ int orc_decode_multirow_direct(const orc_pool *pool, const void *q, const int32_
                                int table_stride, const int32_t *seq_lens, int batch,
                                int num_tokens, int num_q_heads, double scale, double *out);
 
+/* Direct fp64 paged prefill over variable-length chunks (pegainfer #1057,
+ * Description: prompt rows read through a windowed varlen kernel with a
+ * window lower bound; pegainfer #1055, Description: the generated prefill
+ * beside the decode).  Row b's new tokens are its last T_b = cu_q[b+1] -
+ * cu_q[b] keys (already in the pool); token t of row b sits at key index
+ * own = seq_lens[b] - T_b + t and attends keys [lo, own], lo = own - window + 1
+ * clipped at 0 when window > 0, else 0.  q is packed [cu_q[batch]][Hq][key
+ * width], out [cu_q[batch]][Hq][head_dim_v]; cu_q[0] = 0, non-decreasing.
+ * A one-token chunk is orc_decode_direct with window_lo = own - window + 1. */
+int orc_prefill_direct(const orc_pool *pool, const void *q, const int32_t *cu_q,
+                       const int32_t *page_tables, int table_stride, const int32_t *seq_lens,
+                       int window, int batch, int num_q_heads, double scale, double *out);
+
 /* Online fp64 decode: the attended keys of a row are cut into chunks of
  * chunk_tokens (aligned to key index 0), the chunks into num_splits
  * contiguous partitions of ceil(n_chunks / num_splits) chunks (trailing
