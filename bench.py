@@ -71,6 +71,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak() -> float:
+    """Dense bf16 TFLOP/s measured on this machine (burst), else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def recorded_traffic():
     """DRAM bytes per key of the partial kernel from the committed ncu summary,
     or None when the kernel source changed since the counters were taken."""
@@ -321,6 +330,60 @@ class Packed:
         self.host_out.copy_(self.dev_out, non_blocking=True)
 
 
+class PrefillCall:
+    """A paged prefill timed beside the step: each row's last `chunk` keys are
+    its new tokens (already in the pool), each attending keys up to itself
+    (within `window` keys when > 0)."""
+
+    def __init__(self, name, case, chunk, window, dev):
+        import torch
+        import paged_split_kv_attn_gb300 as pskv
+        self.name, self.case, self.chunk, self.window = name, case, chunk, window
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.k, self.v = bf(case.k_pool), bf(case.v_pool)
+        self.layout = pskv.paged_kv_layout_create(self.k, self.v, self.status)
+        b, hq, d = case.q.shape
+        counts = [min(chunk, int(n)) for n in case.seq_lens]
+        self.cu_host = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        self.cu = torch.from_numpy(self.cu_host).to(dev)
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([chunk, 11])))
+        self.q = bf(W.bf16_bits(rng.standard_normal((int(self.cu_host[-1]), hq, d),
+                                                    dtype=np.float32)))
+        self.tables = torch.from_numpy(case.page_tables).to(dev)
+        self.lens = torch.from_numpy(case.seq_lens).to(dev)
+        self.lens_host = case.seq_lens.copy()
+        self.out = torch.empty_like(self.q)
+        self.tokens = int(self.cu_host[-1])
+        # algorithmic FLOPs: 2 D (scores) + 2 D (values) per visible (token, key, q head)
+        vis = 0
+        for L, T in zip(case.seq_lens, counts):
+            own = np.arange(int(L) - T, int(L), dtype=np.int64)
+            seen = own + 1 if window == 0 else np.minimum(own + 1, window)
+            vis += int(seen.sum())
+        self.flops = 4 * hq * d * vis
+
+    def run(self, it: int, events=None):
+        import paged_split_kv_attn_gb300 as pskv
+        pskv.prefill_attn_paged(self.layout, self.q, self.cu, self.cu_host, self.tables,
+                                self.lens, self.lens_host, self.case.scale, window=self.window,
+                                out=self.out, events=events)
+
+
+def make_prefill_calls(args, dev):
+    """--prefill specs: family:context:chunk[:window]."""
+    calls = []
+    for spec in args.prefill:
+        fam, ctx, chunk, *rest = spec.split(":")
+        ctx, chunk, window = int(ctx), int(chunk), int(rest[0]) if rest else 0
+        shape = W.GLOBAL_SHAPE if fam == "global" else W.WINDOW_SHAPE
+        case = W.make_paged_case(ctx + chunk, [ctx], dtype="bf16", **shape)
+        calls.append(PrefillCall(f"prefill_{fam}_{ctx}x{chunk}" + (f"_w{window}" if window else ""),
+                                 case, chunk, window, dev))
+    return calls
+
+
 def make_extra_calls(args, dev):
     """Calls measured one at a time beside the step: the folded format and
     verify windows of the global shape (multi-row decode)."""
@@ -389,6 +452,9 @@ def parse():
                     help="verify-window lengths of the multi-row decode timed beside the step")
     ap.add_argument("--verify-context", type=int, default=40002,
                     help="context of those verify windows (global-layer shape)")
+    ap.add_argument("--prefill", nargs="*",
+                    default=["global:10602:512", "global:4096:4096", "sliding:4096:4096:1024"],
+                    help="paged prefills timed beside the step: family:context:chunk[:window]")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
@@ -652,6 +718,28 @@ def main():
         if c.status[0].item() != 0:
             raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
 
+    # paged prefills beside the step, last (tensor-core work: FLOP/s against the
+    # bf16 peak; heavy enough to move the clocks, so nothing is timed after them)
+    prefill = {}
+    for c in make_prefill_calls(args, dev):
+        cg, _ = capture([c])
+        times = []
+        for it in range(5):
+            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b.record(stream)
+            cg[it % ROTATE].replay()
+            e.record(stream)
+            torch.cuda.synchronize()
+            times.append(b.elapsed_time(e) * 1e3)
+        if c.status[0].item() != 0:
+            raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
+        us = statistics.median(times)
+        tf = c.flops / (us * 1e-6) / 1e12
+        prefill[c.name] = {"tokens": c.tokens, "us_per_call_median": us,
+                           "tokens_per_s": c.tokens / (us * 1e-6), "tflops": tf,
+                           "tflops_frac_of_bf16_peak": tf / measured_tensor_peak()}
+        del cg, c
+
     peak, peak_kind = measured_peak()
     glob = [c for c in calls if not c.windowed]
     part_bytes = sum(c.bytes for c in glob)
@@ -679,6 +767,8 @@ def main():
         line["split_sweep_us"] = sweep
     if prep_step is not None:
         line["prep_step"] = prep_step
+    if prefill:
+        line["prefill"] = prefill
     line["step_launch"] = ("CUDA graph replay (one graph per pool copy, captured once)"
                            if graphs is not None else "eager stream launches")
     line["eager"] = {"ms_per_step": eager_ms, "unit": "GB/s",

@@ -222,7 +222,9 @@ int kv_prep_append(const pskv_layout *layout, const pskv_prep_desc *prep, const 
  *                  [p*c, (p+1)*c) of its attended tiles, c = ceil(tiles / num_splits);
  *                  trailing partitions may be empty.
  *   workspace      device scratch of at least decode_attn_workspace_bytes(...)
- *                  bytes, 256-byte aligned.  On return its head holds the
+ *                  bytes, 256-byte aligned (NULL is fine with num_splits = 1 on
+ *                  a bf16 pool with 1/2/4/8 query heads per KV head: the one
+ *                  partition then writes the output itself and no merge runs).  On return its head holds the
  *                  partials: float m[batch][num_q_heads][P], then (at the next
  *                  256-byte boundary) float l[...][P], then float
  *                  o[batch][num_q_heads][P][head_dim] (m in units of the scaled
@@ -282,6 +284,35 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
                          int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Paged prefill over variable-length chunks (pegainfer #1057, Description:
+ * the sliding family's prompt rows read through a windowed varlen kernel
+ * with a window lower bound; pegainfer #1055, Description: a generated
+ * prefill beside the split-KV decode).  Row b's new tokens are its last
+ * T_b = cu_q[b+1] - cu_q[b] keys, already in the pool (kv_append_rows or
+ * kv_prep_append); token t sits at key own = seq_lens[b] - T_b + t and
+ * attends keys [lo, own], lo = max(0, own - window + 1) when window > 0, else
+ * 0.  As decode_attn_multirow, except:
+ *   q            device [cu_q[batch]][num_q_heads][head_dim_v] (packed rows)
+ *   cu_q_host    host int32[batch + 1]: 0, then non-decreasing, T_b <= seq_lens[b]
+ *   cu_q         device int32[batch + 1]: the same offsets, read by the kernels
+ *                (rows outside [0, cu_q_host[batch]] are never addressed)
+ *   window       keys a token sees, itself included; 0 = all earlier keys
+ *   out          device [cu_q[batch]][num_q_heads][head_dim_v] of out_dtype
+ *   workspace    decode_attn_workspace_bytes(cu_q[batch], num_q_heads, ...)
+ *                bytes; NULL is fine when the plan has one partition (the
+ *                automatic plan for long chunks): each CTA then writes its
+ *                normalised output directly and no merge runs
+ * A CTA serves 16 query columns (query heads of a KV head x tokens) of one
+ * row; its keys are those its tokens see.  bf16 pools with 1/2/4/8 query
+ * heads per KV head.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL,
+ * CUDA. */
+int prefill_attn_paged(const pskv_layout *layout, const void *q, const int32_t *cu_q_host,
+                       const int32_t *cu_q, const int32_t *page_tables, int32_t table_stride,
+                       const int32_t *seq_lens_host, const int32_t *seq_lens, int32_t batch,
+                       int32_t num_q_heads, int32_t window, float scale, int32_t num_splits,
+                       void *workspace, size_t workspace_bytes, void *out, int32_t out_dtype,
+                       const pskv_decode_opts *opts, pskv_stream_t stream);
 
 /* Merge P partials per row in two levels by the exact rescaling identity and
  * normalise (gem design, "Candidate ownership and storage"; pegainfer #1055,

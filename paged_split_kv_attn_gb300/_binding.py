@@ -45,7 +45,8 @@ PSKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 # Every function the header declares, in the header's order.
 EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows", "kv_prep_append",
-           "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow", "merge_partials",
+           "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow",
+           "prefill_attn_paged", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
            "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches", "pskv_version")
@@ -105,6 +106,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                          I32, P, P]
     lib.decode_attn_multirow.argtypes = [P, P, P, I32, P, P, I32, I32, I32, F, I32, P, SZ, P, I32,
                                          P, P]
+    lib.prefill_attn_paged.argtypes = [P, P, P, P, P, I32, P, P, I32, I32, I32, F, I32, P, SZ, P,
+                                       I32, P, P]
     lib.merge_partials.argtypes = [P, P, P, I32, I32, I32, P, I32, P, SZ, P, P, P]
     lib.decode_attn_workspace_bytes.argtypes = [I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.merge_partials_workspace_bytes.argtypes = [I32, I32, I32, ctypes.POINTER(SZ)]
@@ -421,6 +424,41 @@ def decode_attn_multirow(layout: Layout, q, page_tables, seq_lens, seq_lens_host
         float(scale), num_splits, _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dev(out, "out"), _dtype_code(out.dtype),
         None if opts is None else ctypes.byref(opts), _stream(stream)), "decode_attn_multirow")
+    return out
+
+
+def prefill_attn_paged(layout: Layout, q, cu_q, cu_q_host, page_tables, seq_lens, seq_lens_host,
+                       scale, window: int = 0, num_splits: int = 0, workspace=None, out=None,
+                       out_dtype=None, merge_group: int = 0, events=None,
+                       stream=None) -> torch.Tensor:
+    """Paged prefill of variable-length chunks: ``q`` [total, num_q_heads,
+    head_dim] packed by the row offsets ``cu_q`` (device) / ``cu_q_host``; row
+    b's chunk is its last cu_q[b+1]-cu_q[b] keys, each token attending keys up
+    to itself (within ``window`` keys when > 0).  Returns ``out`` [total,
+    num_q_heads, head_dim]."""
+    lib = load_library()
+    if q.dim() != 3:
+        raise ValueError("q must be [total, num_q_heads, head_dim]")
+    total, hq = q.shape[0], q.shape[1]
+    dv = layout.desc.head_dim_v
+    if out is None:
+        out = torch.empty((total, hq, dv), device=q.device, dtype=out_dtype or torch.bfloat16)
+    cu_h = _host_i32(cu_q_host, "cu_q_host")
+    lens_h = _host_i32(seq_lens_host, "seq_lens_host")
+    batch = len(lens_h)
+    if len(cu_h) != batch + 1:
+        raise ValueError("cu_q_host must have batch + 1 entries")
+    if workspace is None and num_splits != 1:
+        workspace = _alloc_workspace(total, hq, dv, num_splits, q.device)
+    opts = _opts(merge_group, events)
+    _check(lib.prefill_attn_paged(
+        layout.handle, _dev(q, "q", layout.dtype), cu_h, _dev(cu_q, "cu_q", torch.int32),
+        _dev(page_tables, "page_tables", torch.int32), page_tables.shape[1], lens_h,
+        _dev(seq_lens, "seq_lens", torch.int32), batch, hq, int(window), float(scale),
+        num_splits, None if workspace is None else _dev(workspace, "workspace"),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(out, "out"), _dtype_code(out.dtype), None if opts is None else ctypes.byref(opts),
+        _stream(stream)), "prefill_attn_paged")
     return out
 
 

@@ -125,6 +125,16 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
   return out != 0;
 }
 
+// The query tokens and keys one CTA serves: row b's tokens are query/output
+// rows r0 .. r0 + T - 1; token t sits at key len - T + t and sees keys up to
+// itself, from lo_fixed (a windowed decode's bound, else 0) or, with a
+// per-token window, from its own key - window + 1.
+struct RowPlan {
+  int b, T, r0, len;
+  int lo_fixed;
+  int window;
+};
+
 // Columns past the window's tokens x G (G < 8 query heads per KV head, or a
 // window that does not fill its last n-tile) have zero queries and are never
 // written back.
@@ -145,13 +155,16 @@ struct MmaConsumer {
   static constexpr int kCols = 8 * kNT;
   static constexpr int kQuarters = 4;              // score partials per n-tile
   static constexpr int kWarps = kQuarters * kNT;
-  static constexpr int kMinBlocks = 2;             // registers sized for two CTAs per SM
+  // registers sized for two CTAs per SM (the compiler accounts for how the
+  // warps spread over the SM's four register files: 96 per thread at 9 warps)
+  static constexpr int kMinBlocks = 2;
   static constexpr bool kCooperative = true;       // every warp takes part in every tile
   static constexpr int DQ = D / kQuarters;         // score columns per warp
   static constexpr int KSQ = DQ / 16;              // k-steps of a warp's score product
   static constexpr int DW = D / kWarps;            // output columns per warp
   static constexpr int KSP = DW / 16;              // m-tiles of a warp's PV product
-  static constexpr int CH = KSQ % 4 == 0 ? 4 : 2;  // score accumulator chains
+  // score accumulator chains (two when the second n-tile's state needs the registers)
+  static constexpr int CH = (KSQ % 4 == 0 && kNT == 1) ? 4 : 2;
   static constexpr int kExtraSmem = 2 * kQuarters * NT * 32 * 16;  // double-buffered exchange
   static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;     // bytes of one stored K row
   static constexpr int kRowBytesV = D * 2;
@@ -167,21 +180,25 @@ struct MmaConsumer {
   float m0[NT], m1[NT];    // reference max (log2 units) of columns 8nt + 2c, +1: the same in every warp
   float l0[NT], l1[NT];    // this lane's share of the sums of those columns
   int lim0[NT], lim1[NT];  // keys below lim are visible to those columns (causal in a window)
+  int lo_fixed, window;    // and keys from lo_fixed on, or from lim - window on with a window
   float scale_log2;
   float4 *xchg;            // [2][kQuarters][NT][32] partial scores
-  int r, c, warp, tokens, cbase;
+  int r, c, warp, tokens, cbase, r0;
 
   __device__ int nt_scored() const { return warp % NT; }  // the n-tile this warp scores
   __device__ int quarter() const { return warp / NT; }     // the quarter of D it scores over
 
   static __device__ void prologue(const PartialArgs &, int, int, unsigned char *) {}
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra,
-                       int len, int cb) {
+  __device__ void init(const PartialArgs &a, const RowPlan &rp, int h0, int lane,
+                       unsigned char *extra, int cb) {
     r = lane >> 2;
     c = lane & 3;
     warp = threadIdx.x >> 5;
-    tokens = a.num_tokens;
+    tokens = rp.T;
+    r0 = rp.r0;
+    lo_fixed = rp.lo_fixed;
+    window = rp.window;
     cbase = cb * kCols;
     scale_log2 = a.scale_log2;
     xchg = reinterpret_cast<float4 *>(extra);
@@ -190,8 +207,7 @@ struct MmaConsumer {
       const bool real = tq < tokens;
       const uint16_t *q =
           static_cast<const uint16_t *>(a.q) +
-          (((size_t)b * tokens + (real ? tq : 0)) * a.num_q_heads + h0 + jq % G) * D +
-          quarter() * DQ;
+          (((size_t)r0 + (real ? tq : 0)) * a.num_q_heads + h0 + jq % G) * D + quarter() * DQ;
 #pragma unroll
       for (int k = 0; k < KSQ; ++k) {
         qf[k][0] = real ? *reinterpret_cast<const uint32_t *>(q + 16 * k + 2 * c) : 0u;
@@ -202,8 +218,10 @@ struct MmaConsumer {
     for (int nt = 0; nt < NT; ++nt) {
       // token t of the row sits at key len - tokens + t and sees keys up to itself
       const int j0 = cbase + 8 * nt + 2 * c, t0 = j0 / G, t1 = (j0 + 1) / G;
-      lim0[nt] = t0 < tokens ? len - tokens + t0 + 1 : 0;
-      lim1[nt] = t1 < tokens ? len - tokens + t1 + 1 : 0;
+      const int own0 = rp.len - tokens + t0, own1 = rp.len - tokens + t1;
+      lim0[nt] = t0 < tokens ? own0 + 1 : 0;
+      lim1[nt] = t1 < tokens ? own1 + 1 : 0;
+
 #pragma unroll
       for (int j = 0; j < KSP; ++j) o[nt][j][0] = o[nt][j][1] = o[nt][j][2] = o[nt][j][3] = 0.f;
       m0[nt] = m1[nt] = -CUDART_INF_F;
@@ -266,11 +284,14 @@ struct MmaConsumer {
         st.z += x.z;
         st.w += x.w;
       }
-      auto vis = [&](int t, int lim) { return !skip && t >= i0 && t < lim; };
-      s00[nt] = vis(tA, lim0[nt]) ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, column 8nt+2c
-      s01[nt] = vis(tA, lim1[nt]) ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, column 8nt+2c+1
-      s10[nt] = vis(tB, lim0[nt]) ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, column 8nt+2c
-      s11[nt] = vis(tB, lim1[nt]) ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, column 8nt+2c+1
+      // a token's first visible key: lo_fixed, or (own + 1) - window with a window
+      const int lo0 = window > 0 ? max(0, lim0[nt] - window) : lo_fixed;
+      const int lo1 = window > 0 ? max(0, lim1[nt] - window) : lo_fixed;
+      auto vis = [&](int t, int lo, int lim) { return !skip && t >= lo && t < lim; };
+      s00[nt] = vis(tA, lo0, lim0[nt]) ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, col 8nt+2c
+      s01[nt] = vis(tA, lo1, lim1[nt]) ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, col 8nt+2c+1
+      s10[nt] = vis(tB, lo0, lim0[nt]) ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, col 8nt+2c
+      s11[nt] = vis(tB, lo1, lim1[nt]) ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, col 8nt+2c+1
       x0[nt] = fmaxf(s00[nt], s10[nt]);
       x1[nt] = fmaxf(s01[nt], s11[nt]);
       need |= x0[nt] > m0[nt] + kSlack || x1[nt] > m1[nt] + kSlack;
@@ -361,8 +382,10 @@ struct MmaConsumer {
   }
 
   // Write this partition's (m, l, o) of every real column: every warp writes
-  // its d slice; warp 0 the scalars.  Column j -> workspace row (b, j / G, h0 + j % G).
-  __device__ void write_partial(const PartialArgs &a, int b, int h0, int p) const {
+  // its d slice; warp 0 the scalars.  Column j -> query row r0 + j / G, head
+  // h0 + j % G.  With one partition (`direct`) the normalised output o / l goes
+  // straight to `out` (zeros and PSKV_FAULT_EMPTY_ROW where no key was seen).
+  __device__ void write_partial(const PartialArgs &a, const RowPlan &, int h0, int p) const {
     const int P = a.num_splits, d0 = warp * DW;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -370,8 +393,29 @@ struct MmaConsumer {
       for (int e = 0; e < 2; ++e) {
         const int jc = cbase + 8 * nt + 2 * c + e, t = jc / G;
         if (t >= tokens) continue;
-        const size_t row =
-            (((size_t)b * tokens + t) * a.num_q_heads + h0 + jc % G) * P + p;
+        const size_t qrow = ((size_t)r0 + t) * a.num_q_heads + h0 + jc % G;
+        if (a.direct) {
+          const float mm = e ? m1[nt] : m0[nt];
+          const float inv = mm == -CUDART_INF_F ? 0.f : 1.f / (e ? l1[nt] : l0[nt]);
+          if (a.out_dtype == PSKV_DTYPE_BF16) {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + qrow * D + d0 + r;
+#pragma unroll
+            for (int j = 0; j < KSP; ++j) {
+              dst[16 * j] = __float2bfloat16_rn(o[nt][j][e] * inv);
+              dst[16 * j + 8] = __float2bfloat16_rn(o[nt][j][2 + e] * inv);
+            }
+          } else {
+            float *dst = static_cast<float *>(a.out) + qrow * D + d0 + r;
+#pragma unroll
+            for (int j = 0; j < KSP; ++j) {
+              dst[16 * j] = o[nt][j][e] * inv;
+              dst[16 * j + 8] = o[nt][j][2 + e] * inv;
+            }
+          }
+          if (mm == -CUDART_INF_F && warp == 0 && r == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
+          continue;
+        }
+        const size_t row = qrow * P + p;
         float *dst = a.ws_o + row * D + d0 + r;
 #pragma unroll
         for (int j = 0; j < KSP; ++j) {
@@ -454,8 +498,9 @@ struct SimtConsumer {
     }
   }
 
-  __device__ void init(const PartialArgs &a, int b, int h0, int lane, unsigned char *extra,
-                       int, int) {
+  __device__ void init(const PartialArgs &a, const RowPlan &rp, int h0, int lane,
+                       unsigned char *extra, int) {
+    const int b = rp.b;
     lane_ = lane;
     scale_log2 = a.scale_log2;
     q_s = reinterpret_cast<const float *>(extra);
@@ -630,7 +675,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   extern __shared__ __align__(128) unsigned char smem[];
   using Geom = typename C::Geom;
   using S = PartialSmem<C>;
-  constexpr int G = C::G, NS = Geom::kStages;
+  constexpr int D = C::D, G = C::G, NS = Geom::kStages;
   constexpr int RBK = C::kRowBytesK, RBV = C::kRowBytesV;  // bytes of a K row, a V row
   constexpr int TBK = Geom::kTileBytesK;
   constexpr int R = Geom::kRowsPerCopy;
@@ -668,21 +713,45 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   pdl_wait();
   pdl_launch_dependents();
 
-  // ---- this partition's tiles
+  // ---- this CTA's query tokens (row b's are query rows r0 .. r0 + T - 1)
+  RowPlan rp;
+  rp.b = b;
+  rp.T = a.num_tokens;
+  rp.r0 = b * a.num_tokens;
+  rp.window = a.window;
+  if (a.cu_q != nullptr) {
+    const int c0 = a.cu_q[b], c1 = a.cu_q[b + 1];
+    if (c0 < 0 || c1 < c0 || c1 > a.total_rows) {  // never address rows outside the arrays
+      if (threadIdx.x == 0 && p == 0 && g == 0 && cb == 0) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
+      rp.T = 0;
+      rp.r0 = 0;
+    } else {
+      rp.T = c1 - c0;
+      rp.r0 = c0;
+    }
+  }
+  const int T = rp.T;
+  if (cb * C::kCols >= T * G) return;  // no real column in this block
+  // ---- and its keys: a token at key len - T + t sees keys up to itself
   const long long cap = (long long)a.table_stride * a.page_size;
   long long len_ll = a.seq_lens[b];
-  if (len_ll < a.num_tokens || len_ll > cap) {  // a row holds at least its query tokens
-    if (threadIdx.x == 0 && p == 0 && g == 0) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
+  if (len_ll < T || len_ll < 1 || len_ll > cap) {  // a row holds at least its query tokens
+    if (threadIdx.x == 0 && p == 0 && g == 0 && cb == 0) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
     len_ll = len_ll < 0 ? 0 : (len_ll > cap ? cap : len_ll);
   }
   const int len = (int)len_ll;
-  int i0 = 0;
+  rp.len = len;
+  rp.lo_fixed = 0;
   if (a.window_lo != nullptr) {
     long long d = (long long)a.window_lo[b] - (long long)a.first_pos[b];
-    i0 = (int)(d < 0 ? 0 : (d > len ? len : d));
+    rp.lo_fixed = (int)(d < 0 ? 0 : (d > len ? len : d));
   }
-  const int n_tiles = (len + kKeyTile - 1) / kKeyTile;
-  const int t_lo = i0 < len ? i0 / kKeyTile : n_tiles;
+  const int t_first = cb * C::kCols / G, t_last = min(T - 1, ((cb + 1) * C::kCols - 1) / G);
+  const int k_hi = max(0, min(len, len - T + t_last + 1));  // keys [k_lo, k_hi) serve this block
+  const int k_lo = min(k_hi, a.window > 0 ? max(0, len - T + t_first - a.window + 1) : rp.lo_fixed);
+  const int i0 = k_lo;
+  const int n_tiles = (k_hi + kKeyTile - 1) / kKeyTile;
+  const int t_lo = k_lo < k_hi ? k_lo / kKeyTile : n_tiles;
   const long long total = n_tiles - t_lo;
   const long long per = (total + P - 1) / P;
   const long long lo_ll = (long long)p * per < total ? (long long)p * per : total;
@@ -690,12 +759,22 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   const int t_begin = t_lo + (int)lo_ll;
   const int n_my = (int)(hi_ll - lo_ll);
 
-  const int T = a.num_tokens;
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0 (T = 1)
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
     const int c0 = cb * C::kCols, c1 = min(c0 + C::kCols, T * G);  // this block's columns
+    if (a.direct) {  // one partition and no key: zeros, flagged
+      for (int i = c0 * D + threadIdx.x; i < c1 * D; i += blockDim.x) {
+        const size_t qrow = ((size_t)rp.r0 + i / D / G) * a.num_q_heads + h0 + (i / D) % G;
+        if (a.out_dtype == PSKV_DTYPE_BF16)
+          static_cast<__nv_bfloat16 *>(a.out)[qrow * D + i % D] = __float2bfloat16_rn(0.f);
+        else
+          static_cast<float *>(a.out)[qrow * D + i % D] = 0.f;
+      }
+      if (threadIdx.x == 0 && c0 < c1) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
+      return;
+    }
     for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
-      const size_t row = (((size_t)b * T + i / G) * a.num_q_heads + h0 + i % G) * P + p;
+      const size_t row = (((size_t)rp.r0 + i / G) * a.num_q_heads + h0 + i % G) * P + p;
       a.ws_m[row] = -CUDART_INF_F;
       a.ws_l[row] = 0.f;
     }
@@ -708,7 +787,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   if (warp == CW) {
     // ---------------- producer warp
     const int32_t *tbl = a.page_tables + (size_t)b * a.table_stride;
-    const int n_slots = (len + a.page_size - 1) / a.page_size;  // table entries in use
+    const int n_slots = (k_hi + a.page_size - 1) / a.page_size;  // table entries in use
     int cache_base = -1, cached = -1;
     int issued = 0;
     for (int j = 0; j < n_my; ++j) {
@@ -734,7 +813,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
       const int page = __shfl_sync(0xffffffffu, cached, slot - cache_base);
       const bool ok = page >= 0 && (long long)page < a.num_pages;
       const int r_lo = i0 > key0 ? i0 - key0 : 0;
-      const int r_hi = len - key0 < kKeyTile ? len - key0 : kKeyTile;
+      const int r_hi = k_hi - key0 < kKeyTile ? k_hi - key0 : kKeyTile;
       unsigned char *kdst = ring + s * Geom::kStageBytes;
       unsigned char *vdst = kdst + TBK;
       if (lane == 0) {
@@ -767,7 +846,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   } else {
     // ---------------- consumer warps
     // cooperative consumers all take every tile; the others take every CW-th
-    cons.init(a, b, h0, lane, extra, len, cb);
+    cons.init(a, rp, h0, lane, extra, cb);
     const int j0 = C::kCooperative ? 0 : warp, dj = C::kCooperative ? 1 : CW;
     for (int j = j0; j < n_my; j += dj) {
       const int s = j % NS;
@@ -786,7 +865,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
         break;
       }
       const unsigned char *kst = ring + s * Geom::kStageBytes;
-      cons.tile(kst, kst + TBK, (t_begin + j) * kKeyTile, i0, len, stage_skip[s] != 0, lane, j);
+      cons.tile(kst, kst + TBK, (t_begin + j) * kKeyTile, i0, k_hi, stage_skip[s] != 0, lane, j);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -796,7 +875,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   if (*abort_flag) return;
 
   if constexpr (C::kCooperative) {
-    if (warp < CW) cons.write_partial(a, b, h0, p);
+    if (warp < CW) cons.write_partial(a, rp, h0, p);
     return;
   } else {
     merge_warp_states<C>(cons, a, ring, red_m, red_l, weight, row0, P, warp);

@@ -77,14 +77,23 @@ int merge_group_of(const pskv_decode_opts *opts, int *group) {
 // Level 2 folds at most this many group results per row.
 constexpr int kMaxGroups = 64;
 
+// The query side of a call: a uniform number of tokens per row (single-token
+// decode, verify windows), or variable-length chunks given by row offsets
+// (prefill), optionally with a per-token window.
+struct QuerySpec {
+  int tokens = 1;
+  const int32_t *cu_q_host = nullptr;  // [B + 1] host copy of the offsets, or null
+  const int32_t *cu_q = nullptr;       // [B + 1] device offsets
+  int window = 0;
+};
+
 int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_tables,
                   int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
                   const int32_t *first_pos, const int32_t *window_lo, bool windowed,
-                  int32_t batch, int32_t num_tokens, int32_t num_q_heads, float scale,
-                  int32_t num_splits,
-                  void *workspace, size_t workspace_bytes, void *out, int32_t out_dtype,
-                  const pskv_decode_opts *opts, pskv_stream_t stream) {
-  if (!layout || !q || !page_tables || !seq_lens_host || !seq_lens || !workspace || !out)
+                  int32_t batch, const QuerySpec &qs, int32_t num_q_heads, float scale,
+                  int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
+                  int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream) {
+  if (!layout || !q || !page_tables || !seq_lens_host || !seq_lens || !out)
     return PSKV_ERR_INVALID_ARG;
   if (windowed && (!first_pos || !window_lo)) return PSKV_ERR_INVALID_ARG;
   if (batch < 1 || batch > 65535 || num_q_heads < 1 || table_stride < 1) return PSKV_ERR_INVALID_ARG;
@@ -99,17 +108,36 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
   if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
   const bool folded = d.format == PSKV_FORMAT_FOLDED;
+  const bool varlen = qs.cu_q_host != nullptr;
+  if (varlen && !qs.cu_q) return PSKV_ERR_INVALID_ARG;
+  if (qs.window < 0) return PSKV_ERR_INVALID_ARG;
+  int rc = check_lengths(layout, batch, table_stride, seq_lens_host, varlen ? 1 : qs.tokens);
+  if (rc) return rc;
+  // query rows and the longest chunk
+  int64_t rows = 0, max_t = 0;
+  if (varlen) {
+    if (qs.cu_q_host[0] != 0) return PSKV_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+      const int64_t t = (int64_t)qs.cu_q_host[b + 1] - qs.cu_q_host[b];
+      if (t < 0 || t > seq_lens_host[b]) return PSKV_ERR_INVALID_ARG;
+      max_t = t > max_t ? t : max_t;
+    }
+    rows = qs.cu_q_host[batch];
+    if (rows < 1) return PSKV_ERR_INVALID_ARG;
+  } else {
+    if (qs.tokens < 1 || qs.tokens > PSKV_MAX_WINDOW_TOKENS) return PSKV_ERR_INVALID_ARG;
+    max_t = qs.tokens;
+    rows = (int64_t)batch * qs.tokens;
+  }
   // Query columns per KV head (heads x tokens): one n-tile of 8 when they fit,
   // else blocks of two n-tiles, one CTA per block (several tokens only on the
   // tensor-core family).
-  if (num_tokens < 1 || num_tokens > PSKV_MAX_WINDOW_TOKENS) return PSKV_ERR_INVALID_ARG;
-  if (num_tokens > 1 && (kernel != kKernelMma || windowed)) return PSKV_ERR_UNSUPPORTED;
-  const int columns = group * num_tokens;
+  if ((max_t > 1 || varlen) && (kernel != kKernelMma || windowed)) return PSKV_ERR_UNSUPPORTED;
+  const int64_t columns = group * max_t;
   const int nt = columns > 8 ? 2 : 1;
-  const int col_blocks = (columns + 8 * nt - 1) / (8 * nt);
-  if ((int64_t)batch * num_tokens * num_q_heads > INT32_MAX) return PSKV_ERR_INVALID_ARG;
-  int rc = check_lengths(layout, batch, table_stride, seq_lens_host, num_tokens);
-  if (rc) return rc;
+  const int64_t col_blocks = (columns + 8 * nt - 1) / (8 * nt);
+  if (rows * num_q_heads > INT32_MAX || col_blocks * PSKV_MAX_SPLITS > INT32_MAX)
+    return PSKV_ERR_INVALID_ARG;
   int mgroup = 0;
   if ((rc = merge_group_of(opts, &mgroup))) return rc;
 
@@ -118,13 +146,15 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     int slots = 0;
     if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
     // every partition launches col_blocks CTAs
-    P = plan_splits(slots / col_blocks, batch, d.num_kv_heads, seq_lens_host);
+    const int64_t per = slots / col_blocks;
+    P = plan_splits(per > 0 ? (int)per : 1, batch, d.num_kv_heads, seq_lens_host);
   }
+  // one partition on the tensor-core kernels: the partial is the output
+  const bool direct = P == 1 && kernel == kKernelMma;
   WorkspacePlan w;
-  const int64_t rows = (int64_t)batch * num_tokens;  // workspace and output rows: (row, token)
   if ((rc = plan_workspace(rows, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
-  if (workspace_bytes < w.total) return PSKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!direct && (!workspace || workspace_bytes < w.total)) return PSKV_ERR_WORKSPACE_TOO_SMALL;
 
   char *ws = static_cast<char *>(workspace);
   PartialArgs a;
@@ -136,21 +166,27 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.first_pos = windowed ? first_pos : nullptr;
   a.window_lo = windowed ? window_lo : nullptr;
   a.status = d.status;
-  a.ws_m = reinterpret_cast<float *>(ws + w.m_off);
-  a.ws_l = reinterpret_cast<float *>(ws + w.l_off);
-  a.ws_o = reinterpret_cast<float *>(ws + w.o_off);
+  a.ws_m = direct ? nullptr : reinterpret_cast<float *>(ws + w.m_off);
+  a.ws_l = direct ? nullptr : reinterpret_cast<float *>(ws + w.l_off);
+  a.ws_o = direct ? nullptr : reinterpret_cast<float *>(ws + w.o_off);
   a.num_pages = d.num_pages;
   a.table_stride = table_stride;
   a.page_size = d.page_size;
   a.num_kv_heads = d.num_kv_heads;
   a.num_q_heads = num_q_heads;
   a.num_splits = P;
-  a.num_tokens = num_tokens;
-  a.col_blocks = col_blocks;
+  a.num_tokens = varlen ? 0 : qs.tokens;
+  a.col_blocks = (int)col_blocks;
   a.scale_log2 = scale * kLog2e;
+  a.cu_q = varlen ? qs.cu_q : nullptr;
+  a.total_rows = (int)rows;
+  a.window = qs.window;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.direct = direct ? 1 : 0;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(P * col_blocks, d.num_kv_heads, batch);
+  const dim3 grid((unsigned)(P * col_blocks), d.num_kv_heads, batch);
   cudaError_t e;
   if (opts && opts->partial_begin) {
     e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
@@ -168,6 +204,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_end), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  if (direct) return PSKV_OK;
 
   MergeArgs m;
   m.m = a.ws_m;
@@ -333,8 +370,8 @@ int decode_attn_splitkv(const pskv_layout *layout, const void *q, const int32_t 
                         int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
                         int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream) {
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
-                       nullptr, false, batch, 1, num_q_heads, scale, num_splits, workspace,
-                       workspace_bytes, out, out_dtype, opts, stream);
+                       nullptr, false, batch, QuerySpec{}, num_q_heads, scale, num_splits,
+                       workspace, workspace_bytes, out, out_dtype, opts, stream);
 }
 
 int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t *page_tables,
@@ -345,8 +382,8 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream) {
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, first_pos,
-                       window_lo, true, batch, 1, num_q_heads, scale, num_splits, workspace,
-                       workspace_bytes, out, out_dtype, opts, stream);
+                       window_lo, true, batch, QuerySpec{}, num_q_heads, scale, num_splits,
+                       workspace, workspace_bytes, out, out_dtype, opts, stream);
 }
 
 int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t *page_tables,
@@ -355,9 +392,27 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
                          int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream) {
+  QuerySpec qs;
+  qs.tokens = num_tokens;
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
-                       nullptr, false, batch, num_tokens, num_q_heads, scale, num_splits,
-                       workspace, workspace_bytes, out, out_dtype, opts, stream);
+                       nullptr, false, batch, qs, num_q_heads, scale, num_splits, workspace,
+                       workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int prefill_attn_paged(const pskv_layout *layout, const void *q, const int32_t *cu_q_host,
+                       const int32_t *cu_q, const int32_t *page_tables, int32_t table_stride,
+                       const int32_t *seq_lens_host, const int32_t *seq_lens, int32_t batch,
+                       int32_t num_q_heads, int32_t window, float scale, int32_t num_splits,
+                       void *workspace, size_t workspace_bytes, void *out, int32_t out_dtype,
+                       const pskv_decode_opts *opts, pskv_stream_t stream) {
+  if (!cu_q_host || !cu_q) return PSKV_ERR_INVALID_ARG;
+  QuerySpec qs;
+  qs.cu_q_host = cu_q_host;
+  qs.cu_q = cu_q;
+  qs.window = window;
+  return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
+                       nullptr, false, batch, qs, num_q_heads, scale, num_splits, workspace,
+                       workspace_bytes, out, out_dtype, opts, stream);
 }
 
 int merge_partials(const float *m, const float *l, const float *o, int32_t rows,

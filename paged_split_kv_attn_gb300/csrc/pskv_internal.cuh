@@ -40,9 +40,15 @@ struct PartialArgs {
   int num_kv_heads;
   int num_q_heads;
   int num_splits;
-  int num_tokens;    // query tokens per row: 1, or a verify window's length
+  int num_tokens;    // query tokens per row (1, or a verify window's length) when cu_q is null
   int col_blocks;    // CTAs per (row, KV head, partition): query columns in blocks
   float scale_log2;  // scale * log2(e)
+  const int32_t *cu_q;  // [B + 1] first query row of each table row (varlen prefill), or null
+  int total_rows;       // query rows in all (checks cu_q)
+  int window;           // per-token window in keys (prefill), 0 = none
+  void *out;            // [rows][Hq][D] of out_dtype: written directly when `direct`
+  int out_dtype;
+  int direct;           // one partition: write o / l to `out`, no partials, no merge
 };
 
 // Arguments of the merge kernels.  Level 1 folds groups of `group` partials

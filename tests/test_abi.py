@@ -220,6 +220,32 @@ def test_prep_refusals_happen_before_any_launch(lib):
             lib.paged_kv_layout_destroy(x)
 
 
+def _prefill_rc(lib, layout, lens, cu, window=0, splits=1, ws_bytes=0, hq=32):
+    lh = (ctypes.c_int32 * len(lens))(*lens)
+    ch = (ctypes.c_int32 * len(cu))(*cu)
+    return lib.prefill_attn_paged(layout, 0x30000, ch, 0x38000, 0x40000, 4, lh, 0x50000,
+                                  len(lens), hq, window, 0.04, splits,
+                                  0x60000 if ws_bytes else None, ws_bytes, 0x70000,
+                                  B.PSKV_DTYPE_BF16, None, None)
+
+
+def test_prefill_refusals_happen_before_any_launch(lib):
+    h = _layout(lib)
+    f32 = _layout(lib, kv_dtype=B.PSKV_DTYPE_F32)
+    try:
+        assert _prefill_rc(lib, h, [100, 50], [1, 5, 9]) == B.PSKV_ERR_INVALID_ARG  # not from 0
+        assert _prefill_rc(lib, h, [100, 50], [0, 5, 2]) == B.PSKV_ERR_INVALID_ARG  # decreasing
+        assert _prefill_rc(lib, h, [100, 50], [0, 5, 56]) == B.PSKV_ERR_INVALID_ARG  # 51 > 50 keys
+        assert _prefill_rc(lib, h, [100, 50], [0, 0, 0]) == B.PSKV_ERR_INVALID_ARG  # no token
+        assert _prefill_rc(lib, h, [100], [0, 5], window=-1) == B.PSKV_ERR_INVALID_ARG
+        assert _prefill_rc(lib, f32, [100], [0, 5]) == B.PSKV_ERR_UNSUPPORTED  # tensor-core only
+        # several partitions need the partial buffer
+        assert _prefill_rc(lib, h, [100], [0, 5], splits=2) == B.PSKV_ERR_WORKSPACE_TOO_SMALL
+    finally:
+        lib.paged_kv_layout_destroy(h)
+        lib.paged_kv_layout_destroy(f32)
+
+
 def test_append_past_pages_refused_on_host(lib):
     h = _layout(lib)
     try:
