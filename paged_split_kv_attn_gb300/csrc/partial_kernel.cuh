@@ -790,6 +790,7 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
     const int n_slots = (k_hi + a.page_size - 1) / a.page_size;  // table entries in use
     int cache_base = -1, cached = -1;
     int issued = 0;
+    const uint64_t stream_policy = make_evict_first_policy();
     for (int j = 0; j < n_my; ++j) {
       const int s = j % NS;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;  // one decision for the whole warp
@@ -833,8 +834,8 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
         const int rb = is_k ? RBK : RBV;
         const unsigned char *src =
             static_cast<const unsigned char *>(is_k ? a.k_pool : a.v_pool) + grow * rb;
-        bulk_g2s(is_k ? kdst + Geom::row_off_k(g_lo) : vdst + Geom::row_off_v(g_lo), src,
-                 (uint32_t)((g_hi - g_lo) * rb), &full_bar[s]);
+        bulk_g2s_hint(is_k ? kdst + Geom::row_off_k(g_lo) : vdst + Geom::row_off_v(g_lo), src,
+                      (uint32_t)((g_hi - g_lo) * rb), &full_bar[s], stream_policy);
       }
       issued = j + 1;
     }
