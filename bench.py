@@ -203,13 +203,15 @@ class Call:
     the prepared queries into ``q`` (one launch); without it the K/V rows are
     copied into the pages as they are (kv_append_rows) and ``q`` is given."""
 
-    def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1, prep=False):
+    def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1, prep=False,
+                 fused=False):
         import torch
         import paged_split_kv_attn_gb300 as pskv
         self.name, self.case, self.windowed = name, case, windowed
         self.tokens = tokens  # query tokens per row: > 1 is a verify window (multi-row decode)
         self.splits = splits
         self.prep = prep
+        self.fused = fused and tokens == 1 and not prep  # the append inside the decode
         bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
             torch.bfloat16).to(dev)
         f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
@@ -273,9 +275,10 @@ class Call:
                                 w_q=self.w_q, w_k=self.w_k, rope_cos=self.rope_cos,
                                 rope_sin=self.rope_sin, first_pos=self.first_pos,
                                 q_out=self.q.view(n, hq, d))
-        else:
+        elif not self.fused:
             pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of,
                                 self.tables, self.pages_of_row)
+        app = (self.k_new, self.v_new, self.pages_of_row) if self.fused else None
         if self.tokens > 1:
             pskv.decode_attn_multirow(layout, self.q, self.tables, self.lens, self.lens_host,
                                       self.case.scale, num_splits=self.splits, workspace=self.ws,
@@ -284,11 +287,11 @@ class Call:
             pskv.decode_attn_windowed(layout, self.q, self.tables, self.lens, self.lens_host,
                                       self.first_pos, self.window_lo, self.case.scale,
                                       num_splits=self.splits, workspace=self.ws, out=self.out,
-                                      events=events)
+                                      events=events, append=app)
         else:
             pskv.decode_attn_splitkv(layout, self.q, self.tables, self.lens, self.lens_host,
                                      self.case.scale, num_splits=self.splits, workspace=self.ws,
-                                     out=self.out, events=events)
+                                     out=self.out, events=events, append=app)
 
 
 
@@ -387,9 +390,9 @@ def make_prefill_calls(args, dev):
 def make_extra_calls(args, dev):
     """Calls measured one at a time beside the step: the folded format and
     verify windows of the global shape (multi-row decode)."""
-    prep = args.append == "prep"
+    prep, fused = args.append == "prep", args.append == "fused"
     calls = [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev,
-                  ROTATE, prep=prep) for ctx in args.folded_contexts]
+                  ROTATE, prep=prep, fused=fused) for ctx in args.folded_contexts]
     for t in args.verify_tokens:
         ctx = args.verify_context
         calls.append(Call(f"verify_{ctx}x{t}", W.global_case(ctx, seed=ctx + 2), False,
@@ -398,13 +401,13 @@ def make_extra_calls(args, dev):
 
 
 def make_calls(args, dev):
-    calls, prep = [], args.append == "prep"
+    calls, prep, fused = [], args.append == "prep", args.append == "fused"
     for ctx in args.contexts:
         calls.append(Call(f"global_{ctx}", W.global_case(ctx, seed=ctx), False, args.splits, dev,
-                          ROTATE, prep=prep))
+                          ROTATE, prep=prep, fused=fused))
     if not args.no_window:
         calls.append(Call(f"window_{WINDOW_RESIDENCY}", W.window_case(WINDOW_RESIDENCY, seed=7),
-                          True, args.window_splits, dev, ROTATE, prep=prep))
+                          True, args.window_splits, dev, ROTATE, prep=prep, fused=fused))
     return calls
 
 
@@ -441,9 +444,10 @@ def parse():
     ap.add_argument("--splits", type=int, default=0, help="global-layer split count (0 = auto)")
     ap.add_argument("--window-splits", type=int, default=0)
     ap.add_argument("--no-window", action="store_true")
-    ap.add_argument("--append", choices=["prep", "copy"], default="copy",
-                    help="new tokens of the step: K/V rows copied into the pages, or projection "
-                         "rows through the fused K/V prep")
+    ap.add_argument("--append", choices=["fused", "copy", "prep"], default="fused",
+                    help="new tokens of the step: K/V rows written by the decode itself, "
+                         "copied into the pages by a separate launch, or projection rows "
+                         "through the fused K/V prep")
     ap.add_argument("--no-prep-step", action="store_true",
                     help="skip timing the step with the fused K/V prep beside the headline step")
     ap.add_argument("--folded-contexts", type=int, nargs="*", default=[40002],
@@ -509,9 +513,11 @@ def config_dict(args):
             {"batch": 1, "num_q_heads": 32, "num_kv_heads": 16, "head_dim": 256,
              "page_size": 64, "window": W.WINDOW, "residency": WINDOW_RESIDENCY,
              "splits": args.window_splits or "auto"},
-            "new_tokens": ("projection rows through the fused K/V prep (RMS norm, rotation, "
-                           "page write, prepared query) in one launch" if args.append == "prep"
-                           else "K/V rows copied into the pages (kv_append_rows)"),
+            "new_tokens": {"prep": "projection rows through the fused K/V prep (RMS norm, "
+                                   "rotation, page write, prepared query) in one launch",
+                           "copy": "K/V rows copied into the pages (kv_append_rows)",
+                           "fused": "K/V rows written into the pages by the decode's own "
+                                    "partial kernel (two launches per call)"}[args.append],
             "kv_dtype": "bf16", "accumulate": "f32", "out_dtype": "bf16",
             "l2": f"inputs larger than L2: {ROTATE} rotating pool copies, >400 MB of K/V per step",
             "parallelism": "replicas"}
@@ -689,7 +695,7 @@ def main():
     # the same step with the fused K/V prep in place of the row copy (projection
     # rows in, normalised and rotated K/V written into the pages, queries out)
     prep_step = None
-    if args.append == "copy" and not args.no_prep_step and graphs is not None:
+    if args.append != "prep" and not args.no_prep_step and graphs is not None:
         pargs = argparse.Namespace(**{**vars(args), "append": "prep"})
         pcalls = make_calls(pargs, dev)
         for it in range(args.warmup):

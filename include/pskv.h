@@ -120,11 +120,27 @@ typedef struct pskv_layout_desc {
 /* Opaque handle: holds a copy of the description (host memory only). */
 typedef struct pskv_layout pskv_layout;
 
-/* Optional per-call settings; pass NULL for the defaults. */
+/* Optional per-call settings; pass NULL (or zeroed fields) for the defaults.
+ *
+ * append_k / append_v / append_pages (single-token decode_attn_splitkv and
+ * decode_attn_windowed only): the step's new K/V row of each table row, its
+ * key seq_lens[b] - 1, is written into its page by the decode itself, as
+ * kv_append_rows would write it (same bits, same checks and fault bits:
+ * PSKV_FAULT_PAST_PAGES, PSKV_FAULT_BAD_PAGE) -- TensorFold #1619, "Writes"
+ * and "Leasing"; pegainfer #1055, Description (the row written where it is
+ * produced).  The CTA whose partition holds that key copies the row before it
+ * loads the tile, so the call takes two launches (partial kernel, merge)
+ * instead of an append launch plus those two.
+ *   append_k      device [batch][num_kv_heads][head_dim_k] of the pool's dtype, 16-byte aligned
+ *   append_v      device [batch][num_kv_heads][head_dim_v], 16-byte aligned
+ *   append_pages  device int32[batch]: pages leased to each row */
 typedef struct pskv_decode_opts {
   int32_t merge_group;        /* partials per level-1 merge group, 1..PSKV_MERGE_GROUP; 0 = PSKV_MERGE_GROUP */
   pskv_event_t partial_begin; /* if not NULL, recorded on the stream just before the partial kernel */
   pskv_event_t partial_end;   /* if not NULL, recorded on the stream just after the partial kernel */
+  const void *append_k;       /* the step's new K rows, or NULL (no append) */
+  const void *append_v;       /* the step's new V rows */
+  const int32_t *append_pages; /* pages leased per row */
 } pskv_decode_opts;
 
 /* Validate `desc` and make a layout handle.  Touches no device.

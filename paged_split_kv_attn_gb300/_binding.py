@@ -78,7 +78,8 @@ class PrepDesc(ctypes.Structure):
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("merge_group", ctypes.c_int32), ("partial_begin", ctypes.c_void_p),
-                ("partial_end", ctypes.c_void_p)]
+                ("partial_end", ctypes.c_void_p), ("append_k", ctypes.c_void_p),
+                ("append_v", ctypes.c_void_p), ("append_pages", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -179,11 +180,18 @@ def _event(ev):
     return int(ev)
 
 
-def _opts(merge_group: int = 0, events=None):
-    if not merge_group and events is None:
+def _opts(merge_group: int = 0, events=None, append=None, dtype=None):
+    """Per-call options; ``append`` = (k_new, v_new, pages_of_row) writes each
+    row's new K/V row (key seq_lens - 1) from inside the decode."""
+    if not merge_group and events is None and append is None:
         return None
     begin, end = (None, None) if events is None else events
-    return DecodeOpts(merge_group, _event(begin), _event(end))
+    ak = av = ap = None
+    if append is not None:
+        k_new, v_new, pages = append
+        ak, av = _dev(k_new, "k_new", dtype), _dev(v_new, "v_new", dtype)
+        ap = _dev(pages, "pages_of_row", torch.int32)
+    return DecodeOpts(merge_group, _event(begin), _event(end), ak, av, ap)
 
 
 # ---- layout ------------------------------------------------------------------
@@ -352,7 +360,7 @@ _alloc_workspace = workspace
 
 def _decode(windowed: bool, layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,
             num_splits, workspace_t, out, out_dtype, merge_group, events, stream,
-            first_pos=None, window_lo=None):
+            first_pos=None, window_lo=None, append=None):
     lib = load_library()
     if q.dim() != 3:
         raise ValueError("q must be [batch, num_q_heads, head_dim]")
@@ -365,7 +373,7 @@ def _decode(windowed: bool, layout: Layout, q, page_tables, seq_lens, seq_lens_h
     lens_h = _host_i32(seq_lens_host, "seq_lens_host")
     if len(lens_h) != batch:
         raise ValueError("seq_lens_host must have one entry per row")
-    opts = _opts(merge_group, events)
+    opts = _opts(merge_group, events, append, layout.dtype)
     common = (_dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
               page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32))
     tail = (batch, hq, float(scale), num_splits, _dev(workspace_t, "workspace"),
@@ -383,19 +391,23 @@ def _decode(windowed: bool, layout: Layout, q, page_tables, seq_lens, seq_lens_h
 
 def decode_attn_splitkv(layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,
                         num_splits: int = 0, workspace=None, out=None, out_dtype=None,
-                        merge_group: int = 0, events=None, stream=None) -> torch.Tensor:
-    """Split-KV decode; returns ``out`` [batch, num_q_heads, head_dim]."""
+                        merge_group: int = 0, events=None, stream=None,
+                        append=None) -> torch.Tensor:
+    """Split-KV decode; returns ``out`` [batch, num_q_heads, head_dim].
+    ``append`` = (k_new, v_new, pages_of_row): each row's new K/V row, key
+    seq_lens - 1, is written into its page by the decode itself."""
     return _decode(False, layout, q, page_tables, seq_lens, seq_lens_host, scale, num_splits,
-                   workspace, out, out_dtype, merge_group, events, stream)
+                   workspace, out, out_dtype, merge_group, events, stream, append=append)
 
 
 def decode_attn_windowed(layout: Layout, q, page_tables, seq_lens, seq_lens_host, first_pos,
                          window_lo, scale, num_splits: int = 0, workspace=None, out=None,
                          out_dtype=None, merge_group: int = 0, events=None,
-                         stream=None) -> torch.Tensor:
+                         stream=None, append=None) -> torch.Tensor:
     """Windowed split-KV decode; keys at positions below ``window_lo`` are masked."""
     return _decode(True, layout, q, page_tables, seq_lens, seq_lens_host, scale, num_splits,
-                   workspace, out, out_dtype, merge_group, events, stream, first_pos, window_lo)
+                   workspace, out, out_dtype, merge_group, events, stream, first_pos, window_lo,
+                   append)
 
 
 def decode_attn_multirow(layout: Layout, q, page_tables, seq_lens, seq_lens_host, scale,

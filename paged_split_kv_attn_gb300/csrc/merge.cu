@@ -111,6 +111,7 @@ constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;     // threads per co
 
 __global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
   __shared__ float w_s[PSKV_MAX_SPLITS];             // level-1 weights, by partial
+  __shared__ float m_s[PSKV_MAX_SPLITS], l_s[PSKV_MAX_SPLITS];  // the row's partial (m, l)
   __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates], wg_s[kMaxStates];  // group states
   __shared__ float4 o1_s[kMaxStates][kColsPerBlock];  // group numerators of this block's columns
   __shared__ float M_s, L_s;
@@ -125,11 +126,17 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs
   pdl_launch_dependents();
   float4 v[kChunk];
   if (j < ng && d4 < dv4) load_chunk<false>(o, min(P, j * G + G), a.dv, d4, j * G, v);
+  // every (m, l) of the row in one round trip, staged in shared memory
+  for (int i = threadIdx.x; i < P; i += kMergeThreads) {
+    m_s[i] = m[i];
+    l_s[i] = l[i];
+  }
+  __syncthreads();
   // level-1 weights and group states
   for (int g = warp; g < ng; g += kMergeThreads / 32) {
     const int i0 = g * G, n = min(P, i0 + G) - i0;
     float Mg, Lg;
-    warp_state_weights<false>(m + i0, l + i0, n, w_s + i0, Mg, Lg, a.status, lane);
+    warp_state_weights<false>(m_s + i0, l_s + i0, n, w_s + i0, Mg, Lg, a.status, lane);
     if (lane == 0) {
       Mg_s[g] = Mg;
       Lg_s[g] = Lg;

@@ -125,6 +125,38 @@ __device__ __forceinline__ bool consumers_all(int n, bool pred) {
   return out != 0;
 }
 
+// The step's new K/V row of table row b, KV head g (key `key`), copied into
+// its page by one warp exactly as kv_append_rows would: the lease and the
+// page id are checked first, a bad one flags the fault word and skips the
+// copy.  The copy is made visible to the bulk-copy (async) proxy before the
+// same warp loads any tile.
+static __device__ void append_new_row(const PartialArgs &a, int b, int g, int key, int lane) {
+  const int lease = a.append_pages[b];
+  if (lease < 0 || lease > a.table_stride || (long long)key >= (long long)lease * a.page_size) {
+    if (lane == 0) raise_fault(a.status, PSKV_FAULT_PAST_PAGES);
+    return;
+  }
+  const int page = a.page_tables[(size_t)b * a.table_stride + key / a.page_size];
+  if (page < 0 || (long long)page >= a.num_pages) {
+    if (lane == 0) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
+    return;
+  }
+  const size_t src = (size_t)b * a.num_kv_heads + g;
+  const size_t dst = ((size_t)page * a.num_kv_heads + g) * a.page_size + key % a.page_size;
+  const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.append_k) +
+                                                    src * a.k_row_bytes);
+  const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.append_v) +
+                                                    src * a.v_row_bytes);
+  uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(const_cast<void *>(a.k_pool)) +
+                                        dst * a.k_row_bytes);
+  uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(const_cast<void *>(a.v_pool)) +
+                                        dst * a.v_row_bytes);
+  for (int v = lane; v < a.k_row_bytes / 16; v += 32) kd[v] = ks[v];
+  for (int v = lane; v < a.v_row_bytes / 16; v += 32) vd[v] = vs[v];
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 // The query tokens and keys one CTA serves: row b's tokens are query/output
 // rows r0 .. r0 + T - 1; token t sits at key len - T + t and sees keys up to
 // itself, from lo_fixed (a windowed decode's bound, else 0) or, with a
@@ -760,7 +792,15 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   const int n_my = (int)(hi_ll - lo_ll);
 
   const size_t row0 = ((size_t)b * a.num_q_heads + h0) * P + p;  // workspace state of head h0 (T = 1)
+  // The step's new row (key len - 1, single-token decode) is written by the
+  // CTA whose partition holds it; when no partition does (a window past the
+  // row's keys), by partition 0.
+  const bool append_here =
+      a.append_k != nullptr && cb == 0 &&
+      (k_lo < k_hi ? (len - 1 >= (t_begin) * kKeyTile && len - 1 < (t_begin + n_my) * kKeyTile)
+                   : p == 0);
   if (n_my <= 0) {  // empty partition: m = -inf, l = 0 (o is not written)
+    if (append_here && warp == 0) append_new_row(a, b, g, len - 1, lane);
     const int c0 = cb * C::kCols, c1 = min(c0 + C::kCols, T * G);  // this block's columns
     if (a.direct) {  // one partition and no key: zeros, flagged
       for (int i = c0 * D + threadIdx.x; i < c1 * D; i += blockDim.x) {
@@ -791,6 +831,10 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
     int cache_base = -1, cached = -1;
     int issued = 0;
     const uint64_t stream_policy = make_evict_first_policy();
+    if (append_here) {
+      append_new_row(a, b, g, len - 1, lane);
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the issuing lane's own order
+    }
     for (int j = 0; j < n_my; ++j) {
       const int s = j % NS;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;  // one decision for the whole warp

@@ -110,6 +110,12 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const bool folded = d.format == PSKV_FORMAT_FOLDED;
   const bool varlen = qs.cu_q_host != nullptr;
   if (varlen && !qs.cu_q) return PSKV_ERR_INVALID_ARG;
+  const bool append = opts && opts->append_k;
+  if (append) {
+    if (!opts->append_v || !opts->append_pages) return PSKV_ERR_INVALID_ARG;
+    if (!aligned(opts->append_k, 16) || !aligned(opts->append_v, 16)) return PSKV_ERR_INVALID_ARG;
+    if (varlen || qs.tokens != 1) return PSKV_ERR_UNSUPPORTED;  // single-token decode only
+  }
   if (qs.window < 0) return PSKV_ERR_INVALID_ARG;
   int rc = check_lengths(layout, batch, table_stride, seq_lens_host, varlen ? 1 : qs.tokens);
   if (rc) return rc;
@@ -184,6 +190,11 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.out = out;
   a.out_dtype = out_dtype;
   a.direct = direct ? 1 : 0;
+  a.append_k = append ? opts->append_k : nullptr;
+  a.append_v = append ? opts->append_v : nullptr;
+  a.append_pages = append ? opts->append_pages : nullptr;
+  a.k_row_bytes = layout->k_row_bytes;
+  a.v_row_bytes = layout->v_row_bytes;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)(P * col_blocks), d.num_kv_heads, batch);
@@ -530,6 +541,6 @@ const char *pskv_last_cuda_error(void) { return g_cuda_error; }
 
 uint64_t pskv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int pskv_version(void) { return 100; }
+int pskv_version(void) { return 101; }
 
 }  // extern "C"

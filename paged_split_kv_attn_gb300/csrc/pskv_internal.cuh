@@ -49,6 +49,10 @@ struct PartialArgs {
   void *out;            // [rows][Hq][D] of out_dtype: written directly when `direct`
   int out_dtype;
   int direct;           // one partition: write o / l to `out`, no partials, no merge
+  const void *append_k;  // [B][Hkv][Dk]: the new row of key len - 1 written by its CTA, or null
+  const void *append_v;  // [B][Hkv][Dv]
+  const int32_t *append_pages;  // [B] pages leased per row
+  int k_row_bytes, v_row_bytes;  // bytes of one stored K / V row of one head
 };
 
 // Arguments of the merge kernels.  Level 1 folds groups of `group` partials
