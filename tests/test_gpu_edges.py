@@ -1,0 +1,88 @@
+"""GPU edge cases: the largest split count, merge group sizes, wide ragged
+batches, one-key rows (closed form), and device lengths past the table."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_split_kv_attn_gb300 as pskv
+import workloads as W
+from gpu_cases import TOL, DevCase, i32, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_split_kv_attn_gb300 import build
+    build.build()
+    pskv.load_library()
+
+
+def ref_direct(c):
+    return oracle.decode_direct(c.q, c.k_pool, c.v_pool, c.page_tables, c.seq_lens, c.scale,
+                                c.first_pos, c.window_lo)
+
+
+def test_the_largest_split_count():
+    """PSKV_MAX_SPLITS partitions over 40,002 keys (2,501 tiles): most hold two
+    or three tiles, the merge folds 64 groups of 16."""
+    c = W.global_case(40002, seed=121)
+    dc = DevCase(c)
+    out = dc.decode(num_splits=pskv.PSKV_MAX_SPLITS)
+    torch.cuda.synchronize()
+    assert max_err(out, ref_direct(c)) <= TOL
+    assert dc.faults() == 0
+
+
+@pytest.mark.parametrize("group,splits", [(1, 48), (5, 48), (16, 48), (3, 7)])
+def test_merge_group_sizes(group, splits):
+    c = W.global_case(10602, seed=122)
+    dc = DevCase(c)
+    out = dc.decode(num_splits=splits, merge_group=group)
+    torch.cuda.synchronize()
+    assert max_err(out, ref_direct(c)) <= TOL
+    assert dc.faults() == 0
+
+
+def test_wide_ragged_batch():
+    """64 rows of 1 to 3,000 keys in one call (grid z = 64), automatic plan."""
+    rng = np.random.default_rng(123)
+    lens = [1, 2, 15, 16, 17] + [int(x) for x in rng.integers(1, 3000, 59)]
+    c = W.make_paged_case(123, lens, num_q_heads=32, num_kv_heads=4, head_dim=512,
+                          page_size=256)
+    dc = DevCase(c)
+    out = dc.decode()
+    torch.cuda.synchronize()
+    assert max_err(out, ref_direct(c)) <= TOL
+    assert dc.faults() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_one_key_rows_return_their_value_exactly(splits):
+    """With one key the softmax weight is exactly 1: the output is the value
+    row itself, bit for bit, in both output types."""
+    c = W.make_paged_case(124, [1, 1, 700], num_q_heads=32, num_kv_heads=4, head_dim=512,
+                          page_size=256)
+    dc = DevCase(c)
+    out32 = dc.decode(num_splits=splits, out_dtype=torch.float32)
+    out16 = dc.decode(num_splits=splits, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    for b in (0, 1):
+        page = int(c.page_tables[b, 0])
+        v = torch.from_numpy(W.bf16_to_f32(c.v_pool[page, :, 0, :]))  # [Hkv, D]
+        exp = v.repeat_interleave(8, dim=0)  # query head h reads KV head h // 8
+        assert torch.equal(out32[b].cpu(), exp)
+        assert torch.equal(out16[b].cpu().float(), exp)
+
+
+def test_device_length_past_the_table_is_flagged():
+    """A device length beyond table_stride * page_size is clamped to the table
+    (entries there point at an in-bounds page) and flagged PSKV_FAULT_BAD_LENGTH."""
+    c = W.make_paged_case(125, [300], num_q_heads=8, num_kv_heads=1, head_dim=512,
+                          page_size=256)
+    dc = DevCase(c)
+    pskv.decode_attn_splitkv(dc.layout, dc.q, dc.tables, i32([1 << 30]), c.seq_lens, c.scale,
+                             num_splits=3)
+    torch.cuda.synchronize()
+    assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
