@@ -298,7 +298,11 @@ class Call:
 class Packed:
     """The step's small per-step tensors (queries, new K/V rows, positions; and
     the outputs) packed into one device buffer each way, with pinned host
-    twins, so the end-to-end step moves them with one copy in and one out."""
+    twins, so the end-to-end step moves them with one copy in and one out.
+
+    Two sets of device buffers alternate between steps, so that step i+1's
+    inputs can be copied in while step i computes and step i's outputs are
+    copied out while step i+1 computes (a copy stream each way)."""
 
     def __init__(self, calls, dev):
         import torch
@@ -315,22 +319,60 @@ class Packed:
                 v.copy_(t)
                 views.append(v)
             return buf, views
+        self.calls = calls
         ins = [(c, k, t) for c in calls for k, t in c.step_inputs().items()]
-        self.dev_in, views = pack([t for _, _, t in ins])
-        for (c, k, _), v in zip(ins, views):
-            setattr(c, k, v)
-        self.dev_out, outs = pack([c.out for c in calls])
-        for c, v in zip(calls, outs):
-            c.out = v
+        self.keys = [(c, k) for c, k, _ in ins]
+        self.dev_in, self.in_views, self.dev_out, self.out_views = [], [], [], []
+        for _ in range(2):
+            buf, views = pack([t for _, _, t in ins])
+            self.dev_in.append(buf)
+            self.in_views.append(views)
+            buf, views = pack([c.out for c in calls])
+            self.dev_out.append(buf)
+            self.out_views.append(views)
+        self.bind(0)
         torch.cuda.synchronize()
-        self.host_in = self.dev_in.cpu().pin_memory()
-        self.host_out = torch.empty_like(self.dev_out, device="cpu").pin_memory()
+        self.host_in = self.dev_in[0].cpu().pin_memory()
+        self.host_out = [torch.empty_like(self.dev_out[0], device="cpu").pin_memory()
+                         for _ in range(2)]
+        self.h2d_stream, self.d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+        self.h2d_done = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.d2h_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step_e2e(self, calls, it: int):
-        self.dev_in.copy_(self.host_in, non_blocking=True)
-        for c in calls:
-            c.run(it)
-        self.host_out.copy_(self.dev_out, non_blocking=True)
+    def bind(self, parity: int):
+        """Point the calls' step tensors at buffer set `parity`."""
+        for (c, k), v in zip(self.keys, self.in_views[parity]):
+            setattr(c, k, v)
+        for c, v in zip(self.calls, self.out_views[parity]):
+            c.out = v
+
+    def step_e2e(self, it: int, run_step, started):
+        """Copy step `it`'s inputs in, run it (run_step(it, parity)), copy its
+        outputs out; `started` is an event recorded where the timed region starts."""
+        import torch
+        p = it % 2
+        compute = torch.cuda.current_stream()
+        with torch.cuda.stream(self.h2d_stream):
+            self.h2d_stream.wait_event(started)
+            if it >= 2:
+                self.h2d_stream.wait_event(self.computed[p])  # step it-2 has used these inputs
+            self.dev_in[p].copy_(self.host_in, non_blocking=True)
+            self.h2d_done[p].record(self.h2d_stream)
+        compute.wait_event(self.h2d_done[p])
+        if it >= 2:
+            compute.wait_event(self.d2h_done[p])  # step it-2's outputs have left this buffer
+        run_step(it, p)
+        self.computed[p].record(compute)
+        with torch.cuda.stream(self.d2h_stream):
+            self.d2h_stream.wait_event(self.computed[p])
+            self.host_out[p].copy_(self.dev_out[p], non_blocking=True)
+            self.d2h_done[p].record(self.d2h_stream)
+
+    def finish(self, it_last: int):
+        """Make the compute stream wait for the last outputs to reach the host."""
+        import torch
+        torch.cuda.current_stream().wait_event(self.d2h_done[it_last % 2])
 
 
 class PrefillCall:
@@ -585,6 +627,9 @@ def main():
     graphs = None
     if not args.eager:
         graphs, launches_per_step = capture(calls)
+        packed.bind(1)  # the same step over the second set of input/output buffers
+        graphs_b, _ = capture(calls)
+        packed.bind(0)
 
     def timed(run_step):
         """K steps between events on the stream, barrier and synchronize on both sides."""
@@ -714,11 +759,32 @@ def main():
         del pgraphs, pcalls
 
     # end-to-end through the public calls: each step copies its inputs in from
-    # pinned host memory (one copy) and its outputs back (one copy)
-    for it in range(args.warmup):
-        packed.step_e2e(calls, it)
-    torch.cuda.synchronize()
-    e2e_ms = timed(lambda it: packed.step_e2e(calls, it))
+    # pinned host memory (one copy) and its outputs back (one copy); the copies
+    # of neighbouring steps overlap the step in between (two buffer sets)
+    def run_e2e(it, parity):
+        if graphs is not None:
+            (graphs, graphs_b)[parity][it % ROTATE].replay()
+        else:
+            packed.bind(parity)
+            for c in calls:
+                c.run(it)
+
+    def timed_e2e(steps):
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for it in range(steps):
+            packed.step_e2e(it, run_e2e, t0)
+        packed.finish(steps - 1)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        return dist.max(t0.elapsed_time(t1) / steps)
+
+    timed_e2e(max(args.warmup, 2))
+    e2e_ms = timed_e2e(args.steps)
+    packed.bind(0)
 
     for c in calls:
         if c.status[0].item() != 0:
@@ -767,7 +833,9 @@ def main():
             "e2e": {"value": whole_job_gbps(step_bytes, dist.world, e2e_ms), "unit": "GB/s",
                     "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": packed.host_in.numel(),
-                    "d2h_bytes_per_step": packed.host_out.numel()},
+                    "d2h_bytes_per_step": packed.host_out[0].numel(),
+                    "copies": "one packed copy in and one out per step, each on its own "
+                              "stream, overlapping the neighbouring steps' compute"},
             "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
     if sweep is not None:
         line["split_sweep_us"] = sweep
