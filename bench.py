@@ -55,10 +55,16 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_mma_d512_ctx40002.md")
 
 
 def partial_kernel_hash() -> str:
+    """Hash of the partial kernel's code (comments and blank space left out, so
+    that editing a comment keeps the recorded counters valid)."""
+    import re
     h = hashlib.sha256()
     for rel in PARTIAL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

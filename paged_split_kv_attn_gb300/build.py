@@ -63,7 +63,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, defines: dict | None
     """Compile and link the library unless it is newer than every source; return its path.
 
     ``defines`` sets the compile-time tuning macros (for example
-    ``{"PSKV_MMA_WARPS": 4}``); a build with defines goes to ``out`` and is
+    ``{"PSKV_MMA_STAGES": 4}``); a build with defines goes to ``out`` and is
     always rebuilt."""
     extra = [f"-D{k}={v}" for k, v in (defines or {}).items()]
     if not force and not verbose_ptxas and not extra and out == LIB and _up_to_date():

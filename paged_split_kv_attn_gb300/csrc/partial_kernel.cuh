@@ -1,30 +1,35 @@
-// partial_kernel.cuh -- the split-KV partial kernel (decode, one query token per row).
+// partial_kernel.cuh -- the split-KV partial kernel (decode, verify windows, prefill).
 //
 // One CTA computes the online-softmax partial of one (row b, KV head g,
-// partition p): for the G query heads that share KV head g it streams the
-// partition's keys and values once and keeps, per head, the running max m,
-// the running sum l and the unnormalised numerator o (gem "Parked D512 fused
-// split-KV decode design", "Candidate ownership and storage": one first-pass
-// worker per (kv_head, partition), each K/V row staged once for all query
-// heads of the group).
+// partition p[, column block]): for the query columns it serves (the G query
+// heads that share KV head g, times the row's query tokens in a verify window
+// or a prefill chunk) it streams the partition's keys and values once and
+// keeps, per column, the running max m, the running sum l and the
+// unnormalised numerator o (gem "Parked D512 fused split-KV decode design",
+// "Candidate ownership and storage": one first-pass worker per (kv_head,
+// partition), each K/V row staged once for all query heads of the group).
 //
 // Structure (GB300):
 //  * the last warp is the producer: per 16-key tile it reads the tile's page id
 //    from the table (32 ids per warp-wide load, so one table read serves up to
 //    32 pages; TensorFold #1619 measured a per-key page lookup at +5.8..7.9 %
-//    and moved it to once per tile) and issues one bulk async copy
-//    (cp.async.bulk) per valid key row into a ring of shared-memory stages,
-//    counted on the stage's "full" mbarrier;
-//  * the other CW warps are consumers: warp w takes tiles w, w+CW, w+2CW, ...
-//    of the partition, each keeping its own (m, l, o) in registers, and
-//    releases the stage on its "empty" mbarrier.  Stage s always belongs to
-//    warp s % CW;
-//  * at the end the warp states are merged in shared memory by the exact
-//    rescaling identity and the partition's (m, l, o) is written to the
-//    workspace.
-// Rows of a tile past the row's length (or below the window bound) are never
-// copied; their scores are set to -inf by selection and their values masked
-// to zero, so stale shared memory can never reach the result.
+//    and moved it to once per tile) and issues bulk async copies
+//    (cp.async.bulk, L2 evict-first) of the tile's valid key rows into a ring
+//    of shared-memory stages, counted on the stage's "full" mbarrier.  When the
+//    call carries the step's new K/V row, the CTA whose partition holds it
+//    first writes it into its page;
+//  * the other warps are consumers.  On the tensor-core path (bf16) they all
+//    take every tile together (MmaConsumer, below); on the CUDA-core path
+//    (f32 pools, 16 query heads per KV head) warp w takes tiles w, w+CW, ...
+//    with its own (m, l, o), and the warp states are merged in shared memory
+//    at the end (SimtConsumer);
+//  * the partition's (m, l, o) per column goes to the workspace for the merge
+//    kernel, or, when the call has a single partition, the CTA normalises and
+//    writes its output itself.
+// Keys outside a column's visible range (past its token, below a window bound,
+// past the row) are masked: rows outside the CTA's key range are never copied,
+// scores are set to -inf by selection and values masked to zero, so stale
+// shared memory can never reach the result.
 //
 // Copy granularity: the bulk copy engine's per-copy cost dominates below
 // about 2 KB (1 KB copies streamed at ~4.6 TB/s on GB300, 2 KB copies at

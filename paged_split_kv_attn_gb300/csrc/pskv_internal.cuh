@@ -55,9 +55,9 @@ struct PartialArgs {
   int k_row_bytes, v_row_bytes;  // bytes of one stored K / V row of one head
 };
 
-// Arguments of the merge kernels.  Level 1 folds groups of `group` partials
-// of each row into (m1, l1, o1); level 2 folds `count` states per row and
-// writes the normalised output.
+// Arguments of the merge kernel: level 1 folds groups of `group` partials of
+// each row into group states (on chip), level 2 folds a row's group states
+// and writes the normalised output.
 struct MergeArgs {
   const float *m;  // [rows][count]
   const float *l;
