@@ -725,22 +725,26 @@ def main():
             if c.windowed:
                 continue
             res = {}
-            for p in args.sweep:
+            ws0 = c.ws  # the step's graphs point at this workspace: keep it alive and restore it
+            for p in args.sweep + [0]:
                 c.splits = p
                 c.ws = pskv.workspace(1, 32, 512, p, dev)
+                cg, _ = capture([c])  # each split count replayed from its own graphs
                 times = []
                 for it in range(10):
                     flush.sum()
                     b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     b.record(stream)
-                    c.run(it)
+                    cg[it % ROTATE].replay()
                     e.record(stream)
                     torch.cuda.synchronize()
                     times.append(b.elapsed_time(e) * 1e3)
-                res[p] = statistics.median(times)
+                del cg
+                key = p if p else "auto(%d)" % pskv.pskv_plan_splits(c.layouts[0], 32, c.lens_host)
+                res[key] = statistics.median(times)
             sweep[c.name] = res
             c.splits = args.splits
-            c.ws = pskv.workspace(1, 32, 512, args.splits, dev)
+            c.ws = ws0
     del flush
 
     # the same step with the fused K/V prep in place of the row copy (projection

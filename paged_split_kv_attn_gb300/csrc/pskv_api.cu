@@ -153,7 +153,9 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
     // every partition launches col_blocks CTAs
     const int64_t per = slots / col_blocks;
-    P = plan_splits(per > 0 ? (int)per : 1, batch, d.num_kv_heads, seq_lens_host);
+    const bool bytes_bound = kernel == kKernelMma && !folded && columns <= 8;
+    P = plan_splits(per > 0 ? (int)per : 1, batch, d.num_kv_heads, seq_lens_host,
+                    bytes_bound ? kFillBytes32 : 32);
   }
   // one partition on the tensor-core kernels: the partial is the output
   const bool direct = P == 1 && kernel == kKernelMma;
@@ -520,7 +522,12 @@ int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_hea
   const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_v,
                                num_q_heads / layout->d.num_kv_heads, layout->d.format, 1, &slots);
   if (rc) return rc;
-  *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host);
+  const bool bytes_bound =
+      pick_kernel(layout->d.kv_dtype, layout->d.head_dim_v, num_q_heads / layout->d.num_kv_heads,
+                  layout->d.format) == kKernelMma &&
+      layout->d.format != PSKV_FORMAT_FOLDED;
+  *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host,
+                            bytes_bound ? kFillBytes32 : 32);
   return PSKV_OK;
 }
 

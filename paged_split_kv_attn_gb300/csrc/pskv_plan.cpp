@@ -66,7 +66,8 @@ int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride
   return PSKV_OK;
 }
 
-int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host) {
+int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host,
+                int fill32) {
   if (slots < 1) slots = 1;
   int64_t total_tiles = 0, max_tiles = 0;
   for (int32_t b = 0; b < batch; ++b) {
@@ -77,10 +78,14 @@ int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *s
   }
   if (max_tiles == 0) return 1;
   // The longest row's pieces should carry about total_tiles * Hkv / slots tiles
-  // each (one wave of CTAs when all rows are equal); for a batch, twice as
-  // many pieces, so that short rows' CTAs fill the tail.
-  int64_t p = (max_tiles * (int64_t)slots) / (total_tiles * (int64_t)num_kv_heads);
+  // each (one wave of CTAs when all rows are equal), filled to fill32 / 32 of
+  // the slots (see pskv_plan.h).  For a batch, twice as many pieces, so that
+  // short rows' CTAs fill the tail.  A piece keeps at least three tiles (short
+  // windows are bound by each CTA's start, not by bytes).
+  if (fill32 < 1 || fill32 > 32) fill32 = 32;
+  int64_t p = (max_tiles * (int64_t)slots * fill32) / (total_tiles * (int64_t)num_kv_heads * 32);
   if (batch > 1) p *= 2;
+  if (p > max_tiles / 3) p = max_tiles / 3;
   if (p < 1) p = 1;
   if (p > max_tiles) p = max_tiles;
   if (p > PSKV_AUTO_MAX_SPLITS) p = PSKV_AUTO_MAX_SPLITS;

@@ -36,8 +36,17 @@ int plan_workspace(int64_t batch, int64_t num_q_heads, int64_t head_dim_v, int64
 int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride,
                   const int32_t *seq_lens_host, int32_t min_len = 1);
 
-// Automatic split count for `slots` CTA slots (SMs x CTAs per SM).
-int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host);
+// Automatic split count for `slots` CTA slots (SMs x CTAs per SM), filling
+// fill32 / 32 of them.  Byte-bound calls (the split-format single-token decode
+// on the tensor-core kernel) fill 27/32: with a few SMs running one CTA
+// instead of two the stream still saturates HBM, and fewer, longer pieces
+// spend less on each CTA's start and on the merge (measured on GB300 over
+// 10.6K-163K keys: 64 pieces of a 304-slot grid beat 76 by 1-3.5 % per call).
+// Calls with more arithmetic per byte (folded rows, verify windows, prefill)
+// fill every slot.
+constexpr int kFillBytes32 = 27;
+int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host,
+                int fill32 = 32);
 
 // Checks host copies of an append's rows against the leases.
 int check_append_host(const pskv_layout *layout, int32_t n, int32_t table_stride, int32_t batch,

@@ -62,8 +62,11 @@ int main() {
   CHECK(check_lengths(&lay, 3, 4, lens.data()) == PSKV_ERR_INVALID_ARG);
 
   std::vector<int32_t> one = {40002};
-  CHECK(plan_splits(304, 1, 4, one.data()) == 76);
+  CHECK(plan_splits(304, 1, 4, one.data()) == 76);                // every slot
+  CHECK(plan_splits(304, 1, 4, one.data(), kFillBytes32) == 64);  // 27/32 of 76
   CHECK(plan_splits(152, 1, 4, one.data()) == 38);
+  std::vector<int32_t> window = {1024};                           // 64 tiles: 3 per piece
+  CHECK(plan_splits(608, 1, 16, window.data(), kFillBytes32) == 21);
   std::vector<int32_t> tiny = {5};
   CHECK(plan_splits(304, 1, 4, tiny.data()) == 1);
   std::vector<int32_t> ragged = {131072, 1, 5000, 17, 90000};
