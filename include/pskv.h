@@ -406,6 +406,13 @@ int decode_attn_splitkv_static(const pskv_layout *layout, const void *q,
                                int32_t num_splits, void *out, int32_t out_dtype,
                                pskv_stream_t stream);
 
+/* Read the layout's fault word: copies status[0] to *flags after all work
+ * already enqueued on `stream`, and optionally clears it for the next calls.
+ * This call synchronizes the stream (the only one that does).  A layout made
+ * without a status word reads as 0.  Errors: INVALID_ARG, CUDA. */
+int pskv_check_flags(const pskv_layout *layout, int32_t clear, pskv_stream_t stream,
+                     uint32_t *flags);
+
 /* Static text for a status code. */
 const char *pskv_strerror(int status);
 

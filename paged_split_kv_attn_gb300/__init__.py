@@ -9,7 +9,8 @@ from ._binding import (EXPORTS, Layout, PskvError, decode_attn_multirow, decode_
                        decode_attn_splitkv_static, decode_attn_windowed,
                        decode_attn_workspace_bytes, kv_append_rows, kv_prep_append, load_library,
                        merge_partials, merge_partials_workspace_bytes, paged_kv_layout_create,
-                       pskv_kernel_launches, pskv_partial_scratch_bytes, pskv_plan_splits,
+                       pskv_check_flags, pskv_kernel_launches, pskv_partial_scratch_bytes,
+                       pskv_plan_splits,
                        prefill_attn_paged,
                        pskv_strerror, pskv_version, workspace)
 
@@ -17,7 +18,8 @@ __all__ = ["EXPORTS", "Layout", "PskvError", "decode_attn_multirow", "decode_att
            "decode_attn_splitkv_static", "decode_attn_windowed",
            "decode_attn_workspace_bytes", "kv_append_rows", "kv_prep_append", "load_library",
            "merge_partials",
-           "merge_partials_workspace_bytes", "paged_kv_layout_create", "pskv_kernel_launches",
+           "merge_partials_workspace_bytes", "paged_kv_layout_create", "pskv_check_flags",
+           "pskv_kernel_launches",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "pskv_strerror", "pskv_version",
            "prefill_attn_paged",
            "workspace"]

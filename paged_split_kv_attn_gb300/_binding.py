@@ -49,7 +49,8 @@ EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows"
            "prefill_attn_paged", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
-           "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches", "pskv_version")
+           "pskv_check_flags", "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches",
+           "pskv_version")
 
 
 class PskvError(RuntimeError):
@@ -115,6 +116,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pskv_partial_scratch_bytes.argtypes = [I64, I64, I64, I64] + [ctypes.POINTER(SZ)] * 4
     lib.pskv_plan_splits.argtypes = [P, I32, I32, P, ctypes.POINTER(I32)]
     lib.decode_attn_splitkv_static.argtypes = [P, P, P, I32, P, P, I32, I32, F, I32, P, I32, P]
+    lib.pskv_check_flags.argtypes = [P, I32, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.pskv_strerror.argtypes = [ctypes.c_int]
     lib.pskv_strerror.restype = ctypes.c_char_p
     lib.pskv_last_cuda_error.argtypes = []
@@ -514,6 +516,15 @@ def merge_partials(m, l, o, out=None, out_dtype=None, workspace=None, status=Non
                               None if opts is None else ctypes.byref(opts), _stream(stream)),
            "merge_partials")
     return out
+
+
+def pskv_check_flags(layout: Layout, clear: bool = False, stream=None) -> int:
+    """The layout's fault word (PSKV_FAULT_* bits) after the work enqueued so
+    far; synchronizes the stream.  ``clear`` zeroes it for the next calls."""
+    flags = ctypes.c_uint32()
+    _check(load_library().pskv_check_flags(layout.handle, int(clear), _stream(stream),
+                                           ctypes.byref(flags)), "pskv_check_flags")
+    return int(flags.value)
 
 
 def pskv_strerror(code: int) -> str:

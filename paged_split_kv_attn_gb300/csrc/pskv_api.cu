@@ -548,6 +548,22 @@ const char *pskv_last_cuda_error(void) { return g_cuda_error; }
 
 uint64_t pskv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int pskv_version(void) { return 101; }
+int pskv_version(void) { return 102; }
+
+int pskv_check_flags(const pskv_layout *layout, int32_t clear, pskv_stream_t stream,
+                     uint32_t *flags) {
+  if (!layout || !flags) return PSKV_ERR_INVALID_ARG;
+  *flags = 0;
+  int32_t *status = layout->d.status;
+  if (!status) return PSKV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = (uint32_t)word;
+  return PSKV_OK;
+}
 
 }  // extern "C"

@@ -86,3 +86,6 @@ def test_device_length_past_the_table_is_flagged():
                              num_splits=3)
     torch.cuda.synchronize()
     assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
+    # the library's reader sees the same word, and clears it on request
+    assert pskv.pskv_check_flags(dc.layout, clear=True) & pskv.PSKV_FAULT_BAD_LENGTH
+    assert pskv.pskv_check_flags(dc.layout) == 0
