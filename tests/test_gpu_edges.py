@@ -89,3 +89,20 @@ def test_device_length_past_the_table_is_flagged():
     # the library's reader sees the same word, and clears it on request
     assert pskv.pskv_check_flags(dc.layout, clear=True) & pskv.PSKV_FAULT_BAD_LENGTH
     assert pskv.pskv_check_flags(dc.layout) == 0
+
+
+def test_device_lengths_rule_over_the_host_copy():
+    """The kernels read the device lengths; the host copy only plans (and lets
+    the producer read its first page ids early).  A device length that differs
+    from the host copy -- as in a captured graph replayed after the device
+    lengths moved -- still decodes exactly its own keys."""
+    import dataclasses
+    c = W.global_case(12000, seed=126)
+    dc = DevCase(c)
+    for dev_len in (9000, 11999, 12000):
+        out = pskv.decode_attn_splitkv(dc.layout, dc.q, dc.tables, i32([dev_len]), c.seq_lens,
+                                       c.scale, num_splits=0, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        ref = ref_direct(dataclasses.replace(c, seq_lens=np.array([dev_len], np.int32)))
+        assert max_err(out, ref) <= TOL, dev_len
+    assert dc.faults() == 0
