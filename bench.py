@@ -654,9 +654,23 @@ def main():
         for c in calls:
             c.run(it)
 
+    def keep_busy(seconds: float):
+        """Replay the step for about `seconds`, so that the clock samples taken
+        around the timed region see the GPU under this load."""
+        t_end = time.perf_counter() + seconds
+        it = 0
+        while time.perf_counter() < t_end:
+            for _ in range(64):
+                if graphs is not None:
+                    graphs[it % ROTATE].replay()
+                else:
+                    eager_step(it)
+                it += 1
+            torch.cuda.synchronize()
+
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    time.sleep(0.3)
+    keep_busy(0.4)
     launches0 = pskv.pskv_kernel_launches()
     if graphs is not None:
         ms = timed(lambda it: graphs[it % ROTATE].replay())
@@ -664,7 +678,9 @@ def main():
     else:
         ms = timed(eager_step)
         launches = pskv.pskv_kernel_launches() - launches0
+    keep_busy(0.2)
     clock_info = clocks.stop()
+    clock_info["window"] = "sampled every 100 ms while the step ran: 0.4 s before the timed region, then it, then 0.2 s"
     value = whole_job_gbps(step_bytes, dist.world, ms)
     eager_ms = ms if graphs is None else timed(eager_step)
 
