@@ -240,9 +240,10 @@ int kv_prep_append(const pskv_layout *layout, const pskv_prep_desc *prep, const 
  *   workspace      device scratch of at least decode_attn_workspace_bytes(...)
  *                  bytes, 256-byte aligned (NULL is fine with num_splits = 1 on
  *                  a bf16 pool with 1/2/4/8 query heads per KV head: the one
- *                  partition then writes the output itself and no merge runs).  On return its head holds the
- *                  partials: float m[batch][num_q_heads][P], then (at the next
- *                  256-byte boundary) float l[...][P], then float
+ *                  partition then writes the output itself and no merge runs).
+ *                  Otherwise, on return its head holds the partials: float
+ *                  m[batch][num_q_heads][P], then (at the next 256-byte
+ *                  boundary) float l[...][P], then float
  *                  o[batch][num_q_heads][P][head_dim] (m in units of the scaled
  *                  score; o of a partition with m = -inf is left unwritten).
  *   out            device [batch][num_q_heads][head_dim] of out_dtype
