@@ -92,8 +92,8 @@ def test_device_length_past_the_table_is_flagged():
 
 
 def test_device_lengths_rule_over_the_host_copy():
-    """The kernels read the device lengths; the host copy only plans (and lets
-    the producer read its first page ids early).  A device length that differs
+    """The kernels read the device lengths; the host copy only plans.  A
+    device length that differs
     from the host copy -- as in a captured graph replayed after the device
     lengths moved -- still decodes exactly its own keys."""
     import dataclasses
