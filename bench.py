@@ -436,8 +436,8 @@ def make_prefill_calls(args, dev):
 
 
 def make_extra_calls(args, dev):
-    """Calls measured one at a time beside the step: the folded format and
-    verify windows of the global shape (multi-row decode)."""
+    """Calls measured one at a time beside the step: the folded format, verify
+    windows of the global shape (multi-row decode) and a ragged batch."""
     prep, fused = args.append == "prep", args.append == "fused"
     calls = [Call(f"folded_{ctx}", W.folded_case(ctx, seed=ctx + 1), False, args.splits, dev,
                   ROTATE, prep=prep, fused=fused) for ctx in args.folded_contexts]
@@ -445,6 +445,9 @@ def make_extra_calls(args, dev):
         ctx = args.verify_context
         calls.append(Call(f"verify_{ctx}x{t}", W.global_case(ctx, seed=ctx + 2), False,
                           args.splits, dev, ROTATE, tokens=t, prep=prep))
+    if not args.no_ragged:
+        calls.append(Call("ragged16", W.ragged_case(0), False, args.splits, dev, ROTATE,
+                          prep=prep, fused=fused))
     return calls
 
 
@@ -492,6 +495,8 @@ def parse():
     ap.add_argument("--splits", type=int, default=0, help="global-layer split count (0 = auto)")
     ap.add_argument("--window-splits", type=int, default=0)
     ap.add_argument("--no-window", action="store_true")
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the 16-row ragged batch timed beside the step")
     ap.add_argument("--append", choices=["fused", "copy", "prep"], default="fused",
                     help="new tokens of the step: K/V rows written by the decode itself, "
                          "copied into the pages by a separate launch, or projection rows "
@@ -710,8 +715,9 @@ def main():
         part = [b.elapsed_time(e) for b, e in pe]
         per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
                             "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9,
-                            "note": ("folded format" if c.tokens == 1 else
-                                     f"verify window of {c.tokens} tokens")
+                            "note": ("16-row ragged batch (lengths log-uniform up to 131,072)"
+                                     if c.name == "ragged16" else "folded format"
+                                     if c.tokens == 1 else f"verify window of {c.tokens} tokens")
                             + ", measured beside the step (not in value)"}
     # each call replayed from its own graphs, so host launch overhead stays out
     flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
