@@ -3,6 +3,7 @@
 // Each entry point checks its host-visible arguments (pskv_plan.cpp), makes
 // the plan, carves the caller's workspace and enqueues the kernels on the
 // caller's stream.  It never allocates device memory and never synchronizes.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -147,8 +148,25 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int mgroup = 0;
   if ((rc = merge_group_of(opts, &mgroup))) return rc;
 
+  // Prefill at head dim 256 (bf16, split pools) runs on the tensor-memory
+  // kernel: blocks of 128 query columns, one CTA per block and partition.
+  const bool tc_path = varlen && kernel == kKernelMma && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
+                       d.head_dim_k == 256 && d.head_dim_v == 256 && (group & (group - 1)) == 0 &&
+                       aligned(d.k_pool, 16) && aligned(d.v_pool, 16) &&
+                       (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
+  const int64_t tc_qblocks = (columns + 127) / 128;
+  if (tc_path && tc_qblocks * PSKV_MAX_SPLITS > INT32_MAX) return PSKV_ERR_INVALID_ARG;
   int P = num_splits;
-  if (P == 0) {
+  if (P == 0 && tc_path) {
+    // one wave at least: split the keys only when the blocks alone leave SMs idle
+    int n_sm = 0;
+    if ((rc = sm_count(&n_sm))) return rc;
+    const int64_t ctas = tc_qblocks * d.num_kv_heads * batch;
+    int64_t max_len = 1;
+    for (int32_t b = 0; b < batch; ++b) max_len = seq_lens_host[b] > max_len ? seq_lens_host[b] : max_len;
+    const int64_t cap = std::max<int64_t>(1, (max_len + 63) / 64 / 4);  // >= 4 tiles per partition
+    P = (int)std::min<int64_t>({(n_sm + ctas - 1) / ctas, cap, (int64_t)PSKV_AUTO_MAX_SPLITS});
+  } else if (P == 0) {
     int slots = 0;
     if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
     // every partition launches col_blocks CTAs
@@ -205,7 +223,34 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (kernel == kKernelMma)
+  if (tc_path) {
+    TcArgs t;
+    t.q = q;
+    t.page_tables = page_tables;
+    t.seq_lens = seq_lens;
+    t.cu_q = qs.cu_q;
+    t.status = d.status;
+    t.ws_m = a.ws_m;
+    t.ws_l = a.ws_l;
+    t.ws_o = a.ws_o;
+    t.out = out;
+    t.out_dtype = out_dtype;
+    t.direct = direct ? 1 : 0;
+    t.num_pages = d.num_pages;
+    t.table_stride = table_stride;
+    t.page_size = d.page_size;
+    t.num_kv_heads = d.num_kv_heads;
+    t.num_q_heads = num_q_heads;
+    t.group_shift = __builtin_ctz((unsigned)group);
+    t.num_splits = P;
+    t.qblocks = (int)tc_qblocks;
+    t.total_rows = (int)rows;
+    t.window = qs.window;
+    t.box_rows = d.page_size % 64 == 0 ? 64 : 16;
+    t.scale_log2 = scale * kLog2e;
+    e = launch_attn_tc(t, d.k_pool, d.v_pool,
+                       dim3((unsigned)(tc_qblocks * P), d.num_kv_heads, batch), s);
+  } else if (kernel == kKernelMma)
     e = launch_partial_mma(a, d.head_dim_v, group, folded, nt, grid, s);
   else if (d.kv_dtype == PSKV_DTYPE_F32)
     e = launch_partial_simt_f32(a, d.head_dim_v, group, grid, s);

@@ -1,0 +1,172 @@
+"""GPU parity of paged prefill at head dim 256, the tensor-memory (tcgen05)
+kernel's shape, against the oracle.
+
+The kernel serves blocks of 128 query columns (tokens x the KV group's
+heads), 64-key tiles brought in by tensor copies in 16- or 64-row boxes
+(pages of 16 or 32 keys, pages of 64 or more), one CTA per block and
+partition.  Cases cover several blocks with a ragged last one, every group
+size, windows that cut tiles anywhere, empty partitions, pages outside the
+pool and the NaN-filled rows the generator leaves past each row's keys.
+Bars as for decode: max |out - fp64| <= 2e-3 in the fp32 output mode, the
+bf16 output the round-to-nearest-even of the fp32 one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_split_kv_attn_gb300 as pskv
+import workloads as W
+from gpu_cases import TOL, DevCase, bf16_of, i32, max_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_split_kv_attn_gb300 import build
+    build.build()
+    pskv.load_library()
+
+
+def _cu(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def _q(case, counts, seed=0):
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 11])))
+    q = rng.standard_normal((int(sum(counts)), case.num_q_heads, case.head_dim), dtype=np.float32)
+    return W.bf16_bits(q)
+
+
+def _case(seed, lens, hq, hkv, ps, **kw):
+    return W.make_paged_case(seed, lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=256,
+                             page_size=ps, dtype="bf16", **kw)
+
+
+def run(dc, q, cu, window=0, splits=0, out_dtype=torch.float32, tables=None):
+    c = dc.case
+    return pskv.prefill_attn_paged(dc.layout, q, i32(cu), cu,
+                                   dc.tables if tables is None else tables, dc.lens, c.seq_lens,
+                                   c.scale, window=window, num_splits=splits, out_dtype=out_dtype)
+
+
+def check(case, counts, window=0, splits=(0,), seed=0):
+    dc = DevCase(case)
+    qn = _q(case, counts, seed)
+    cu = _cu(counts)
+    ref = oracle.prefill_direct(qn, cu, case.k_pool, case.v_pool, case.page_tables,
+                                case.seq_lens, case.scale, window)
+    q = to_dev(qn, "bf16")
+    for p in splits:
+        out32 = run(dc, q, cu, window, p)
+        out16 = run(dc, q, cu, window, p, torch.bfloat16)
+        torch.cuda.synchronize()
+        assert np.all(np.isfinite(out32.cpu().numpy())), f"non-finite output (splits={p})"
+        err = max_err(out32, ref)
+        assert err <= TOL, f"max |err| {err:.3e} > {TOL} (splits={p})"
+        assert torch.equal(out16, bf16_of(out32)), "bf16 output is not RNE of the fp32 output"
+    assert dc.faults() == 0
+
+
+def test_causal_prompt_several_blocks():
+    """32 q / 16 KV heads (G = 2), pages of 64: a whole prompt of 300 tokens
+    (600 columns: four full blocks and one of 88) and a chunk of 40 at 517
+    keys; one partition, three, and the automatic plan."""
+    check(_case(201, [300, 517], 32, 16, 64), [300, 40], splits=(0, 1, 3))
+
+
+def test_window_cuts_tiles():
+    """A window of 100 keys (not a multiple of the 64-key tile) on the same
+    shapes: every block starts and ends mid-tile."""
+    check(_case(202, [300, 517], 32, 16, 64), [300, 40], window=100, splits=(0, 1, 2))
+
+
+def test_group_of_eight_large_pages():
+    """8 q / 1 KV head (G = 8), pages of 256: a chunk of 100 tokens at 700
+    keys (800 columns: six full blocks and one of 32)."""
+    check(_case(203, [700], 8, 1, 256), [100], splits=(0, 1, 2))
+
+
+def test_group_of_one_small_pages():
+    """4 q / 4 KV heads (G = 1), pages of 16 (16-row copies): a chunk of 130
+    tokens at 250 keys (two blocks, the second of 2 columns)."""
+    check(_case(204, [250, 31], 4, 4, 16), [130, 31], splits=(0, 1, 4))
+
+
+def test_group_of_four_pages_of_32_with_empty_and_single_chunks():
+    """8 q / 2 KV heads (G = 4), pages of 32: chunks of 1, 0 and 77 tokens."""
+    check(_case(205, [5, 64, 200], 8, 2, 32), [1, 0, 77], window=50, splits=(0, 1, 3))
+
+
+def test_more_partitions_than_tiles():
+    """Sixteen partitions over rows of at most five tiles: most CTAs see no
+    key and write empty states the merge must skip."""
+    check(_case(206, [300, 90], 32, 16, 64), [20, 90], splits=(16,))
+
+
+def test_long_context_chunk_with_window_and_short_rows():
+    """A chunk of 256 tokens at 4,000 keys with a window of 1,024 beside two
+    short whole prompts (the sliding family's prefill)."""
+    check(_case(207, [4000, 130, 65], 32, 16, 64), [256, 130, 65], window=1024, splits=(0, 1))
+
+
+def test_one_token_chunk_matches_windowed_decode():
+    """A one-token chunk with a window is the windowed decode with
+    window_lo = own - W + 1 (the prefill of head dim 256 runs on its own
+    kernel, so the two agree to the fp32 bar, not bit for bit)."""
+    case = _case(208, [1088, 700], 32, 16, 64)
+    dc = DevCase(case)
+    wnd = 1024
+    q = to_dev(case.q, "bf16")
+    own = case.seq_lens - 1
+    fp, wl = i32([0, 0]), i32(np.maximum(0, own - wnd + 1))
+    ref = oracle.decode_direct(case.q, case.k_pool, case.v_pool, case.page_tables,
+                               case.seq_lens, case.scale, np.zeros(2, np.int32),
+                               np.maximum(0, own - wnd + 1).astype(np.int32))
+    for p in (1, 6):
+        a = run(dc, q, _cu([1, 1]), window=wnd, splits=p)
+        b = pskv.decode_attn_windowed(dc.layout, q, dc.tables, dc.lens, case.seq_lens, fp, wl,
+                                      case.scale, num_splits=p, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert max_err(a, ref) <= TOL and max_err(b, ref) <= TOL
+        assert float((a - b).abs().max()) <= TOL
+    assert dc.faults() == 0
+
+
+def test_page_outside_the_pool_is_skipped_and_flagged():
+    """A table entry past the pool: its keys are skipped (no copy is issued),
+    PSKV_FAULT_BAD_PAGE is raised, and the outputs stay finite."""
+    case = _case(209, [400], 32, 16, 64)
+    dc = DevCase(case)
+    tables = case.page_tables.copy()
+    tables[0, 2] = case.page_tables.max() + 1000
+    q = to_dev(_q(case, [200]), "bf16")
+    for p in (1, 3):
+        out = run(dc, q, _cu([200]), splits=p, tables=i32(tables))
+        torch.cuda.synchronize()
+        assert np.all(np.isfinite(out.cpu().numpy()))
+    assert dc.faults() & pskv.PSKV_FAULT_BAD_PAGE
+
+
+def test_bench_sliding_prompt_sampled_tokens():
+    """The bench's sliding prompt at full size (4,096 tokens, 32 q / 16 KV
+    heads, pages of 64, a window of 1,024 keys) in the automatic plan, checked
+    on sampled tokens: each equals the oracle's windowed decode of its row cut
+    at its own key."""
+    n = 4096
+    case = _case(210, [n], 32, 16, 64, keep_dense=False)
+    dc = DevCase(case)
+    qn = _q(case, [n], seed=3)
+    q = to_dev(qn, "bf16")
+    out = run(dc, q, _cu([n]), window=1024, splits=0)
+    torch.cuda.synchronize()
+    assert dc.faults() == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for t in (0, 1, 63, 64, 127, 1000, 1023, 1024, 2047, 3000, 4094, 4095):
+        lens = np.array([t + 1], np.int32)
+        ref = oracle.decode_direct(qn[t:t + 1], case.k_pool, case.v_pool, case.page_tables, lens,
+                                   case.scale, np.zeros(1, np.int32),
+                                   np.array([max(0, t - 1023)], np.int32))
+        err = float(np.abs(got[t:t + 1].astype(np.float64) - ref).max())
+        assert err <= TOL, f"token {t}: max |err| {err:.3e}"
