@@ -6,23 +6,24 @@
 // at head dim 256, bf16 pools in the split format.  One CTA takes a block of
 // 128 query rows of one (row, KV head): row i of the block is query column
 // qb * 128 + i of the row's chunk (token column / G, head column % G), and a
-// partition of the keys those tokens can see.  Per tile of 64 keys:
-//   S  = Q K^T    M = 128 rows, N = 64 keys, K = 256 (16 MMAs; S in tensor memory)
-//   softmax       one thread per query row reads its 64 scores from tensor
-//                 memory, masks them (causal, window, keys outside the
-//                 CTA's range), keeps the row's reference max and sum (exp2
-//                 units; the max moves only past a slack of 8, as in the
-//                 decode kernels) and writes P as a bf16 hi + lo pair into
-//                 shared memory
-//   O += P V      M = 128, N = 256, K = 64 keys, hi then lo (8 MMAs; O in tensor memory)
-// Q (64 KB) and the K and V tiles (two stages each) arrive by tensor copies in
-// the 128-byte swizzled layout the MMA descriptors read.  Warp 0 issues the
-// MMAs, warp 1 the copies; warps 2-5 run the softmax and the epilogue (warp w
-// owns tensor-memory lanes 32 (w % 4) .. + 31).  The two issuing warps are the
-// oldest of their schedulers, so the softmax's long instruction streams do not
-// hold them back.  Every wait is bounded; on expiry the CTA flags
-// PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its tensor
-// memory.
+// partition of the keys those tokens can see.  Per tile j of 64 keys:
+//   S  = Q K^T    M = 128 rows, N = 64 keys, K = 256 (16 MMAs)
+//   softmax       one thread per query row reads its 64 scores, masks them
+//                 (causal, window, keys outside the CTA's range), keeps the
+//                 row's reference max and sum (exp2 units; the max moves only
+//                 past a slack of 8, as in the decode kernels) and writes P
+//                 as a bf16 hi + lo pair over the scores it read
+//   O += P V      M = 128, N = 256, K = 64 keys, hi then lo (8 MMAs)
+// Tensor memory (512 columns): Q (bf16 pairs) at [0, 128), two score / P
+// regions at [128, 192) and [192, 256) (tile j uses region j % 2), O (f32) at
+// [256, 512).  Q and P feed the MMAs from tensor memory; K and V tiles arrive
+// by tensor copies in the 128-byte swizzled layout, three stages each.  Warp 0
+// issues the MMAs, warp 1 the copies; warps 2-5 stage Q and run the softmax
+// and the epilogue (warp w owns tensor-memory lanes 32 (w % 4) .. + 31).  The
+// two issuing warps are the oldest of their schedulers, so the softmax's long
+// instruction streams do not hold them back.  Every wait is bounded; on
+// expiry the CTA flags PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and
+// frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -37,30 +38,40 @@ namespace {
 constexpr int kD = 256;                     // head dim served
 constexpr int kRows = 128;                  // query rows per CTA (MMA M)
 constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of PV)
-constexpr int kQSlab = kRows * 128;         // bytes of one 64-column slab of Q
 constexpr int kKVSlab = kKeys * 128;        // bytes of one 64-column slab of a K or V tile
-constexpr int kQBytes = 4 * kQSlab;         // 64 KB
 constexpr int kKVBytes = 4 * kKVSlab;       // 32 KB
-constexpr int kPBytes = kRows * kKeys * 2;  // 16 KB per P buffer (hi, lo)
+constexpr int kStages = 3;
 constexpr int kThreads = 192;               // MMA warp, copy warp, 4 softmax warps
-constexpr int kTmemCols = 512;              // S at columns [0, 64), O at [64, 320)
-constexpr int kOCol = 64;
+constexpr int kTmemCols = 512;
+constexpr int kQCol = 0;                    // Q: 256 bf16 = 128 columns
+constexpr int kSCol = 128;                  // score / P region r at kSCol + 64 r
+constexpr int kOCol = 256;                  // O: 256 f32 columns
 constexpr float kSlack = 8.f;               // reference-max slack (log2 units)
 
 // shared memory (offsets from a 1,024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;       // K stage s at kOffK + s * kKVBytes
-constexpr int kOffV = kOffK + 2 * kKVBytes;  // V stage s at kOffV + s * kKVBytes
-constexpr int kOffP = kOffV + 2 * kKVBytes;  // P hi, then P lo
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-// barriers: fullK[2], fullV[2], emptyK[2], emptyV[2], s_full, s_free, p_full, pv_done, drain,
-// q_full, info_free[2]
-constexpr int kNumBars = 16;
-constexpr int kOffInfo = kOffBar + kNumBars * 8;  // StageInfo[2]
-constexpr int kOffSlot = kOffInfo + 2 * 16;       // tensor-memory address
+constexpr int kOffK = 0;                          // K stage s at kOffK + s * kKVBytes
+constexpr int kOffV = kOffK + kStages * kKVBytes;  // V stage s at kOffV + s * kKVBytes
+constexpr int kOffBar = kOffV + kStages * kKVBytes;
+
+// barrier slots
+enum : int {
+  kFullK = 0,                   // [3] K tile landed (copy bytes)
+  kFullV = kFullK + kStages,    // [3] V tile landed
+  kEmptyK = kFullV + kStages,   // [3] S of the stage's tile done (MMA commit)
+  kEmptyV = kEmptyK + kStages,  // [3] PV of the stage's tile done (MMA commit)
+  kInfoFree = kEmptyV + kStages,  // [3] the softmax warps read the stage's record
+  kSFull = kInfoFree + kStages,   // [2] S of region r done (MMA commit)
+  kPFull = kSFull + 2,            // [2] P of region r written (softmax warps)
+  kPvDone = kPFull + 2,           // [2] PV of region r's tile done (MMA commit)
+  kDrain = kPvDone + 2,           // every MMA done (MMA commit)
+  kQReady = kDrain + 1,           // Q written to tensor memory (softmax warps)
+  kNumBars = kQReady + 1
+};
+constexpr int kOffInfo = kOffBar + kNumBars * 8;   // StageInfo[3]
+constexpr int kOffSlot = kOffInfo + kStages * 16;  // tensor-memory address
 constexpr int kOffAbort = kOffSlot + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;      // + alignment of the dynamic base
+constexpr int kSmemBytes = kSmemUsed + 1024;       // + alignment of the dynamic base
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kIdescS = tc::instr_desc(kRows, kKeys, false, false);
@@ -76,8 +87,8 @@ struct StageInfo {
   int pad;
 };
 
-}  // namespace
 
+}  // namespace
 
 namespace {
 
@@ -135,6 +146,7 @@ __device__ __forceinline__ TcPlan make_plan(const TcArgs &a) {
   return pl;
 }
 
+
 // Bounded wait that gives up at once when another thread of the CTA already has.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                         int32_t *status) {
@@ -145,6 +157,13 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
   return false;
 }
 
+// The same wait taken by a whole warp: one verdict for all lanes.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+  const bool ok = tc_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
   asm volatile(
@@ -153,7 +172,15 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// Page ids of 32 consecutive table slots held across the control warp's lanes.
+// 2^x by the special-function unit (inputs of -inf give 0; results below the
+// smallest normal flush to 0, far below what a weight can contribute).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Page ids of 32 consecutive table slots held across the copy warp's lanes.
 struct PageCache {
   int base = -1, val = -1;
   __device__ int get(const int32_t *tbl, int slot, int n_slots, int lane) {
@@ -165,28 +192,17 @@ struct PageCache {
   }
 };
 
-// Barrier slots.
-enum : int {
-  kFullK = 0, kFullV = 2, kEmptyK = 4, kEmptyV = 6,
-  kSFull = 8, kSFree = 9, kPFull = 10, kPvDone = 11, kDrain = 12, kQFull = 13, kInfoFree = 14
-};
-
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
-  const bool ok = tc_wait(bar, parity, abort_flag, status);
-  return __all_sync(0xffffffffu, ok);
-}
 
 // The copy warp (all lanes converged; one elected lane issues).  Tile j's K
-// and V go to stage j % 2:
-//   K(j) once S(j - 2) has released the stage and the softmax warps have
-//        read the stage's record of tile j - 2;
-//   V(j) once PV(j - 2) has released the stage.
-// Q (four 64-column slabs of the 128-row block) is requested first.
+// and V go to stage j % 3:
+//   K(j) once S(j - 3) has released the stage and the softmax warps have read
+//        the stage's record of tile j - 3;
+//   V(j) once PV(j - 3) has released the stage.
+// The first three tiles are requested before the CTA's first barrier.
 struct Loader {
   const TcArgs &a;
   const TcPlan &pl;
-  const CUtensorMap *qmap, *kmap, *vmap;
+  const CUtensorMap *kmap, *vmap;
   unsigned char *sm;
   uint64_t *bars;
   StageInfo *info;
@@ -196,11 +212,10 @@ struct Loader {
   PageCache kpages, vpages;
   int k_issued = 0, v_issued = 0;
 
-  __device__ Loader(const TcArgs &a_, const TcPlan &pl_, const CUtensorMap *qm,
-                    const CUtensorMap *km, const CUtensorMap *vm, unsigned char *sm_,
-                    uint64_t *bars_, StageInfo *info_, volatile int *ab)
-      : a(a_), pl(pl_), qmap(qm), kmap(km), vmap(vm), sm(sm_), bars(bars_), info(info_),
-        abort_flag(ab) {
+  __device__ Loader(const TcArgs &a_, const TcPlan &pl_, const CUtensorMap *km,
+                    const CUtensorMap *vm, unsigned char *sm_, uint64_t *bars_, StageInfo *info_,
+                    volatile int *ab)
+      : a(a_), pl(pl_), kmap(km), vmap(vm), sm(sm_), bars(bars_), info(info_), abort_flag(ab) {
     lane = threadIdx.x & 31;
     n_slots = (pl.k_hi + a.page_size - 1) / a.page_size;
   }
@@ -211,6 +226,7 @@ struct Loader {
   // (bit c of the bad mask per 16 rows).  The K copy writes the stage's record
   // before the barrier is armed (the arrive releases it).
   __device__ void load(int j, bool is_v) {
+    const int st = j % kStages;
     const int key0 = (pl.t_begin + j) * kKeys;
     const int vlo = max(0, pl.k_lo - key0), vhi = min(kKeys, pl.k_hi - key0);
     const int32_t *tbl = a.page_tables + (size_t)pl.b * a.table_stride;
@@ -231,14 +247,14 @@ struct Loader {
       pages[c] = page;
       bytes += (uint32_t)(br * 128 * 4);
     }
-    unsigned char *dst = sm + (is_v ? kOffV : kOffK) + (j & 1) * kKVBytes;
-    uint64_t *bar = bars + (is_v ? kFullV : kFullK) + (j & 1);
+    unsigned char *dst = sm + (is_v ? kOffV : kOffK) + st * kKVBytes;
+    uint64_t *bar = bars + (is_v ? kFullV : kFullK) + st;
     if (elect_one()) {
       if (bad) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
       if (!is_v) {
-        info[j & 1].vlo = vlo;
-        info[j & 1].vhi = vhi;
-        info[j & 1].bad = bad;
+        info[st].vlo = vlo;
+        info[st].vhi = vhi;
+        info[st].bad = bad;
       }
       mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
@@ -255,60 +271,43 @@ struct Loader {
     (is_v ? v_issued : k_issued) = j + 1;
   }
 
-  // Q block: box (64 columns, the G heads, 128 / G tokens) from the chunk's
-  // first token of the block; rows past the packed query rows read zeros.
-  __device__ void load_q() {
-    if (elect_one()) {
-      uint64_t *bar = bars + kQFull;
-      mbar_arrive_expect_tx(bar, (uint32_t)kQBytes);
-      const int t0 = pl.r0 + ((pl.qb * kRows) >> a.group_shift);
-      const int h0 = pl.g << a.group_shift;
-#pragma unroll
-      for (int sl = 0; sl < 4; ++sl) tc::tma_load_3d(sm + kOffQ + sl * kQSlab, qmap, sl * 64, h0, t0, bar);
-    }
-    __syncwarp();
-  }
-
   __device__ bool wait(int slot, uint32_t parity) {
     return warp_wait(bars + slot, parity, abort_flag, a.status);
   }
 
   __device__ void prologue() {
-    load_q();
-    load(0, false);
-    load(0, true);
-    if (pl.n > 1) {
-      load(1, false);
-      load(1, true);
+    for (int j = 0; j < kStages && j < pl.n; ++j) {
+      load(j, false);
+      load(j, true);
     }
   }
 
   __device__ bool run() {
-    for (int j = 2; j < pl.n; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = ((j - 2) >> 1) & 1;  // completion (j - 2) / 2 of the stage's barriers
-      if (!wait(kEmptyK + s, ph) || !wait(kInfoFree + s, ph)) return false;
+    for (int j = kStages; j < pl.n; ++j) {
+      const int st = j % kStages;
+      const uint32_t ph = ((j - kStages) / kStages) & 1;  // the stage's previous use
+      if (!wait(kEmptyK + st, ph) || !wait(kInfoFree + st, ph)) return false;
       load(j, false);
-      if (!wait(kEmptyV + s, ph)) return false;
+      if (!wait(kEmptyV + st, ph)) return false;
       load(j, true);
     }
     return true;
   }
 
-  // Wait (bounded) for the last copy issued into each stage (and Q).
+  // Wait (bounded) for the last copy issued into each stage.
   __device__ void drain() {
-    mbar_wait(bars + kQFull, 0);
-    for (int s = 0; s < 2; ++s) {
-      const int jk = k_issued - 1 - ((k_issued - 1 - s) & 1);  // last K tile of stage s
-      if (jk >= 0) mbar_wait(bars + kFullK + s, (jk >> 1) & 1);
-      const int jv = v_issued - 1 - ((v_issued - 1 - s) & 1);
-      if (jv >= 0) mbar_wait(bars + kFullV + s, (jv >> 1) & 1);
+    for (int st = 0; st < kStages; ++st) {
+      for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
+        if (j % kStages == st) mbar_wait(bars + kFullK + st, (j / kStages) & 1);
+      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
+        if (j % kStages == st) mbar_wait(bars + kFullV + st, (j / kStages) & 1);
     }
   }
 };
 
 // The MMA warp (all lanes converged; one elected lane issues).  Per tile j:
-//   S(j) = Q K(j)^T once K(j) has landed and the softmax has read S(j - 1);
+//   S(j) = Q K(j)^T into region j % 2 once K(j) has landed and PV(j - 2) has
+//        consumed the P that region held;
 //   O += P(j - 1) V(j - 1) once P(j - 1) is written and V(j - 1) has landed.
 struct Issuer {
   const TcArgs &a;
@@ -322,45 +321,44 @@ struct Issuer {
   }
 
   __device__ bool run(uint32_t tmem) {
-    const uint32_t q_addr = smem_u32(sm + kOffQ);
-    const uint32_t p_addr = smem_u32(sm + kOffP);
-    // descriptors at the operands' first k-step; a k-step adds its byte offset / 16
-    const uint64_t dq = tc::smem_desc(q_addr, 16, 1024);
-    const uint64_t dp = tc::smem_desc(p_addr, 16, 1024);
     const int n = pl.n;
-    if (!wait(kQFull, 0)) return false;
+    if (!wait(kQReady, 0)) return false;
     for (int j = 0; j <= n; ++j) {
       if (j < n) {
-        const int s = j & 1;
-        if (!wait(kFullK + s, (j >> 1) & 1)) return false;
-        if (j >= 1 && !wait(kSFree, (j - 1) & 1)) return false;
+        const int st = j % kStages, r = j & 1;
+        if (!wait(kFullK + st, (j / kStages) & 1)) return false;
+        if (j >= 2 && !wait(kPvDone + r, ((j - 2) >> 1) & 1)) return false;
         tc::fence_after_sync();
-        const uint64_t dk = tc::smem_desc(smem_u32(sm + kOffK + s * kKVBytes), 16, 1024);
+        const uint64_t dk = tc::smem_desc(smem_u32(sm + kOffK + st * kKVBytes), 16, 1024);
         if (elect_one()) {
+          // A = Q from tensor memory (8 columns per 16 elements), B = K (K-major)
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            tc::mma(tmem, dq + (uint64_t)(((kk >> 2) * kQSlab + (kk & 3) * 32) >> 4),
-                    dk + (uint64_t)(((kk >> 2) * kKVSlab + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
-          tc::commit(bars + kSFull);
-          tc::commit(bars + kEmptyK + s);
+            tc::mma_ts(tmem + kSCol + 64 * r, tmem + kQCol + 8 * kk,
+                       dk + (uint64_t)(((kk >> 2) * kKVSlab + (kk & 3) * 32) >> 4), kIdescS,
+                       kk > 0);
+          tc::commit(bars + kSFull + r);
+          tc::commit(bars + kEmptyK + st);
         }
         __syncwarp();
       }
       if (j >= 1) {
-        const int jp = j - 1, sp = jp & 1;
-        if (!wait(kPFull, jp & 1)) return false;
-        if (!wait(kFullV + sp, (jp >> 1) & 1)) return false;
+        const int jp = j - 1, st = jp % kStages, r = jp & 1;
+        if (!wait(kPFull + r, (jp >> 1) & 1)) return false;
+        if (!wait(kFullV + st, (jp / kStages) & 1)) return false;
         tc::fence_after_sync();
-        const uint64_t dv = tc::smem_desc(smem_u32(sm + kOffV + sp * kKVBytes), 8192, 1024);
+        const uint64_t dv = tc::smem_desc(smem_u32(sm + kOffV + st * kKVBytes), 8192, 1024);
         if (elect_one()) {
+          // A = P hi (columns 0-31 of the region), then P lo (32-63); B = V (MN-major)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
-              tc::mma(tmem + kOCol, dp + (uint64_t)((part * kPBytes + kk * 32) >> 4),
-                      dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, jp > 0 || part > 0 || kk > 0);
-          tc::commit(bars + kPvDone);
-          tc::commit(bars + kEmptyV + sp);
+              tc::mma_ts(tmem + kOCol, tmem + kSCol + 64 * r + 32 * part + 8 * kk,
+                         dv + (uint64_t)((kk * 2048) >> 4), kIdescPV,
+                         jp > 0 || part > 0 || kk > 0);
+          tc::commit(bars + kPvDone + r);
+          tc::commit(bars + kEmptyV + st);
         }
         __syncwarp();
       }
@@ -377,13 +375,47 @@ struct Issuer {
   }
 };
 
-// One softmax thread per query row (thread i = tensor-memory lane i).
+// One softmax thread per query row (thread = tensor-memory lane).
 struct RowState {
   float m;  // reference max (log2 units), -inf until a key is seen
   float l;  // sum of exp2(score - m)
 };
 
-// Multiply this warp's 128 x 256 O rows in tensor memory by alpha (1 keeps a row).
+// Query row of block row i (output / partial row index without the partition).
+__device__ __forceinline__ size_t query_row(const TcArgs &a, const TcPlan &pl, int i, bool *real) {
+  const int col = pl.qb * kRows + i, t = col >> a.group_shift;
+  *real = t < pl.T;
+  const int h = (pl.g << a.group_shift) + (col & ((1 << a.group_shift) - 1));
+  return ((size_t)pl.r0 + (*real ? t : 0)) * a.num_q_heads + h;
+}
+
+// Q into tensor memory: this thread's row (zeros past the chunk), 256 bf16 as
+// 128 columns of pairs.  All 32 loads are in flight before the first store.
+__device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint32_t tmem) {
+  const int w = (threadIdx.x >> 5) & 3, i = 32 * w + (threadIdx.x & 31);
+  bool real;
+  const size_t qrow = query_row(a, pl, i, &real);
+  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qrow * kD);
+  uint4 q[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) q[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+  const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t v[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      v[4 * c] = q[8 * b + c].x;
+      v[4 * c + 1] = q[8 * b + c].y;
+      v[4 * c + 2] = q[8 * b + c].z;
+      v[4 * c + 3] = q[8 * b + c].w;
+    }
+    tc::st32(lane_base + kQCol + 32 * b, v);
+  }
+  tc::wait_st();
+}
+
+// Multiply this warp's rows of O in tensor memory by alpha (1 keeps a row).
 __device__ __forceinline__ void rescale_o(uint32_t lane_base, float alpha) {
 #pragma unroll 1
   for (int c = 0; c < kD / 32; ++c) {
@@ -402,8 +434,6 @@ __device__ __forceinline__ void rescale_o(uint32_t lane_base, float alpha) {
 __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, unsigned char *sm,
                                              uint64_t *bars, const StageInfo *info, uint32_t tmem,
                                              volatile int *abort_flag, RowState &st) {
-  uint64_t *fullK = bars, *fullV = bars + 2;
-  uint64_t *s_full = bars + 8, *s_free = bars + 9, *p_full = bars + 10, *pv_done = bars + 11;
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, i = 32 * w + lane;
   const int col = pl.qb * kRows + i, t = col >> a.group_shift;
   const bool real = t < pl.T;
@@ -411,29 +441,25 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
   const int lim = real ? own + 1 : 0;  // keys below lim, from lo on, are visible
   const int lo = a.window > 0 ? max(0, own - a.window + 1) : 0;
   const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
-  unsigned char *p_hi = sm + kOffP + i * 128, *p_lo = p_hi + kPBytes;
   const float sc = a.scale_log2;
-  auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-    const bool ok = tc_wait(bar, parity, abort_flag, a.status);
-    return __all_sync(0xffffffffu, ok);
+  auto wait_all = [&](int slot, uint32_t parity) {
+    return warp_wait(bars + slot, parity, abort_flag, a.status);
   };
   for (int j = 0; j < pl.n; ++j) {
-    const int s = j & 1, key0 = (pl.t_begin + j) * kKeys;
-    if (!wait_all(s_full, j & 1)) return false;
-    if (!wait_all(&fullK[s], (j >> 1) & 1)) return false;  // complete: publishes the record
-    const StageInfo inf = info[s];
+    const int stg = j % kStages, r = j & 1, key0 = (pl.t_begin + j) * kKeys;
+    const uint32_t region = lane_base + kSCol + 64 * r;
+    if (!wait_all(kSFull + r, (j >> 1) & 1)) return false;
+    if (!wait_all(kFullK + stg, (j / kStages) & 1)) return false;  // publishes the record
+    const StageInfo inf = info[stg];
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + kInfoFree + s);  // the record may be rewritten
+    if (lane == 0) mbar_arrive(bars + kInfoFree + stg);  // the record may be rewritten
     tc::fence_after_sync();
     uint32_t va[32], vb[32];
-    tc::ld32(lane_base, va);
-    tc::ld32(lane_base + 32, vb);
+    tc::ld32(region, va);
+    tc::ld32(region + 32, vb);
     tc::wait_ld();
     tc::reg_fence(va);
     tc::reg_fence(vb);
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(s_free);
 
     // ---- mask (by selection: scores of keys never loaded may be anything) and tile max
     float x[kKeys];
@@ -461,64 +487,57 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     bool rescale = false;
     if (mt > st.m + kSlack) {
       rescale = st.m != -CUDART_INF_F;  // with m = -inf the row's O and l are still 0
-      alpha = rescale ? exp2f(st.m - mt) : 1.f;
+      alpha = rescale ? ex2(st.m - mt) : 1.f;
       st.l *= alpha;
       st.m = mt;
     }
-    // ---- P = exp2(x - m) as hi + lo bf16 pairs, built in registers while PV(j - 1) runs
+
+    // ---- P = exp2(x - m) as hi + lo bf16 pairs
     const float u = st.m == -CUDART_INF_F ? 0.f : st.m;
     uint32_t h[kKeys / 2], lw[kKeys / 2];
     float sum = 0.f;
 #pragma unroll
     for (int e = 0; e < kKeys / 2; ++e) {
-      const float p0 = exp2f(x[2 * e] - u), p1 = exp2f(x[2 * e + 1] - u);
+      const float p0 = ex2(x[2 * e] - u), p1 = ex2(x[2 * e + 1] - u);
       sum += p0 + p1;
       h[e] = pack_bf16x2(p0, p1);
       lw[e] = pack_bf16x2(p0 - bf16_lo(h[e]), p1 - bf16_hi(h[e]));
     }
     st.l += sum;
 
-    // ---- V rows outside the CTA's keys or in skipped chunks: zero (they meet P = 0)
+    // ---- V rows outside the CTA's keys or in skipped chunks: zero (they meet P = 0).
+    // Every tile's V barrier is waited, in order, so that each wait's parity
+    // names the phase it means.
+    if (!wait_all(kFullV + stg, (j / kStages) & 1)) return false;
     if (inf.vlo > 0 || inf.vhi < kKeys || inf.bad != 0) {
-      if (!wait_all(&fullV[s], (j >> 1) & 1)) return false;
-      const int r = i >> 1;
-      if (r < inf.vlo || r >= inf.vhi || ((inf.bad >> (r >> 4)) & 1u)) {
-        unsigned char *vrow = sm + kOffV + s * kKVBytes + r * 128 + (i & 1) * 2 * kKVSlab;
+      const int rr = i >> 1;
+      if (rr < inf.vlo || rr >= inf.vhi || ((inf.bad >> (rr >> 4)) & 1u)) {
+        unsigned char *vrow = sm + kOffV + stg * kKVBytes + rr * 128 + (i & 1) * 2 * kKVSlab;
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             *reinterpret_cast<uint4 *>(vrow + sl * kKVSlab + q * 16) = make_uint4(0, 0, 0, 0);
       }
+      tc::fence_smem_for_async();
     }
 
-    // PV(j - 1) must be done before O is rescaled and before P is rewritten
-    if (j >= 1 && !wait_all(pv_done, (j - 1) & 1)) return false;
-    tc::fence_after_sync();
-    if (__any_sync(0xffffffffu, rescale)) rescale_o(lane_base, alpha);
-    // rows in the 128-byte swizzled layout: 16-byte chunk cc of row i at cc ^ (i % 8)
-#pragma unroll
-    for (int cc = 0; cc < kKeys / 8; ++cc) {
-      const int off = ((cc ^ (i & 7)) * 16);
-      *reinterpret_cast<uint4 *>(p_hi + off) =
-          make_uint4(h[4 * cc], h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
-      *reinterpret_cast<uint4 *>(p_lo + off) =
-          make_uint4(lw[4 * cc], lw[4 * cc + 1], lw[4 * cc + 2], lw[4 * cc + 3]);
+    // ---- O of the rows whose reference moved: rescaled once PV(j - 1) is done
+    if (__any_sync(0xffffffffu, rescale)) {
+      // PV(j - 3) is known done (S(j - 1) waited for it), so this parity is unambiguous
+      if (!wait_all(kPvDone + ((j - 1) & 1), ((j - 1) >> 1) & 1)) return false;
+      tc::fence_after_sync();
+      rescale_o(lane_base, alpha);
     }
-    tc::fence_smem_for_async();
+    // P over the scores it came from: hi at columns 0-31 of the region, lo at 32-63
+    tc::st32(region, h);
+    tc::st32(region + 32, lw);
+    tc::wait_st();
     tc::fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(p_full);
+    if (lane == 0) mbar_arrive(bars + kPFull + r);
   }
   return true;
-}
-
-// Query row of block row i (output / partial row index without the partition).
-__device__ __forceinline__ size_t query_row(const TcArgs &a, const TcPlan &pl, int i, bool *real) {
-  const int col = pl.qb * kRows + i, t = col >> a.group_shift;
-  *real = t < pl.T;
-  const int h = (pl.g << a.group_shift) + (col & ((1 << a.group_shift) - 1));
-  return ((size_t)pl.r0 + (*real ? t : 0)) * a.num_q_heads + h;
 }
 
 // Write row i's result: o / l to `out` (direct) or the partial (m, l, o).
@@ -602,8 +621,7 @@ __device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl) {
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
-    pskv_attn_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap qmap,
-                        const __grid_constant__ CUtensorMap kmap,
+    pskv_attn_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -626,19 +644,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  Loader ld(a, pl, &qmap, &kmap, &vmap, sm, bars, info, abort_flag);
+  Loader ld(a, pl, &kmap, &vmap, sm, bars, info, abort_flag);
   if (warp == 1) {
-    // the copy warp sets up the barriers and requests Q and the first tiles at once
+    // the copy warp sets up the barriers and requests the first tiles at once
     if (lane == 0) {
-      for (int k = 0; k < 8; ++k) mbar_init(&bars[k], 1);  // fullK, fullV, emptyK, emptyV
-      mbar_init(&bars[kSFull], 1);   // MMA commit
-      mbar_init(&bars[kSFree], 4);   // one arrive per softmax warp
-      mbar_init(&bars[kPFull], 4);   // one arrive per softmax warp
-      mbar_init(&bars[kPvDone], 1);  // MMA commit
-      mbar_init(&bars[kDrain], 1);   // MMA commit
-      mbar_init(&bars[kQFull], 1);
-      mbar_init(&bars[kInfoFree], 4);      // one arrive per softmax warp
-      mbar_init(&bars[kInfoFree + 1], 4);
+      for (int k = 0; k < 4 * kStages; ++k) mbar_init(&bars[k], 1);  // full / empty K, V
+      for (int k = 0; k < kStages; ++k) mbar_init(&bars[kInfoFree + k], 4);  // per softmax warp
+      for (int r = 0; r < 2; ++r) {
+        mbar_init(&bars[kSFull + r], 1);  // MMA commit
+        mbar_init(&bars[kPFull + r], 4);  // per softmax warp
+      }
+      mbar_init(&bars[kPvDone], 1);  // MMA commits
+      mbar_init(&bars[kPvDone + 1], 1);
+      mbar_init(&bars[kDrain], 1);
+      mbar_init(&bars[kQReady], 4);
       *abort_flag = 0;
       mbar_fence_init();
     }
@@ -660,11 +679,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ld.run();
     ld.drain();  // every copy landed before the CTA leaves
   } else {
+    stage_q(a, pl, tmem);
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kQReady);
     RowState st;
     st.m = -CUDART_INF_F;
     st.l = 0.f;
     if (softmax_loop(a, pl, sm, bars, info, tmem, abort_flag, st)) {
-      const bool ok = tc_wait(bars + kPvDone, (pl.n - 1) & 1, abort_flag, a.status);
+      // PV(n - 1); PV(n - 3) is known done, as S(n - 1) waited for it
+      const bool ok =
+          tc_wait(bars + kPvDone + ((pl.n - 1) & 1), ((pl.n - 1) >> 1) & 1, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc::fence_after_sync();
         write_rows(a, pl, tmem, st);
@@ -678,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::dealloc(tmem, kTmemCols);
   }
 }
+
 
 namespace {
 
@@ -708,20 +734,6 @@ bool make_map(CUtensorMap *m, const void *region, long long rows, int box_rows) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The packed queries [rows][Hq][256] as a 3-D tensor (columns, heads, rows),
-// read in boxes of 64 columns x G heads x 128 / G rows.
-bool make_qmap(CUtensorMap *m, const void *q, int rows, int heads, int group) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * heads};
-  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(kRows / group)};
-  const cuuint32_t elem[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
-             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, dim3 grid,
@@ -737,12 +749,11 @@ cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_po
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const long long rows = a.num_pages * a.num_kv_heads * a.page_size;
-  CUtensorMap qm, km, vm;
-  if (!make_qmap(&qm, a.q, a.total_rows, a.num_q_heads, 1 << a.group_shift) ||
-      !make_map(&km, k_pool, rows, a.box_rows) || !make_map(&vm, v_pool, rows, a.box_rows))
+  CUtensorMap km, vm;
+  if (!make_map(&km, k_pool, rows, a.box_rows) || !make_map(&vm, v_pool, rows, a.box_rows))
     return cudaErrorInvalidValue;
-  return launch_pdl(pskv_attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, stream, a, qm,
-                    km, vm);
+  return launch_pdl(pskv_attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, stream, a, km,
+                    vm);
 }
 
 }  // namespace pskv

@@ -49,6 +49,16 @@ __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t a, uint64_t b, uin
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
+// D[tmem] (+)= A[tmem] * B: A (M rows = lanes, bf16 pairs per 32-bit column,
+// the lower element in the low half) read from tensor memory.
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
+                                       uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
 __device__ __forceinline__ void commit(uint64_t *bar) {
   asm volatile(
