@@ -18,12 +18,14 @@
 // regions at [128, 192) and [192, 256) (tile j uses region j % 2), O (f32) at
 // [256, 512).  Q and P feed the MMAs from tensor memory; K and V tiles arrive
 // by tensor copies in the 128-byte swizzled layout, three stages each.  Warp 0
-// issues the MMAs, warp 1 the copies; warps 2-5 stage Q and run the softmax
-// and the epilogue (warp w owns tensor-memory lanes 32 (w % 4) .. + 31).  The
-// two issuing warps are the oldest of their schedulers, so the softmax's long
-// instruction streams do not hold them back.  Every wait is bounded; on
-// expiry the CTA flags PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and
-// frees its tensor memory.
+// issues the MMAs, warp 1 the K copies and warp 6 the V copies (so that a K
+// tile is requested three tiles ahead whatever the V side waits for); warps
+// 2-5 stage Q and run the softmax and the epilogue (warp w owns tensor-memory
+// lanes 32 (w % 4) .. + 31).  The issuing warps are the oldest of their
+// schedulers, so the softmax's long instruction streams do not hold them
+// back.  Every wait is bounded; on expiry the CTA flags
+// PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its tensor
+// memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -41,7 +43,7 @@ constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of P
 constexpr int kKVSlab = kKeys * 128;        // bytes of one 64-column slab of a K or V tile
 constexpr int kKVBytes = 4 * kKVSlab;       // 32 KB
 constexpr int kStages = 3;
-constexpr int kThreads = 192;               // MMA warp, copy warp, 4 softmax warps
+constexpr int kThreads = 224;               // MMA warp, K copy warp, 4 softmax warps, V copy warp
 constexpr int kTmemCols = 512;
 constexpr int kQCol = 0;                    // Q: 256 bf16 = 128 columns
 constexpr int kSCol = 128;                  // score / P region r at kSCol + 64 r
@@ -193,12 +195,12 @@ struct PageCache {
 };
 
 
-// The copy warp (all lanes converged; one elected lane issues).  Tile j's K
-// and V go to stage j % 3:
+// A copy warp (all lanes converged; one elected lane issues), for K or for V.
+// Tile j's K and V go to stage j % 3:
 //   K(j) once S(j - 3) has released the stage and the softmax warps have read
 //        the stage's record of tile j - 3;
 //   V(j) once PV(j - 3) has released the stage.
-// The first three tiles are requested before the CTA's first barrier.
+// The first three K tiles are requested before the CTA's first barrier.
 struct Loader {
   const TcArgs &a;
   const TcPlan &pl;
@@ -209,8 +211,8 @@ struct Loader {
   volatile int *abort_flag;
   int lane;
   int n_slots;  // table slots the CTA's keys use
-  PageCache kpages, vpages;
-  int k_issued = 0, v_issued = 0;
+  PageCache pages;  // each copy warp's own
+  int issued = 0;
 
   __device__ Loader(const TcArgs &a_, const TcPlan &pl_, const CUtensorMap *km,
                     const CUtensorMap *vm, unsigned char *sm_, uint64_t *bars_, StageInfo *info_,
@@ -231,20 +233,19 @@ struct Loader {
     const int vlo = max(0, pl.k_lo - key0), vhi = min(kKeys, pl.k_hi - key0);
     const int32_t *tbl = a.page_tables + (size_t)pl.b * a.table_stride;
     const int br = a.box_rows;
-    PageCache &pc = is_v ? vpages : kpages;
     uint32_t bad = 0, bytes = 0;
-    int pages[4];
+    int pg[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      pages[c] = -1;
+      pg[c] = -1;
       if (c * br >= kKeys) continue;
       if ((c + 1) * br <= vlo || c * br >= vhi) continue;  // no row of the chunk is in range
-      const int page = pc.get(tbl, (key0 + c * br) / a.page_size, n_slots, lane);
+      const int page = pages.get(tbl, (key0 + c * br) / a.page_size, n_slots, lane);
       if (page < 0 || (long long)page >= a.num_pages) {
         bad |= (br == kKeys ? 0xFu : 1u << c);
         continue;
       }
-      pages[c] = page;
+      pg[c] = page;
       bytes += (uint32_t)(br * 128 * 4);
     }
     unsigned char *dst = sm + (is_v ? kOffV : kOffK) + st * kKVBytes;
@@ -259,49 +260,44 @@ struct Loader {
       mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if (pages[c] < 0) continue;
+        if (pg[c] < 0) continue;
         const int key = key0 + c * br;
-        const int y = (pages[c] * a.num_kv_heads + pl.g) * a.page_size + key % a.page_size;
+        const int y = (pg[c] * a.num_kv_heads + pl.g) * a.page_size + key % a.page_size;
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl)
           tc::tma_load_2d(dst + sl * kKVSlab + c * br * 128, is_v ? vmap : kmap, sl * 64, y, bar);
       }
     }
     __syncwarp();
-    (is_v ? v_issued : k_issued) = j + 1;
+    issued = j + 1;
   }
 
   __device__ bool wait(int slot, uint32_t parity) {
     return warp_wait(bars + slot, parity, abort_flag, a.status);
   }
 
-  __device__ void prologue() {
-    for (int j = 0; j < kStages && j < pl.n; ++j) {
-      load(j, false);
-      load(j, true);
-    }
+  __device__ void prologue(bool is_v) {
+    for (int j = 0; j < kStages && j < pl.n; ++j) load(j, is_v);
   }
 
-  __device__ bool run() {
+  __device__ bool run(bool is_v) {
     for (int j = kStages; j < pl.n; ++j) {
       const int st = j % kStages;
       const uint32_t ph = ((j - kStages) / kStages) & 1;  // the stage's previous use
-      if (!wait(kEmptyK + st, ph) || !wait(kInfoFree + st, ph)) return false;
-      load(j, false);
-      if (!wait(kEmptyV + st, ph)) return false;
-      load(j, true);
+      if (is_v) {
+        if (!wait(kEmptyV + st, ph)) return false;
+      } else {
+        if (!wait(kEmptyK + st, ph) || !wait(kInfoFree + st, ph)) return false;
+      }
+      load(j, is_v);
     }
     return true;
   }
 
   // Wait (bounded) for the last copy issued into each stage.
-  __device__ void drain() {
-    for (int st = 0; st < kStages; ++st) {
-      for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
-        if (j % kStages == st) mbar_wait(bars + kFullK + st, (j / kStages) & 1);
-      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
-        if (j % kStages == st) mbar_wait(bars + kFullV + st, (j / kStages) & 1);
-    }
+  __device__ void drain(bool is_v) {
+    for (int j = max(0, issued - kStages); j < issued; ++j)
+      mbar_wait(bars + (is_v ? kFullV : kFullK) + j % kStages, (j / kStages) & 1);
   }
 };
 
@@ -662,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_fence_init();
     }
     __syncwarp();
-    ld.prologue();
+    ld.prologue(false);
   } else if (warp == 0) {
     tc::alloc(slot, kTmemCols);
   }
@@ -675,9 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Issuer is{a, pl, sm, bars, abort_flag};
     is.run(tmem);
     is.drain();  // every MMA done before the memory is released
-  } else if (warp == 1) {
-    ld.run();
-    ld.drain();  // every copy landed before the CTA leaves
+  } else if (warp == 1 || warp == 6) {
+    const bool is_v = warp == 6;
+    if (is_v) ld.prologue(true);
+    ld.run(is_v);
+    ld.drain(is_v);  // every copy landed before the CTA leaves
   } else {
     stage_q(a, pl, tmem);
     tc::fence_before_sync();
