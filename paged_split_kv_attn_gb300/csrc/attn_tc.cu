@@ -37,23 +37,23 @@ namespace pskv {
 
 namespace {
 
-constexpr int kD = 256;                     // head dim served
+constexpr int kD = 256;                     // head-dim columns per CTA
 constexpr int kRows = 128;                  // query rows per CTA (MMA M)
 constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of PV)
 constexpr int kKVSlab = kKeys * 128;        // bytes of one 64-column slab of a K or V tile
 constexpr int kKVBytes = 4 * kKVSlab;       // 32 KB
-constexpr int kStages = 3;
+constexpr int kStages = 3;                  // K stages
 constexpr int kThreads = 224;               // MMA warp, K copy warp, 4 softmax warps, V copy warp
+constexpr int kXBytes = kRows * kKeys * 4;  // one block of partial scores (32 KB)
 constexpr int kTmemCols = 512;
 constexpr int kQCol = 0;                    // Q: 256 bf16 = 128 columns
 constexpr int kSCol = 128;                  // score / P region r at kSCol + 64 r
 constexpr int kOCol = 256;                  // O: 256 f32 columns
 constexpr float kSlack = 8.f;               // reference-max slack (log2 units)
 
-// shared memory (offsets from a 1,024-byte aligned base)
-constexpr int kOffK = 0;                          // K stage s at kOffK + s * kKVBytes
-constexpr int kOffV = kOffK + kStages * kKVBytes;  // V stage s at kOffV + s * kKVBytes
-constexpr int kOffBar = kOffV + kStages * kKVBytes;
+// shared memory (offsets from a 1,024-byte aligned base): K stages, V stages,
+// (CTA pair) two blocks of the peer's partial scores, barriers, stage records
+constexpr int kOffK = 0;  // K stage s at kOffK + s * kKVBytes
 
 // barrier slots
 enum : int {
@@ -67,14 +67,27 @@ enum : int {
   kPvDone = kPFull + 2,           // [2] PV of region r's tile done (MMA commit)
   kDrain = kPvDone + 2,           // every MMA done (MMA commit)
   kQReady = kDrain + 1,           // Q written to tensor memory (softmax warps)
-  kNumBars = kQReady + 1
+  kXFull = kQReady + 1,           // [2] the peer's partial scores arrived (CTA pair)
+  kXFree = kXFull + 2,            // [2] the peer read the partial scores sent to it
+  kNumBars = kXFree + 2
 };
-constexpr int kOffInfo = kOffBar + kNumBars * 8;   // StageInfo[3]
-constexpr int kOffSlot = kOffInfo + kStages * 16;  // tensor-memory address
-constexpr int kOffAbort = kOffSlot + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;       // + alignment of the dynamic base
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// Head dim 256: one CTA.  Head dim 512: a cluster of two CTAs, rank c holding
+// columns [256 c, 256 c + 256) of Q, K, V and O (two V stages, to make room
+// for the exchanged partial scores).
+template <bool kPair>
+struct Lay {
+  static constexpr int kDT = kPair ? 2 * kD : kD;  // the pool's head dim
+  static constexpr int kStagesV = kPair ? 2 : 3;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;  // V stage s at kOffV + s * kKVBytes
+  static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // partial-score block b at + b * kXBytes
+  static constexpr int kOffBar = kOffX + (kPair ? 2 * kXBytes : 0);
+  static constexpr int kOffInfo = kOffBar + kNumBars * 8;   // StageInfo[3]
+  static constexpr int kOffSlot = kOffInfo + kStages * 16;  // tensor-memory address
+  static constexpr int kOffAbort = kOffSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment of the dynamic base
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 constexpr uint32_t kIdescS = tc::instr_desc(kRows, kKeys, false, false);
 constexpr uint32_t kIdescPV = tc::instr_desc(kRows, kD, false, true);
@@ -103,9 +116,8 @@ struct TcPlan {
   bool ok;           // the row's offsets and length are usable
 };
 
-__device__ __forceinline__ TcPlan make_plan(const TcArgs &a) {
+__device__ __forceinline__ TcPlan make_plan(const TcArgs &a, int x) {
   TcPlan pl;
-  const int x = blockIdx.x;
   // heavier (later) query blocks first: under causality they see more keys
   pl.qb = a.qblocks - 1 - x % a.qblocks;
   pl.p = x / a.qblocks;
@@ -195,13 +207,71 @@ struct PageCache {
 };
 
 
+// ---- the CTA pair: distributed shared memory and cluster-scope barriers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                           uint32_t w) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y),
+               "r"(z), "r"(w)
+               : "memory");
+}
+// Arrive on a barrier of another CTA, releasing this thread's writes at cluster scope.
+__device__ __forceinline__ void arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+      "%2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire, one verdict for the warp.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, int32_t *status) {
+  bool ok = !*abort_flag;
+  if (ok && !try_wait_cluster(bar, parity)) {
+    ok = false;
+    for (uint32_t i = 0; i < kWaitPolls; ++i)
+      if (try_wait_cluster(bar, parity)) {
+        ok = true;
+        break;
+      }
+    if (!ok) {
+      *abort_flag = 1;
+      raise_fault(status, PSKV_FAULT_WAIT_TIMEOUT);
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 // A copy warp (all lanes converged; one elected lane issues), for K or for V.
 // Tile j's K and V go to stage j % 3:
 //   K(j) once S(j - 3) has released the stage and the softmax warps have read
 //        the stage's record of tile j - 3;
 //   V(j) once PV(j - 3) has released the stage.
 // The first three K tiles are requested before the CTA's first barrier.
+template <bool kPair>
 struct Loader {
+  using L = Lay<kPair>;
   const TcArgs &a;
   const TcPlan &pl;
   const CUtensorMap *kmap, *vmap;
@@ -213,11 +283,13 @@ struct Loader {
   int n_slots;  // table slots the CTA's keys use
   PageCache pages;  // each copy warp's own
   int issued = 0;
+  int col0;         // first head-dim column this CTA holds
 
   __device__ Loader(const TcArgs &a_, const TcPlan &pl_, const CUtensorMap *km,
                     const CUtensorMap *vm, unsigned char *sm_, uint64_t *bars_, StageInfo *info_,
-                    volatile int *ab)
-      : a(a_), pl(pl_), kmap(km), vmap(vm), sm(sm_), bars(bars_), info(info_), abort_flag(ab) {
+                    volatile int *ab, int col0_)
+      : a(a_), pl(pl_), kmap(km), vmap(vm), sm(sm_), bars(bars_), info(info_), abort_flag(ab),
+        col0(col0_) {
     lane = threadIdx.x & 31;
     n_slots = (pl.k_hi + a.page_size - 1) / a.page_size;
   }
@@ -228,7 +300,7 @@ struct Loader {
   // (bit c of the bad mask per 16 rows).  The K copy writes the stage's record
   // before the barrier is armed (the arrive releases it).
   __device__ void load(int j, bool is_v) {
-    const int st = j % kStages;
+    const int st = j % (is_v ? L::kStagesV : kStages);
     const int key0 = (pl.t_begin + j) * kKeys;
     const int vlo = max(0, pl.k_lo - key0), vhi = min(kKeys, pl.k_hi - key0);
     const int32_t *tbl = a.page_tables + (size_t)pl.b * a.table_stride;
@@ -248,7 +320,7 @@ struct Loader {
       pg[c] = page;
       bytes += (uint32_t)(br * 128 * 4);
     }
-    unsigned char *dst = sm + (is_v ? kOffV : kOffK) + st * kKVBytes;
+    unsigned char *dst = sm + (is_v ? L::kOffV : kOffK) + st * kKVBytes;
     uint64_t *bar = bars + (is_v ? kFullV : kFullK) + st;
     if (elect_one()) {
       if (bad) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
@@ -265,7 +337,8 @@ struct Loader {
         const int y = (pg[c] * a.num_kv_heads + pl.g) * a.page_size + key % a.page_size;
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl)
-          tc::tma_load_2d(dst + sl * kKVSlab + c * br * 128, is_v ? vmap : kmap, sl * 64, y, bar);
+          tc::tma_load_2d(dst + sl * kKVSlab + c * br * 128, is_v ? vmap : kmap, col0 + sl * 64, y,
+                          bar);
       }
     }
     __syncwarp();
@@ -277,13 +350,14 @@ struct Loader {
   }
 
   __device__ void prologue(bool is_v) {
-    for (int j = 0; j < kStages && j < pl.n; ++j) load(j, is_v);
+    for (int j = 0; j < (is_v ? L::kStagesV : kStages) && j < pl.n; ++j) load(j, is_v);
   }
 
   __device__ bool run(bool is_v) {
-    for (int j = kStages; j < pl.n; ++j) {
-      const int st = j % kStages;
-      const uint32_t ph = ((j - kStages) / kStages) & 1;  // the stage's previous use
+    const int S = is_v ? L::kStagesV : kStages;
+    for (int j = S; j < pl.n; ++j) {
+      const int st = j % S;
+      const uint32_t ph = ((j - S) / S) & 1;  // the stage's previous use
       if (is_v) {
         if (!wait(kEmptyV + st, ph)) return false;
       } else {
@@ -296,8 +370,9 @@ struct Loader {
 
   // Wait (bounded) for the last copy issued into each stage.
   __device__ void drain(bool is_v) {
-    for (int j = max(0, issued - kStages); j < issued; ++j)
-      mbar_wait(bars + (is_v ? kFullV : kFullK) + j % kStages, (j / kStages) & 1);
+    const int S = is_v ? L::kStagesV : kStages;
+    for (int j = max(0, issued - S); j < issued; ++j)
+      mbar_wait(bars + (is_v ? kFullV : kFullK) + j % S, (j / S) & 1);
   }
 };
 
@@ -305,7 +380,9 @@ struct Loader {
 //   S(j) = Q K(j)^T into region j % 2 once K(j) has landed and PV(j - 2) has
 //        consumed the P that region held;
 //   O += P(j - 1) V(j - 1) once P(j - 1) is written and V(j - 1) has landed.
+template <bool kPair>
 struct Issuer {
+  using L = Lay<kPair>;
   const TcArgs &a;
   const TcPlan &pl;
   unsigned char *sm;
@@ -339,11 +416,11 @@ struct Issuer {
         __syncwarp();
       }
       if (j >= 1) {
-        const int jp = j - 1, st = jp % kStages, r = jp & 1;
+        const int jp = j - 1, st = jp % L::kStagesV, r = jp & 1;
         if (!wait(kPFull + r, (jp >> 1) & 1)) return false;
-        if (!wait(kFullV + st, (jp / kStages) & 1)) return false;
+        if (!wait(kFullV + st, (jp / L::kStagesV) & 1)) return false;
         tc::fence_after_sync();
-        const uint64_t dv = tc::smem_desc(smem_u32(sm + kOffV + st * kKVBytes), 8192, 1024);
+        const uint64_t dv = tc::smem_desc(smem_u32(sm + L::kOffV + st * kKVBytes), 8192, 1024);
         if (elect_one()) {
           // A = P hi (columns 0-31 of the region), then P lo (32-63); B = V (MN-major)
 #pragma unroll
@@ -387,11 +464,13 @@ __device__ __forceinline__ size_t query_row(const TcArgs &a, const TcPlan &pl, i
 
 // Q into tensor memory: this thread's row (zeros past the chunk), 256 bf16 as
 // 128 columns of pairs.  All 32 loads are in flight before the first store.
-__device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint32_t tmem) {
+template <bool kPair>
+__device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint32_t tmem, int col0) {
   const int w = (threadIdx.x >> 5) & 3, i = 32 * w + (threadIdx.x & 31);
   bool real;
   const size_t qrow = query_row(a, pl, i, &real);
-  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qrow * kD);
+  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
+                                                     qrow * Lay<kPair>::kDT + col0);
   uint4 q[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) q[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
@@ -427,9 +506,12 @@ __device__ __forceinline__ void rescale_o(uint32_t lane_base, float alpha) {
 }
 
 // The softmax warps' loop over the partition's tiles.  Returns false on an abort.
+template <bool kPair>
 __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, unsigned char *sm,
                                              uint64_t *bars, const StageInfo *info, uint32_t tmem,
-                                             volatile int *abort_flag, RowState &st) {
+                                             volatile int *abort_flag, RowState &st,
+                                             uint32_t rank) {
+  using L = Lay<kPair>;
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, i = 32 * w + lane;
   const int col = pl.qb * kRows + i, t = col >> a.group_shift;
   const bool real = t < pl.T;
@@ -442,13 +524,14 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     return warp_wait(bars + slot, parity, abort_flag, a.status);
   };
   for (int j = 0; j < pl.n; ++j) {
-    const int stg = j % kStages, r = j & 1, key0 = (pl.t_begin + j) * kKeys;
+    const int sk = j % kStages, sv = j % L::kStagesV, r = j & 1;
+    const int key0 = (pl.t_begin + j) * kKeys;
     const uint32_t region = lane_base + kSCol + 64 * r;
     if (!wait_all(kSFull + r, (j >> 1) & 1)) return false;
-    if (!wait_all(kFullK + stg, (j / kStages) & 1)) return false;  // publishes the record
-    const StageInfo inf = info[stg];
+    if (!wait_all(kFullK + sk, (j / kStages) & 1)) return false;  // publishes the record
+    const StageInfo inf = info[sk];
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + kInfoFree + stg);  // the record may be rewritten
+    if (lane == 0) mbar_arrive(bars + kInfoFree + sk);  // the record may be rewritten
     tc::fence_after_sync();
     uint32_t va[32], vb[32];
     tc::ld32(region, va);
@@ -456,6 +539,40 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     tc::wait_ld();
     tc::reg_fence(va);
     tc::reg_fence(vb);
+    if constexpr (kPair) {
+      // The scores are the sum of the two CTAs' products over their halves of
+      // the head dim: send this row's partial to the peer (row i of its block
+      // xb, 16-byte chunk q at q ^ (i % 16) against bank conflicts), take the
+      // peer's, add.  Both CTAs then hold the same bits and run the same softmax.
+      const int xb = j & 1;
+      const uint32_t peer = rank ^ 1u;
+      auto wait_cl = [&](int slot, uint32_t parity) {
+        return warp_wait_cluster(bars + slot, parity, abort_flag, a.status);
+      };
+      if (j >= 2 && !wait_cl(kXFree + xb, ((j - 2) >> 1) & 1)) return false;  // peer read j - 2
+      const uint32_t xrow = smem_u32(sm + L::kOffX + xb * kXBytes + i * (kKeys * 4));
+      const uint32_t xr = map_to(xrow, peer);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_cluster(xr + 16 * (q ^ (i & 15)), va[4 * q], va[4 * q + 1], va[4 * q + 2], va[4 * q + 3]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_cluster(xr + 16 * ((q + 8) ^ (i & 15)), vb[4 * q], vb[4 * q + 1], vb[4 * q + 2],
+                   vb[4 * q + 3]);
+      arrive_cluster(map_to(smem_u32(bars + kXFull + xb), peer));
+      if (!wait_cl(kXFull + xb, (j >> 1) & 1)) return false;  // the peer's partial of tile j
+      const unsigned char *xo = sm + L::kOffX + xb * kXBytes + i * (kKeys * 4);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(xo + 16 * (q ^ (i & 15)));
+        uint32_t *v = q < 8 ? &va[4 * q] : &vb[4 * (q - 8)];
+        v[0] = __float_as_uint(__uint_as_float(v[0]) + __uint_as_float(t.x));
+        v[1] = __float_as_uint(__uint_as_float(v[1]) + __uint_as_float(t.y));
+        v[2] = __float_as_uint(__uint_as_float(v[2]) + __uint_as_float(t.z));
+        v[3] = __float_as_uint(__uint_as_float(v[3]) + __uint_as_float(t.w));
+      }
+      arrive_cluster(map_to(smem_u32(bars + kXFree + xb), peer));  // block xb may be rewritten
+    }
 
     // ---- mask (by selection: scores of keys never loaded may be anything) and tile max
     float x[kKeys];
@@ -504,11 +621,11 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     // ---- V rows outside the CTA's keys or in skipped chunks: zero (they meet P = 0).
     // Every tile's V barrier is waited, in order, so that each wait's parity
     // names the phase it means.
-    if (!wait_all(kFullV + stg, (j / kStages) & 1)) return false;
+    if (!wait_all(kFullV + sv, (j / L::kStagesV) & 1)) return false;
     if (inf.vlo > 0 || inf.vhi < kKeys || inf.bad != 0) {
       const int rr = i >> 1;
       if (rr < inf.vlo || rr >= inf.vhi || ((inf.bad >> (rr >> 4)) & 1u)) {
-        unsigned char *vrow = sm + kOffV + stg * kKVBytes + rr * 128 + (i & 1) * 2 * kKVSlab;
+        unsigned char *vrow = sm + L::kOffV + sv * kKVBytes + rr * 128 + (i & 1) * 2 * kKVSlab;
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
@@ -536,9 +653,12 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
   return true;
 }
 
-// Write row i's result: o / l to `out` (direct) or the partial (m, l, o).
+// Write row i's result (this CTA's columns): o / l to `out` (direct) or the
+// partial (m, l, o); the pair's rank 0 writes m and l.
+template <bool kPair>
 __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, uint32_t tmem,
-                                           const RowState &st) {
+                                           const RowState &st, int col0) {
+  constexpr int DT = Lay<kPair>::kDT;
   const int w = (threadIdx.x >> 5) & 3, i = 32 * w + (threadIdx.x & 31);
   const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
   bool real;
@@ -555,8 +675,8 @@ __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, ui
     if (!real) continue;
     if (a.direct) {
       if (a.out_dtype == PSKV_DTYPE_BF16) {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + qrow * kD +
-                                               32 * c);
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + qrow * DT +
+                                               col0 + 32 * c);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t wd[4];
@@ -567,7 +687,8 @@ __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, ui
           dst[q] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
       } else {
-        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + qrow * kD + 32 * c);
+        float4 *dst =
+            reinterpret_cast<float4 *>(static_cast<float *>(a.out) + qrow * DT + col0 + 32 * c);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
@@ -575,14 +696,14 @@ __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, ui
                                __uint_as_float(v[4 * q + 3]) * inv);
       }
     } else {
-      float4 *dst = reinterpret_cast<float4 *>(a.ws_o + prow * kD + 32 * c);
+      float4 *dst = reinterpret_cast<float4 *>(a.ws_o + prow * DT + col0 + 32 * c);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
     }
   }
-  if (!real) return;
+  if (!real || col0 != 0) return;
   if (a.direct) {
     if (empty) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   } else {
@@ -593,20 +714,22 @@ __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, ui
 
 // A block whose partition holds no tile: empty partial states, or (one
 // partition) zeros flagged as empty rows.
-__device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl) {
+template <bool kPair>
+__device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl, int col0) {
+  constexpr int DT = Lay<kPair>::kDT;
   for (int i = threadIdx.x; i < kRows; i += blockDim.x) {
     bool real;
     const size_t qrow = query_row(a, pl, i, &real);
     if (!real) continue;
     if (a.direct) {
-      for (int d = 0; d < kD; ++d) {
+      for (int d = col0; d < col0 + kD; ++d) {
         if (a.out_dtype == PSKV_DTYPE_BF16)
-          static_cast<__nv_bfloat16 *>(a.out)[qrow * kD + d] = __float2bfloat16_rn(0.f);
+          static_cast<__nv_bfloat16 *>(a.out)[qrow * DT + d] = __float2bfloat16_rn(0.f);
         else
-          static_cast<float *>(a.out)[qrow * kD + d] = 0.f;
+          static_cast<float *>(a.out)[qrow * DT + d] = 0.f;
       }
       raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
-    } else {
+    } else if (col0 == 0) {
       const size_t prow = qrow * a.num_splits + pl.p;
       a.ws_m[prow] = -CUDART_INF_F;
       a.ws_l[prow] = 0.f;
@@ -616,42 +739,49 @@ __device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl) {
 
 }  // namespace
 
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     pskv_attn_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
+  using L = Lay<kPair>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-  StageInfo *info = reinterpret_cast<StageInfo *>(sm + kOffInfo);
-  uint32_t *slot = reinterpret_cast<uint32_t *>(sm + kOffSlot);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffAbort);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+  StageInfo *info = reinterpret_cast<StageInfo *>(sm + L::kOffInfo);
+  uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kOffSlot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a pair's two CTAs are adjacent in x and share one plan; rank c holds columns [256 c, +256)
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int col0 = (int)rank * kD;
 
   // every read of caller memory comes after the previous kernel's writes
   pdl_wait();
   pdl_launch_dependents();
-  const TcPlan pl = make_plan(a);
+  const TcPlan pl = make_plan(a, kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x);
   if (!pl.ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
     raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
+  // (both CTAs of a pair leave here together, before any exchange)
   if (pl.qb * kRows >= (pl.T << a.group_shift)) return;  // no query row in this block
   if (pl.n <= 0) {
-    write_empty(a, pl);
+    write_empty<kPair>(a, pl, col0);
     return;
   }
 
-  Loader ld(a, pl, &kmap, &vmap, sm, bars, info, abort_flag);
+  Loader<kPair> ld(a, pl, &kmap, &vmap, sm, bars, info, abort_flag, col0);
   if (warp == 1) {
     // the copy warp sets up the barriers and requests the first tiles at once
     if (lane == 0) {
-      for (int k = 0; k < 4 * kStages; ++k) mbar_init(&bars[k], 1);  // full / empty K, V
+      for (int k = 0; k < kInfoFree; ++k) mbar_init(&bars[k], 1);  // full / empty K, V
       for (int k = 0; k < kStages; ++k) mbar_init(&bars[kInfoFree + k], 4);  // per softmax warp
       for (int r = 0; r < 2; ++r) {
-        mbar_init(&bars[kSFull + r], 1);  // MMA commit
-        mbar_init(&bars[kPFull + r], 4);  // per softmax warp
+        mbar_init(&bars[kSFull + r], 1);   // MMA commit
+        mbar_init(&bars[kPFull + r], 4);   // per softmax warp
+        mbar_init(&bars[kPvDone + r], 1);  // MMA commit
+        mbar_init(&bars[kXFull + r], 128);  // per softmax thread of the peer
+        mbar_init(&bars[kXFree + r], 128);
       }
-      mbar_init(&bars[kPvDone], 1);  // MMA commits
-      mbar_init(&bars[kPvDone + 1], 1);
       mbar_init(&bars[kDrain], 1);
       mbar_init(&bars[kQReady], 4);
       *abort_flag = 0;
@@ -665,10 +795,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (kPair) cluster_sync();  // the peer's barriers are set up before any exchange
   const uint32_t tmem = *slot;
 
   if (warp == 0) {
-    Issuer is{a, pl, sm, bars, abort_flag};
+    Issuer<kPair> is{a, pl, sm, bars, abort_flag};
     is.run(tmem);
     is.drain();  // every MMA done before the memory is released
   } else if (warp == 1 || warp == 6) {
@@ -677,25 +808,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     ld.run(is_v);
     ld.drain(is_v);  // every copy landed before the CTA leaves
   } else {
-    stage_q(a, pl, tmem);
+    stage_q<kPair>(a, pl, tmem, col0);
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + kQReady);
     RowState st;
     st.m = -CUDART_INF_F;
     st.l = 0.f;
-    if (softmax_loop(a, pl, sm, bars, info, tmem, abort_flag, st)) {
+    if (softmax_loop<kPair>(a, pl, sm, bars, info, tmem, abort_flag, st, rank)) {
       // PV(n - 1); PV(n - 3) is known done, as S(n - 1) waited for it
       const bool ok =
           tc_wait(bars + kPvDone + ((pl.n - 1) & 1), ((pl.n - 1) >> 1) & 1, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc::fence_after_sync();
-        write_rows(a, pl, tmem, st);
+        write_rows<kPair>(a, pl, tmem, st, col0);
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (kPair) cluster_sync();  // no exchange still targets this CTA's memory
   if (warp == 0) {
     tc::fence_after_sync();
     tc::dealloc(tmem, kTmemCols);
@@ -718,13 +850,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool region as a 2-D tensor of `rows` rows of 256 bf16, read in boxes
+// The pool region as a 2-D tensor of `rows` rows of `dt` bf16, read in boxes
 // of 64 columns x box_rows rows in the 128-byte swizzled layout.
-bool make_map(CUtensorMap *m, const void *region, long long rows, int box_rows) {
+bool make_map(CUtensorMap *m, const void *region, long long rows, int dt, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)dt, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)dt * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t elem[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(region), dims, strides,
@@ -732,26 +864,49 @@ bool make_map(CUtensorMap *m, const void *region, long long rows, int box_rows) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, dim3 grid,
-                           cudaStream_t stream) {
+template <bool kPair>
+cudaError_t launch_tc(const TcArgs &a, const void *k_pool, const void *v_pool, dim3 grid,
+                      cudaStream_t stream) {
+  using L = Lay<kPair>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (!(dev >= 0 && dev < 64 && attr_set[dev])) {
-    e = cudaFuncSetAttribute(pskv_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(pskv_attn_tc_kernel<kPair>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const long long rows = a.num_pages * a.num_kv_heads * a.page_size;
   CUtensorMap km, vm;
-  if (!make_map(&km, k_pool, rows, a.box_rows) || !make_map(&vm, v_pool, rows, a.box_rows))
+  if (!make_map(&km, k_pool, rows, L::kDT, a.box_rows) ||
+      !make_map(&vm, v_pool, rows, L::kDT, a.box_rows))
     return cudaErrorInvalidValue;
-  return launch_pdl(pskv_attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, stream, a, km,
-                    vm);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kPair ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid.x * (kPair ? 2 : 1), grid.y, grid.z);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = kPair ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, pskv_attn_tc_kernel<kPair>, a, km, vm);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool,
+                           int head_dim, dim3 grid, cudaStream_t stream) {
+  if (head_dim == 2 * kD) return launch_tc<true>(a, k_pool, v_pool, grid, stream);
+  if (head_dim == kD) return launch_tc<false>(a, k_pool, v_pool, grid, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pskv

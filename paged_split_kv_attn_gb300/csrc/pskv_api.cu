@@ -148,24 +148,24 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int mgroup = 0;
   if ((rc = merge_group_of(opts, &mgroup))) return rc;
 
-  // Prefill at head dim 256 (bf16, split pools) runs on the tensor-memory
-  // kernel: blocks of 128 query columns, one CTA per block and partition.
+  // Prefill at head dim 256 or 512 (bf16, split pools) runs on the tensor-memory
+  // kernel: blocks of 128 query columns, one CTA (head dim 512: a CTA pair) per
+  // block and partition.
   const bool tc_path = varlen && kernel == kKernelMma && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
-                       d.head_dim_k == 256 && d.head_dim_v == 256 && (group & (group - 1)) == 0 &&
+                       d.head_dim_k == d.head_dim_v &&
+                       (d.head_dim_v == 256 || d.head_dim_v == 512) && (group & (group - 1)) == 0 &&
                        aligned(d.k_pool, 16) && aligned(d.v_pool, 16) &&
                        (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
   const int64_t tc_qblocks = (columns + 127) / 128;
   if (tc_path && tc_qblocks * PSKV_MAX_SPLITS > INT32_MAX) return PSKV_ERR_INVALID_ARG;
   int P = num_splits;
   if (P == 0 && tc_path) {
-    // one wave at least: split the keys only when the blocks alone leave SMs idle
     int n_sm = 0;
     if ((rc = sm_count(&n_sm))) return rc;
-    const int64_t ctas = tc_qblocks * d.num_kv_heads * batch;
     int64_t max_len = 1;
     for (int32_t b = 0; b < batch; ++b) max_len = seq_lens_host[b] > max_len ? seq_lens_host[b] : max_len;
-    const int64_t cap = std::max<int64_t>(1, (max_len + 63) / 64 / 4);  // >= 4 tiles per partition
-    P = (int)std::min<int64_t>({(n_sm + ctas - 1) / ctas, cap, (int64_t)PSKV_AUTO_MAX_SPLITS});
+    P = plan_tc_splits(tc_qblocks * d.num_kv_heads * batch, d.head_dim_v == 512 ? n_sm / 2 : n_sm,
+                       (max_len + 63) / 64);
   } else if (P == 0) {
     int slots = 0;
     if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
@@ -248,7 +248,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     t.window = qs.window;
     t.box_rows = d.page_size % 64 == 0 ? 64 : 16;
     t.scale_log2 = scale * kLog2e;
-    e = launch_attn_tc(t, d.k_pool, d.v_pool,
+    e = launch_attn_tc(t, d.k_pool, d.v_pool, d.head_dim_v,
                        dim3((unsigned)(tc_qblocks * P), d.num_kv_heads, batch), s);
   } else if (kernel == kKernelMma)
     e = launch_partial_mma(a, d.head_dim_v, group, folded, nt, grid, s);

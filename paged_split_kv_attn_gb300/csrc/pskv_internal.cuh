@@ -124,8 +124,9 @@ struct PrepArgs {
 };
 
 // Arguments of the tensor-memory (tcgen05) attention kernel: paged prefill at
-// head dim 256 over bf16 split pools; grid (qblocks * P, Hkv, B), one CTA per
-// block of 128 query columns (tokens x the KV group's heads) and partition.
+// head dim 256 or 512 over bf16 split pools; grid (qblocks * P, Hkv, B), one CTA
+// (head dim 512: a pair of CTAs) per block of 128 query columns (tokens x the
+// KV group's heads) and partition.
 struct TcArgs {
   const void *q;               // bf16 [rows][Hq][256]
   const int32_t *page_tables;  // [B][table_stride]
@@ -158,9 +159,10 @@ cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
-// Encodes the pools' tensor maps (rows = num_pages * Hkv * page_size < 2^31) and launches.
-cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, dim3 grid,
-                           cudaStream_t s);
+// Encodes the pools' tensor maps (rows = num_pages * Hkv * page_size < 2^31) and launches:
+// head dim 256 one CTA per (query block, partition) of `grid`, head dim 512 a pair of CTAs.
+cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, int head_dim,
+                           dim3 grid, cudaStream_t s);
 
 // Launch `kernel` with programmatic dependent launch allowed: it may start
 // while the previous kernel on the stream is still running, and must execute

@@ -45,6 +45,14 @@ int check_lengths(const pskv_layout *layout, int32_t batch, int32_t table_stride
 // Calls with more arithmetic per byte (folded rows, verify windows, prefill)
 // fill every slot.
 constexpr int kFillBytes32 = 27;
+// Key partitions for the tensor-memory prefill kernel: `units` blocks of 128
+// query columns (x KV heads x rows) over `slots` concurrent units (SMs, or SM
+// pairs at head dim 512), each block holding up to max_tiles 64-key tiles.
+// Splits the keys only when the blocks alone leave slots idle: P = ceil(slots /
+// units), at most 16 and at least 4 tiles per partition; with a wave or more
+// of blocks, P = 1 (a block's fixed costs and the merge outweigh balancing the
+// last wave).
+int plan_tc_splits(int64_t units, int slots, int64_t max_tiles);
 int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host,
                 int fill32 = 32);
 

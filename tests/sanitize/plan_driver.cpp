@@ -75,6 +75,14 @@ int main() {
   std::vector<int32_t> big(4096, INT32_MAX);
   CHECK(plan_splits(INT32_MAX, 4096, 4, big.data()) <= PSKV_AUTO_MAX_SPLITS);
 
+  // tensor-memory prefill: a wave or more of blocks runs unsplit
+  CHECK(plan_tc_splits(1024, 152, 64) == 1);
+  CHECK(plan_tc_splits(128, 76, 166) == 1);
+  CHECK(plan_tc_splits(32, 152, 1000) == 5);   // ceil(152 / 32)
+  CHECK(plan_tc_splits(32, 152, 8) == 2);      // at most 8 / 4 partitions
+  CHECK(plan_tc_splits(5, 152, 100000) == 16); // capped at 16
+  CHECK(plan_tc_splits(0, 152, 10) == 1);
+
   std::vector<int32_t> rows = {0, 1}, pos = {3, 600}, lease = {1, 2};
   CHECK(check_append_host(&lay, 2, 4, 2, rows.data(), pos.data(), lease.data()) ==
         PSKV_ERR_PAST_PAGES);
