@@ -67,21 +67,23 @@ enum : int {
   kPvDone = kPFull + 2,           // [2] PV of region r's tile done (MMA commit)
   kDrain = kPvDone + 2,           // every MMA done (MMA commit)
   kQReady = kDrain + 1,           // Q written to tensor memory (softmax warps)
-  kXFull = kQReady + 1,           // [2] the peer's partial scores arrived (CTA pair)
-  kXFree = kXFull + 2,            // [2] the peer read the partial scores sent to it
-  kNumBars = kXFree + 2
+  kXFull = kQReady + 1,           // the peer's partial scores arrived (CTA pair)
+  kXFree = kXFull + 1,            // the peer read the partial scores sent to it
+  kNumBars = kXFree + 1
 };
 
 // Head dim 256: one CTA.  Head dim 512: a cluster of two CTAs, rank c holding
 // columns [256 c, 256 c + 256) of Q, K, V and O (two V stages, to make room
-// for the exchanged partial scores).
+// for the block of partial scores received from the peer and the block staged
+// for sending to it).
 template <bool kPair>
 struct Lay {
   static constexpr int kDT = kPair ? 2 * kD : kD;  // the pool's head dim
   static constexpr int kStagesV = kPair ? 2 : 3;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;  // V stage s at kOffV + s * kKVBytes
-  static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // partial-score block b at + b * kXBytes
-  static constexpr int kOffBar = kOffX + (kPair ? 2 * kXBytes : 0);
+  static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // received partial scores
+  static constexpr int kOffXs = kOffX + (kPair ? kXBytes : 0);  // partial scores to send
+  static constexpr int kOffBar = kOffXs + (kPair ? kXBytes : 0);
   static constexpr int kOffInfo = kOffBar + kNumBars * 8;   // StageInfo[3]
   static constexpr int kOffSlot = kOffInfo + kStages * 16;  // tensor-memory address
   static constexpr int kOffAbort = kOffSlot + 4;
@@ -219,12 +221,6 @@ __device__ __forceinline__ uint32_t map_to(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
-                                           uint32_t w) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y),
-               "r"(z), "r"(w)
-               : "memory");
-}
 // Arrive on a barrier of another CTA, releasing this thread's writes at cluster scope.
 __device__ __forceinline__ void arrive_cluster(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
@@ -257,6 +253,21 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity
     }
   }
   return __all_sync(0xffffffffu, ok);
+}
+// Bulk copy of this CTA's shared memory into the peer's (both addresses
+// 16-byte aligned, bytes a multiple of 16), completion counted on the peer's
+// barrier `remote_bar`; the copy's reads are tracked by this thread's bulk group.
+__device__ __forceinline__ void bulk_s2peer(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];\n\tcp.async.bulk.commit_group;" ::"r"(remote_dst),
+      "r"(local_src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+// Wait until every bulk copy this thread committed has read its source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -541,37 +552,54 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     tc::reg_fence(vb);
     if constexpr (kPair) {
       // The scores are the sum of the two CTAs' products over their halves of
-      // the head dim: send this row's partial to the peer (row i of its block
-      // xb, 16-byte chunk q at q ^ (i % 16) against bank conflicts), take the
-      // peer's, add.  Both CTAs then hold the same bits and run the same softmax.
-      const int xb = j & 1;
+      // the head dim.  Each warp stages its 32 rows of partial scores (row i,
+      // 16-byte chunk q at q ^ (i % 16) against bank conflicts) and one bulk
+      // copy sends them into the peer's receive block, completing on the
+      // peer's barrier; the peer's rows arrive the same way and are added.
+      // Both CTAs then hold the same bits and run the same softmax.
       const uint32_t peer = rank ^ 1u;
       auto wait_cl = [&](int slot, uint32_t parity) {
         return warp_wait_cluster(bars + slot, parity, abort_flag, a.status);
       };
-      if (j >= 2 && !wait_cl(kXFree + xb, ((j - 2) >> 1) & 1)) return false;  // peer read j - 2
-      const uint32_t xrow = smem_u32(sm + L::kOffX + xb * kXBytes + i * (kKeys * 4));
-      const uint32_t xr = map_to(xrow, peer);
+      const int row0 = 32 * w;  // this warp's rows
+      unsigned char *xs = sm + L::kOffXs + i * (kKeys * 4);
+      if (lane == 0) bulk_wait_read();  // the previous send has read the staging rows
+      __syncwarp();
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_cluster(xr + 16 * (q ^ (i & 15)), va[4 * q], va[4 * q + 1], va[4 * q + 2], va[4 * q + 3]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_cluster(xr + 16 * ((q + 8) ^ (i & 15)), vb[4 * q], vb[4 * q + 1], vb[4 * q + 2],
-                   vb[4 * q + 3]);
-      arrive_cluster(map_to(smem_u32(bars + kXFull + xb), peer));
-      if (!wait_cl(kXFull + xb, (j >> 1) & 1)) return false;  // the peer's partial of tile j
-      const unsigned char *xo = sm + L::kOffX + xb * kXBytes + i * (kKeys * 4);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint4 t = *reinterpret_cast<const uint4 *>(xo + 16 * (q ^ (i & 15)));
-        uint32_t *v = q < 8 ? &va[4 * q] : &vb[4 * (q - 8)];
-        v[0] = __float_as_uint(__uint_as_float(v[0]) + __uint_as_float(t.x));
-        v[1] = __float_as_uint(__uint_as_float(v[1]) + __uint_as_float(t.y));
-        v[2] = __float_as_uint(__uint_as_float(v[2]) + __uint_as_float(t.z));
-        v[3] = __float_as_uint(__uint_as_float(v[3]) + __uint_as_float(t.w));
+      for (int q = 0; q < 8; ++q) {
+        *reinterpret_cast<uint4 *>(xs + 16 * (q ^ (i & 15))) =
+            make_uint4(va[4 * q], va[4 * q + 1], va[4 * q + 2], va[4 * q + 3]);
+        *reinterpret_cast<uint4 *>(xs + 16 * ((q + 8) ^ (i & 15))) =
+            make_uint4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
       }
-      arrive_cluster(map_to(smem_u32(bars + kXFree + xb), peer));  // block xb may be rewritten
+      tc::fence_smem_for_async();
+      __syncwarp();
+      // the peer has read what this CTA sent for tile j - 1
+      if (j >= 1 && !wait_cl(kXFree, (j - 1) & 1)) return false;
+      if (lane == 0) {
+        const uint32_t off = (uint32_t)row0 * (kKeys * 4);
+        bulk_s2peer(map_to(smem_u32(sm + L::kOffX) + off, peer), smem_u32(sm + L::kOffXs) + off,
+                    32 * kKeys * 4, map_to(smem_u32(bars + kXFull), peer));
+        mbar_arrive_expect_tx(bars + kXFull, 32 * kKeys * 4);  // this warp's rows from the peer
+      }
+      if (!wait_cl(kXFull, j & 1)) return false;  // the peer's partial of tile j
+      const unsigned char *xo = sm + L::kOffX + i * (kKeys * 4);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(xo + 16 * (q ^ (i & 15)));
+        const uint4 u = *reinterpret_cast<const uint4 *>(xo + 16 * ((q + 8) ^ (i & 15)));
+        va[4 * q] = __float_as_uint(__uint_as_float(va[4 * q]) + __uint_as_float(t.x));
+        va[4 * q + 1] = __float_as_uint(__uint_as_float(va[4 * q + 1]) + __uint_as_float(t.y));
+        va[4 * q + 2] = __float_as_uint(__uint_as_float(va[4 * q + 2]) + __uint_as_float(t.z));
+        va[4 * q + 3] = __float_as_uint(__uint_as_float(va[4 * q + 3]) + __uint_as_float(t.w));
+        vb[4 * q] = __float_as_uint(__uint_as_float(vb[4 * q]) + __uint_as_float(u.x));
+        vb[4 * q + 1] = __float_as_uint(__uint_as_float(vb[4 * q + 1]) + __uint_as_float(u.y));
+        vb[4 * q + 2] = __float_as_uint(__uint_as_float(vb[4 * q + 2]) + __uint_as_float(u.z));
+        vb[4 * q + 3] = __float_as_uint(__uint_as_float(vb[4 * q + 3]) + __uint_as_float(u.w));
+      }
+      tc::fence_smem_for_async();  // these reads before the peer's next copy into the block
+      __syncwarp();
+      if (lane == 0) arrive_cluster(map_to(smem_u32(bars + kXFree), peer));
     }
 
     // ---- mask (by selection: scores of keys never loaded may be anything) and tile max
@@ -779,9 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[kSFull + r], 1);   // MMA commit
         mbar_init(&bars[kPFull + r], 4);   // per softmax warp
         mbar_init(&bars[kPvDone + r], 1);  // MMA commit
-        mbar_init(&bars[kXFull + r], 128);  // per softmax thread of the peer
-        mbar_init(&bars[kXFree + r], 128);
       }
+      mbar_init(&bars[kXFull], 4);  // per local softmax warp (with the peer's bytes)
+      mbar_init(&bars[kXFree], 4);  // per softmax warp of the peer
       mbar_init(&bars[kDrain], 1);
       mbar_init(&bars[kQReady], 4);
       *abort_flag = 0;
@@ -824,6 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         write_rows<kPair>(a, pl, tmem, st, col0);
       }
     }
+    if (kPair && lane == 0) bulk_wait_read();  // no send still reads this CTA's memory
   }
   tc::fence_before_sync();
   __syncthreads();
