@@ -42,8 +42,7 @@ constexpr int kRows = 128;                  // query rows per CTA (MMA M)
 constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of PV)
 constexpr int kKVSlab = kKeys * 128;        // bytes of one 64-column slab of a K or V tile
 constexpr int kKVBytes = 4 * kKVSlab;       // 32 KB
-constexpr int kStages = 3;                  // K stages
-constexpr int kThreads = 224;               // MMA warp, K copy warp, 4 softmax warps, V copy warp
+constexpr int kStages = 3;                  // most K or V stages (barrier and record slots)
 constexpr int kXBytes = kRows * kKeys * 4;  // one block of partial scores (32 KB)
 constexpr int kTmemCols = 512;
 constexpr int kQCol = 0;                    // Q: 256 bf16 = 128 columns
@@ -67,9 +66,10 @@ enum : int {
   kPvDone = kPFull + 2,           // [2] PV of region r's tile done (MMA commit)
   kDrain = kPvDone + 2,           // every MMA done (MMA commit)
   kQReady = kDrain + 1,           // Q written to tensor memory (softmax warps)
-  kXFull = kQReady + 1,           // the peer's partial scores arrived (CTA pair)
-  kXFree = kXFull + 1,            // the peer read the partial scores sent to it
-  kNumBars = kXFree + 1
+  kXFull = kQReady + 1,           // [2] the peer's partial scores arrived (CTA pair)
+  kXFree = kXFull + 2,            // [2] the peer read the partial scores sent to it
+  kSReady = kXFree + 2,           // [2] the full scores of region r are in place (CTA pair)
+  kNumBars = kSReady + 2
 };
 
 // Head dim 256: one CTA.  Head dim 512: a cluster of two CTAs, rank c holding
@@ -79,10 +79,13 @@ enum : int {
 template <bool kPair>
 struct Lay {
   static constexpr int kDT = kPair ? 2 * kD : kD;  // the pool's head dim
+  // warps: 0 MMA, 1 K copies, 2-5 softmax, 6 V copies, (pair) 7-10 score exchange
+  static constexpr int kThreads = kPair ? 352 : 224;
+  static constexpr int kStagesK = kPair ? 2 : 3;
   static constexpr int kStagesV = kPair ? 2 : 3;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;  // V stage s at kOffV + s * kKVBytes
-  static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // received partial scores
-  static constexpr int kOffXs = kOffX + (kPair ? kXBytes : 0);  // partial scores to send
+  static constexpr int kOffV = kOffK + kStagesK * kKVBytes;  // V stage s at kOffV + s * kKVBytes
+  static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // received partial scores [2]
+  static constexpr int kOffXs = kOffX + (kPair ? 2 * kXBytes : 0);  // partial scores to send
   static constexpr int kOffBar = kOffXs + (kPair ? kXBytes : 0);
   static constexpr int kOffInfo = kOffBar + kNumBars * 8;   // StageInfo[3]
   static constexpr int kOffSlot = kOffInfo + kStages * 16;  // tensor-memory address
@@ -311,7 +314,7 @@ struct Loader {
   // (bit c of the bad mask per 16 rows).  The K copy writes the stage's record
   // before the barrier is armed (the arrive releases it).
   __device__ void load(int j, bool is_v) {
-    const int st = j % (is_v ? L::kStagesV : kStages);
+    const int st = j % (is_v ? L::kStagesV : L::kStagesK);
     const int key0 = (pl.t_begin + j) * kKeys;
     const int vlo = max(0, pl.k_lo - key0), vhi = min(kKeys, pl.k_hi - key0);
     const int32_t *tbl = a.page_tables + (size_t)pl.b * a.table_stride;
@@ -361,11 +364,11 @@ struct Loader {
   }
 
   __device__ void prologue(bool is_v) {
-    for (int j = 0; j < (is_v ? L::kStagesV : kStages) && j < pl.n; ++j) load(j, is_v);
+    for (int j = 0; j < (is_v ? L::kStagesV : L::kStagesK) && j < pl.n; ++j) load(j, is_v);
   }
 
   __device__ bool run(bool is_v) {
-    const int S = is_v ? L::kStagesV : kStages;
+    const int S = is_v ? L::kStagesV : L::kStagesK;
     for (int j = S; j < pl.n; ++j) {
       const int st = j % S;
       const uint32_t ph = ((j - S) / S) & 1;  // the stage's previous use
@@ -381,7 +384,7 @@ struct Loader {
 
   // Wait (bounded) for the last copy issued into each stage.
   __device__ void drain(bool is_v) {
-    const int S = is_v ? L::kStagesV : kStages;
+    const int S = is_v ? L::kStagesV : L::kStagesK;
     for (int j = max(0, issued - S); j < issued; ++j)
       mbar_wait(bars + (is_v ? kFullV : kFullK) + j % S, (j / S) & 1);
   }
@@ -409,8 +412,8 @@ struct Issuer {
     if (!wait(kQReady, 0)) return false;
     for (int j = 0; j <= n; ++j) {
       if (j < n) {
-        const int st = j % kStages, r = j & 1;
-        if (!wait(kFullK + st, (j / kStages) & 1)) return false;
+        const int st = j % L::kStagesK, r = j & 1;
+        if (!wait(kFullK + st, (j / L::kStagesK) & 1)) return false;
         if (j >= 2 && !wait(kPvDone + r, ((j - 2) >> 1) & 1)) return false;
         tc::fence_after_sync();
         const uint64_t dk = tc::smem_desc(smem_u32(sm + kOffK + st * kKVBytes), 16, 1024);
@@ -535,11 +538,12 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     return warp_wait(bars + slot, parity, abort_flag, a.status);
   };
   for (int j = 0; j < pl.n; ++j) {
-    const int sk = j % kStages, sv = j % L::kStagesV, r = j & 1;
+    const int sk = j % L::kStagesK, sv = j % L::kStagesV, r = j & 1;
     const int key0 = (pl.t_begin + j) * kKeys;
     const uint32_t region = lane_base + kSCol + 64 * r;
-    if (!wait_all(kSFull + r, (j >> 1) & 1)) return false;
-    if (!wait_all(kFullK + sk, (j / kStages) & 1)) return false;  // publishes the record
+    // (CTA pair: the exchange warps put the full scores in place)
+    if (!wait_all((kPair ? kSReady : kSFull) + r, (j >> 1) & 1)) return false;
+    if (!wait_all(kFullK + sk, (j / L::kStagesK) & 1)) return false;  // publishes the record
     const StageInfo inf = info[sk];
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + kInfoFree + sk);  // the record may be rewritten
@@ -550,57 +554,6 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     tc::wait_ld();
     tc::reg_fence(va);
     tc::reg_fence(vb);
-    if constexpr (kPair) {
-      // The scores are the sum of the two CTAs' products over their halves of
-      // the head dim.  Each warp stages its 32 rows of partial scores (row i,
-      // 16-byte chunk q at q ^ (i % 16) against bank conflicts) and one bulk
-      // copy sends them into the peer's receive block, completing on the
-      // peer's barrier; the peer's rows arrive the same way and are added.
-      // Both CTAs then hold the same bits and run the same softmax.
-      const uint32_t peer = rank ^ 1u;
-      auto wait_cl = [&](int slot, uint32_t parity) {
-        return warp_wait_cluster(bars + slot, parity, abort_flag, a.status);
-      };
-      const int row0 = 32 * w;  // this warp's rows
-      unsigned char *xs = sm + L::kOffXs + i * (kKeys * 4);
-      if (lane == 0) bulk_wait_read();  // the previous send has read the staging rows
-      __syncwarp();
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        *reinterpret_cast<uint4 *>(xs + 16 * (q ^ (i & 15))) =
-            make_uint4(va[4 * q], va[4 * q + 1], va[4 * q + 2], va[4 * q + 3]);
-        *reinterpret_cast<uint4 *>(xs + 16 * ((q + 8) ^ (i & 15))) =
-            make_uint4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
-      }
-      tc::fence_smem_for_async();
-      __syncwarp();
-      // the peer has read what this CTA sent for tile j - 1
-      if (j >= 1 && !wait_cl(kXFree, (j - 1) & 1)) return false;
-      if (lane == 0) {
-        const uint32_t off = (uint32_t)row0 * (kKeys * 4);
-        bulk_s2peer(map_to(smem_u32(sm + L::kOffX) + off, peer), smem_u32(sm + L::kOffXs) + off,
-                    32 * kKeys * 4, map_to(smem_u32(bars + kXFull), peer));
-        mbar_arrive_expect_tx(bars + kXFull, 32 * kKeys * 4);  // this warp's rows from the peer
-      }
-      if (!wait_cl(kXFull, j & 1)) return false;  // the peer's partial of tile j
-      const unsigned char *xo = sm + L::kOffX + i * (kKeys * 4);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 t = *reinterpret_cast<const uint4 *>(xo + 16 * (q ^ (i & 15)));
-        const uint4 u = *reinterpret_cast<const uint4 *>(xo + 16 * ((q + 8) ^ (i & 15)));
-        va[4 * q] = __float_as_uint(__uint_as_float(va[4 * q]) + __uint_as_float(t.x));
-        va[4 * q + 1] = __float_as_uint(__uint_as_float(va[4 * q + 1]) + __uint_as_float(t.y));
-        va[4 * q + 2] = __float_as_uint(__uint_as_float(va[4 * q + 2]) + __uint_as_float(t.z));
-        va[4 * q + 3] = __float_as_uint(__uint_as_float(va[4 * q + 3]) + __uint_as_float(t.w));
-        vb[4 * q] = __float_as_uint(__uint_as_float(vb[4 * q]) + __uint_as_float(u.x));
-        vb[4 * q + 1] = __float_as_uint(__uint_as_float(vb[4 * q + 1]) + __uint_as_float(u.y));
-        vb[4 * q + 2] = __float_as_uint(__uint_as_float(vb[4 * q + 2]) + __uint_as_float(u.z));
-        vb[4 * q + 3] = __float_as_uint(__uint_as_float(vb[4 * q + 3]) + __uint_as_float(u.w));
-      }
-      tc::fence_smem_for_async();  // these reads before the peer's next copy into the block
-      __syncwarp();
-      if (lane == 0) arrive_cluster(map_to(smem_u32(bars + kXFree), peer));
-    }
 
     // ---- mask (by selection: scores of keys never loaded may be anything) and tile max
     float x[kKeys];
@@ -677,6 +630,88 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const TcPlan &pl, 
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + kPFull + r);
+  }
+  return true;
+}
+
+// The CTA pair's score exchange (warps 7-10; warp w owns tensor-memory lanes
+// 32 (w % 4) .. + 31): the scores are the sum of the two CTAs' products over
+// their halves of the head dim.  Per tile j each warp reads its 32 rows of
+// partial scores from the tile's region, stages them (row i, 16-byte chunk q
+// at q ^ (i % 16) against bank conflicts) and one bulk copy sends them into
+// the peer's receive block j % 2, completing on the peer's barrier; the
+// peer's rows arrive the same way, are added, and the full scores go back
+// into the region for the softmax warps.  Both CTAs then hold the same bits
+// and run the same softmax.  Exchanging tile j + 1 overlaps the softmax of j.
+__device__ __forceinline__ bool exchange_loop(const TcArgs &a, const TcPlan &pl, unsigned char *sm,
+                                              uint64_t *bars, uint32_t tmem,
+                                              volatile int *abort_flag, uint32_t rank) {
+  using L = Lay<true>;
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, i = 32 * w + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t rows_off = (uint32_t)(32 * w) * (kKeys * 4);  // this warp's rows in a block
+  auto wait_all = [&](int slot, uint32_t parity) {
+    return warp_wait(bars + slot, parity, abort_flag, a.status);
+  };
+  auto wait_cl = [&](int slot, uint32_t parity) {
+    return warp_wait_cluster(bars + slot, parity, abort_flag, a.status);
+  };
+  unsigned char *xs = sm + L::kOffXs + i * (kKeys * 4);
+  for (int j = 0; j < pl.n; ++j) {
+    const int r = j & 1, xb = j & 1;
+    const uint32_t region = lane_base + kSCol + 64 * r;
+    if (!wait_all(kSFull + r, (j >> 1) & 1)) return false;  // this CTA's partial S(j)
+    tc::fence_after_sync();
+    uint32_t va[32], vb[32];
+    tc::ld32(region, va);
+    tc::ld32(region + 32, vb);
+    tc::wait_ld();
+    tc::reg_fence(va);
+    tc::reg_fence(vb);
+    if (lane == 0) bulk_wait_read();  // the previous send has read the staging rows
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      *reinterpret_cast<uint4 *>(xs + 16 * (q ^ (i & 15))) =
+          make_uint4(va[4 * q], va[4 * q + 1], va[4 * q + 2], va[4 * q + 3]);
+      *reinterpret_cast<uint4 *>(xs + 16 * ((q + 8) ^ (i & 15))) =
+          make_uint4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
+    }
+    tc::fence_smem_for_async();
+    __syncwarp();
+    // the peer has read what this CTA sent into its block xb for tile j - 2
+    if (j >= 2 && !wait_cl(kXFree + xb, ((j - 2) >> 1) & 1)) return false;
+    if (lane == 0) {
+      bulk_s2peer(map_to(smem_u32(sm + L::kOffX + xb * kXBytes) + rows_off, peer),
+                  smem_u32(sm + L::kOffXs) + rows_off, 32 * kKeys * 4,
+                  map_to(smem_u32(bars + kXFull + xb), peer));
+      mbar_arrive_expect_tx(bars + kXFull + xb, 32 * kKeys * 4);  // this warp's rows from the peer
+    }
+    if (!wait_cl(kXFull + xb, (j >> 1) & 1)) return false;  // the peer's partial of tile j
+    const unsigned char *xo = sm + L::kOffX + xb * kXBytes + i * (kKeys * 4);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 t = *reinterpret_cast<const uint4 *>(xo + 16 * (q ^ (i & 15)));
+      const uint4 u = *reinterpret_cast<const uint4 *>(xo + 16 * ((q + 8) ^ (i & 15)));
+      va[4 * q] = __float_as_uint(__uint_as_float(va[4 * q]) + __uint_as_float(t.x));
+      va[4 * q + 1] = __float_as_uint(__uint_as_float(va[4 * q + 1]) + __uint_as_float(t.y));
+      va[4 * q + 2] = __float_as_uint(__uint_as_float(va[4 * q + 2]) + __uint_as_float(t.z));
+      va[4 * q + 3] = __float_as_uint(__uint_as_float(va[4 * q + 3]) + __uint_as_float(t.w));
+      vb[4 * q] = __float_as_uint(__uint_as_float(vb[4 * q]) + __uint_as_float(u.x));
+      vb[4 * q + 1] = __float_as_uint(__uint_as_float(vb[4 * q + 1]) + __uint_as_float(u.y));
+      vb[4 * q + 2] = __float_as_uint(__uint_as_float(vb[4 * q + 2]) + __uint_as_float(u.z));
+      vb[4 * q + 3] = __float_as_uint(__uint_as_float(vb[4 * q + 3]) + __uint_as_float(u.w));
+    }
+    tc::fence_smem_for_async();  // these reads before the peer's next copy into the block
+    __syncwarp();
+    if (lane == 0) arrive_cluster(map_to(smem_u32(bars + kXFree + xb), peer));
+    tc::st32(region, va);
+    tc::st32(region + 32, vb);
+    tc::wait_st();
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kSReady + r);
   }
   return true;
 }
@@ -768,7 +803,7 @@ __device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl, i
 }  // namespace
 
 template <bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
     pskv_attn_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using L = Lay<kPair>;
@@ -808,8 +843,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[kPFull + r], 4);   // per softmax warp
         mbar_init(&bars[kPvDone + r], 1);  // MMA commit
       }
-      mbar_init(&bars[kXFull], 4);  // per local softmax warp (with the peer's bytes)
-      mbar_init(&bars[kXFree], 4);  // per softmax warp of the peer
+      for (int r = 0; r < 2; ++r) {
+        mbar_init(&bars[kXFull + r], 4);   // per exchange warp here (with the peer's bytes)
+        mbar_init(&bars[kXFree + r], 4);   // per exchange warp of the peer
+        mbar_init(&bars[kSReady + r], 4);  // per exchange warp
+      }
       mbar_init(&bars[kDrain], 1);
       mbar_init(&bars[kQReady], 4);
       *abort_flag = 0;
@@ -835,6 +873,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (is_v) ld.prologue(true);
     ld.run(is_v);
     ld.drain(is_v);  // every copy landed before the CTA leaves
+  } else if (warp >= 7) {
+    if constexpr (kPair) {
+      exchange_loop(a, pl, sm, bars, tmem, abort_flag, rank);
+      if (lane == 0) bulk_wait_read();  // no send still reads this CTA's memory
+    }
   } else {
     stage_q<kPair>(a, pl, tmem, col0);
     tc::fence_before_sync();
@@ -852,7 +895,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         write_rows<kPair>(a, pl, tmem, st, col0);
       }
     }
-    if (kPair && lane == 0) bulk_wait_read();  // no send still reads this CTA's memory
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -921,7 +963,7 @@ cudaError_t launch_tc(const TcArgs &a, const void *k_pool, const void *v_pool, d
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid.x * (kPair ? 2 : 1), grid.y, grid.z);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(L::kThreads);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
