@@ -1,9 +1,9 @@
-"""GPU parity of paged prefill at head dim 256, the tensor-memory (tcgen05)
-kernel's shape, against the oracle.
+"""GPU parity of paged prefill on the tensor-memory (tcgen05) kernel against
+the oracle: head dim 256 on one CTA, head dim 512 on a CTA pair.
 
 The kernel serves blocks of 128 query columns (tokens x the KV group's
 heads), 64-key tiles brought in by tensor copies in 16- or 64-row boxes
-(pages of 16 or 32 keys, pages of 64 or more), one CTA per block and
+(pages of 16 or 32 keys, pages of 64 or more), one CTA (pair) per block and
 partition.  Cases cover several blocks with a ragged last one, every group
 size, windows that cut tiles anywhere, empty partitions, pages outside the
 pool and the NaN-filled rows the generator leaves past each row's keys.
@@ -170,3 +170,35 @@ def test_bench_sliding_prompt_sampled_tokens():
                                    np.array([max(0, t - 1023)], np.int32))
         err = float(np.abs(got[t:t + 1].astype(np.float64) - ref).max())
         assert err <= TOL, f"token {t}: max |err| {err:.3e}"
+
+
+def test_bench_global_prompt_sampled_tokens():
+    """The bench's global prompt at full size (4,096 tokens, 32 q / 4 KV heads,
+    head dim 512 on a CTA pair, pages of 256, causal) in the automatic plan,
+    checked on sampled tokens against the oracle's decode of the row cut at
+    each token's own key."""
+    n = 4096
+    case = W.make_paged_case(211, [n], num_q_heads=32, num_kv_heads=4, head_dim=512,
+                             page_size=256, dtype="bf16", keep_dense=False)
+    dc = DevCase(case)
+    qn = _q(case, [n], seed=4)
+    q = to_dev(qn, "bf16")
+    out = run(dc, q, _cu([n]), splits=0)
+    torch.cuda.synchronize()
+    assert dc.faults() == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for t in (0, 1, 15, 16, 63, 64, 255, 1000, 2047, 4094, 4095):
+        ref = oracle.decode_direct(qn[t:t + 1], case.k_pool, case.v_pool, case.page_tables,
+                                   np.array([t + 1], np.int32), case.scale)
+        err = float(np.abs(got[t:t + 1].astype(np.float64) - ref).max())
+        assert err <= TOL, f"token {t}: max |err| {err:.3e}"
+
+
+def test_pair_group_of_one_small_pages_and_splits():
+    """Head dim 512 with one query head per KV head (G = 1) and pages of 16
+    (16-row copies): a chunk of 150 tokens at 400 keys, one and four
+    partitions (partials merged)."""
+    case = W.make_paged_case(212, [400, 37], num_q_heads=2, num_kv_heads=2, head_dim=512,
+                             page_size=16, dtype="bf16")
+    check(case, [150, 37], window=90, splits=(0, 1, 4))
