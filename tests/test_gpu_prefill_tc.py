@@ -202,3 +202,36 @@ def test_pair_group_of_one_small_pages_and_splits():
     case = W.make_paged_case(212, [400, 37], num_q_heads=2, num_kv_heads=2, head_dim=512,
                              page_size=16, dtype="bf16")
     check(case, [150, 37], window=90, splits=(0, 1, 4))
+
+
+@pytest.mark.parametrize("hd,hq,hkv,ps", [(256, 4, 2, 64), (512, 8, 1, 256)])
+def test_bad_device_offsets_and_lengths_are_flagged(hd, hq, hkv, ps):
+    """Device offsets past the packed rows, and a device length shorter than
+    the row's chunk, are refused per row on the device (PSKV_FAULT_BAD_LENGTH),
+    with nothing outside q / out addressed and the other row still right."""
+    case = W.make_paged_case(213, [300, 300], num_q_heads=hq, num_kv_heads=hkv, head_dim=hd,
+                             page_size=ps, dtype="bf16")
+    dc = DevCase(case)
+    counts = [40, 40]
+    qn = _q(case, counts)
+    q = to_dev(qn, "bf16")
+    cu = _cu(counts)
+    ref = oracle.prefill_direct(qn, cu, case.k_pool, case.v_pool, case.page_tables,
+                                case.seq_lens, case.scale, 0)
+    # row 1's offsets point past the 80 packed rows
+    out = pskv.prefill_attn_paged(dc.layout, q, i32([0, 40, 1 << 20]), cu, dc.tables, dc.lens,
+                                  case.seq_lens, case.scale, num_splits=1,
+                                  out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
+    assert max_err(out[:40], ref[:40]) <= TOL
+    # row 0's device length shorter than its chunk: that row reads no key
+    dc.status.zero_()
+    bad_lens = i32([10, 300])
+    out = pskv.prefill_attn_paged(dc.layout, q, i32(cu), cu, dc.tables, bad_lens,
+                                  case.seq_lens, case.scale, num_splits=1,
+                                  out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
+    assert max_err(out[40:], ref[40:]) <= TOL
+    assert np.all(np.isfinite(out.cpu().numpy()))
