@@ -176,7 +176,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
   return false;
 }
 
-// The same wait taken by a whole warp: one verdict for all lanes.
+// The same wait taken by a whole warp: one answer for all lanes.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status) {
   const bool ok = tc_wait(bar, parity, abort_flag, status);
@@ -239,7 +239,7 @@ __device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait with cluster-scope acquire, one verdict for the warp.
+// Bounded wait with cluster-scope acquire, one answer for the whole warp.
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort_flag, int32_t *status) {
   bool ok = !*abort_flag;
