@@ -320,10 +320,13 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
  *                bytes; NULL is fine when the plan has one partition (the
  *                automatic plan for long chunks): each CTA then writes its
  *                normalised output directly and no merge runs
- * A CTA serves 16 query columns (query heads of a KV head x tokens) of one
- * row; its keys are those its tokens see.  bf16 pools with 1/2/4/8 query
- * heads per KV head.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL,
- * CUDA. */
+ * Split-format bf16 pools of head dim 256 or 512 run on the tensor-memory
+ * kernel: a CTA (head dim 512: a cluster of two, each holding half of the
+ * head dim) serves 128 query columns (query heads of a KV head x tokens) of
+ * one row, for 1, 2, 4, ..., 128 query heads per KV head; its keys are those
+ * its tokens see.  Folded bf16 pools run 16 columns per CTA on the split-KV
+ * kernels, with 1/2/4/8 query heads per KV head.  Other pools: UNSUPPORTED.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 int prefill_attn_paged(const pskv_layout *layout, const void *q, const int32_t *cu_q_host,
                        const int32_t *cu_q, const int32_t *page_tables, int32_t table_stride,
                        const int32_t *seq_lens_host, const int32_t *seq_lens, int32_t batch,

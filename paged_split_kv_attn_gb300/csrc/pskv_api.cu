@@ -107,10 +107,20 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   if (d.num_kv_heads > 65535) return PSKV_ERR_UNSUPPORTED;
   const int group = num_q_heads / d.num_kv_heads;
   const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
-  if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
   const bool folded = d.format == PSKV_FORMAT_FOLDED;
   const bool varlen = qs.cu_q_host != nullptr;
   if (varlen && !qs.cu_q) return PSKV_ERR_INVALID_ARG;
+  // Prefill of bf16 split pools at head dim 256 or 512 runs on the
+  // tensor-memory kernel: blocks of 128 query columns (any power-of-two group
+  // up to 128 query heads per KV head), one CTA (head dim 512: a CTA pair)
+  // per block and partition.
+  const bool tc_path = varlen && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
+                       d.head_dim_k == d.head_dim_v &&
+                       (d.head_dim_v == 256 || d.head_dim_v == 512) && group <= 128 &&
+                       (group & (group - 1)) == 0 && aligned(d.k_pool, 16) &&
+                       aligned(d.v_pool, 16) &&
+                       (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
+  if (kernel < 0 && !tc_path) return PSKV_ERR_UNSUPPORTED;
   const bool append = opts && opts->append_k;
   if (append) {
     if (!opts->append_v || !opts->append_pages) return PSKV_ERR_INVALID_ARG;
@@ -139,7 +149,8 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   // Query columns per KV head (heads x tokens): one n-tile of 8 when they fit,
   // else blocks of two n-tiles, one CTA per block (several tokens only on the
   // tensor-core family).
-  if ((max_t > 1 || varlen) && (kernel != kKernelMma || windowed)) return PSKV_ERR_UNSUPPORTED;
+  if ((max_t > 1 || varlen) && !tc_path && (kernel != kKernelMma || windowed))
+    return PSKV_ERR_UNSUPPORTED;
   const int64_t columns = group * max_t;
   const int nt = columns > 8 ? 2 : 1;
   const int64_t col_blocks = (columns + 8 * nt - 1) / (8 * nt);
@@ -148,14 +159,6 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int mgroup = 0;
   if ((rc = merge_group_of(opts, &mgroup))) return rc;
 
-  // Prefill at head dim 256 or 512 (bf16, split pools) runs on the tensor-memory
-  // kernel: blocks of 128 query columns, one CTA (head dim 512: a CTA pair) per
-  // block and partition.
-  const bool tc_path = varlen && kernel == kKernelMma && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
-                       d.head_dim_k == d.head_dim_v &&
-                       (d.head_dim_v == 256 || d.head_dim_v == 512) && (group & (group - 1)) == 0 &&
-                       aligned(d.k_pool, 16) && aligned(d.v_pool, 16) &&
-                       (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
   const int64_t tc_qblocks = (columns + 127) / 128;
   if (tc_path && tc_qblocks * PSKV_MAX_SPLITS > INT32_MAX) return PSKV_ERR_INVALID_ARG;
   int P = num_splits;
@@ -176,7 +179,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
                     bytes_bound ? kFillBytes32 : 32);
   }
   // one partition on the tensor-core kernels: the partial is the output
-  const bool direct = P == 1 && kernel == kKernelMma;
+  const bool direct = P == 1 && (kernel == kKernelMma || tc_path);
   WorkspacePlan w;
   if ((rc = plan_workspace(rows, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;

@@ -239,6 +239,9 @@ def test_prefill_refusals_happen_before_any_launch(lib):
         assert _prefill_rc(lib, h, [100, 50], [0, 0, 0]) == B.PSKV_ERR_INVALID_ARG  # no token
         assert _prefill_rc(lib, h, [100], [0, 5], window=-1) == B.PSKV_ERR_INVALID_ARG
         assert _prefill_rc(lib, f32, [100], [0, 5]) == B.PSKV_ERR_UNSUPPORTED  # tensor-core only
+        # query heads per KV head: a power of two up to 128 (a block of 128 columns)
+        assert _prefill_rc(lib, h, [100], [0, 5], hq=12) == B.PSKV_ERR_UNSUPPORTED   # G = 3
+        assert _prefill_rc(lib, h, [100], [0, 5], hq=1024) == B.PSKV_ERR_UNSUPPORTED  # G = 256
         # several partitions need the partial buffer
         assert _prefill_rc(lib, h, [100], [0, 5], splits=2) == B.PSKV_ERR_WORKSPACE_TOO_SMALL
     finally:

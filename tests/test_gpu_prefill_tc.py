@@ -235,3 +235,16 @@ def test_bad_device_offsets_and_lengths_are_flagged(hd, hq, hkv, ps):
     assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
     assert max_err(out[40:], ref[40:]) <= TOL
     assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+@pytest.mark.parametrize("hd,hq,hkv,lens,counts,window", [
+    (256, 32, 2, [300, 37], [100, 37], 0),    # G = 16: 8 tokens per block
+    (256, 32, 1, [130], [40], 50),            # G = 32: 4 tokens per block
+    (512, 32, 2, [200, 70], [50, 9], 0),      # G = 16 on the CTA pair
+])
+def test_large_groups(hd, hq, hkv, lens, counts, window):
+    """Groups the decode kernels do not serve (16 or 32 query heads per KV
+    head) prefill on the tensor-memory kernel: 128 / G tokens per block."""
+    case = W.make_paged_case(214 + hq // hkv, lens, num_q_heads=hq, num_kv_heads=hkv,
+                             head_dim=hd, page_size=64, dtype="bf16")
+    check(case, counts, window=window, splits=(0, 1, 3))
