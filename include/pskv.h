@@ -286,13 +286,16 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
  *   num_tokens  1..PSKV_MAX_WINDOW_TOKENS.  The window's query columns per KV
  *               head (query heads per KV head x num_tokens) are served 8 per
  *               CTA when they fit in 8, else 16 per CTA, the CTAs of one
- *               partition reading the same keys (the later ones mostly from L2)
+ *               partition reading the same keys (the later ones mostly from L2);
+ *               from 40 columns on (bf16 split pools, head dim 256 or 512) by
+ *               the tensor-memory kernel, 128 columns per CTA (pair)
  *   seq_lens    every length at least num_tokens
  *   workspace   decode_attn_workspace_bytes(batch * num_tokens, num_q_heads, ...)
  *               bytes; its partials are laid out as for batch * num_tokens rows
  *               (row b * num_tokens + t)
- * bf16 pools with 1/2/4/8 query heads per KV head only; no
- * key window.  num_tokens = 1 gives decode_attn_splitkv's bits.
+ * bf16 pools with 1/2/4/8 query heads per KV head (any power of two up to
+ * 128 when the window has 40 columns or more on a split pool); no key window.
+ * num_tokens = 1 gives decode_attn_splitkv's bits.
  * Errors: INVALID_ARG (also a host length below num_tokens), UNSUPPORTED,
  * WORKSPACE_TOO_SMALL, CUDA. */
 int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t *page_tables,

@@ -129,7 +129,9 @@ __device__ __forceinline__ TcPlan make_plan(const TcArgs &a, int x) {
   pl.g = blockIdx.y;
   pl.b = blockIdx.z;
   pl.ok = true;
-  const int c0 = a.cu_q[pl.b], c1 = a.cu_q[pl.b + 1];
+  // a verify window (no offsets): num_tokens query rows per table row
+  const int c0 = a.cu_q ? a.cu_q[pl.b] : pl.b * a.num_tokens;
+  const int c1 = a.cu_q ? a.cu_q[pl.b + 1] : c0 + a.num_tokens;
   if (c0 < 0 || c1 < c0 || c1 > a.total_rows) {  // never address rows outside the arrays
     pl.ok = false;
     pl.T = 0;

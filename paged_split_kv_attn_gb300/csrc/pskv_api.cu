@@ -78,6 +78,13 @@ int merge_group_of(const pskv_decode_opts *opts, int *group) {
 // Level 2 folds at most this many group results per row.
 constexpr int kMaxGroups = 64;
 
+// Verify windows with at least this many query columns per KV head (tokens x
+// query heads per KV head) run on the tensor-memory kernel: a block of 128
+// columns costs the same whatever its real columns, and at 40,002 keys (head
+// dim 512, 8 query heads per KV head) it took ~128 us against 109 / 160 us for
+// 4 / 6 tokens on the split-KV kernels.
+constexpr int64_t kTcMinColumns = 40;
+
 // The query side of a call: a uniform number of tokens per row (single-token
 // decode, verify windows), or variable-length chunks given by row offsets
 // (prefill), optionally with a per-token window.
@@ -113,8 +120,11 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   // Prefill of bf16 split pools at head dim 256 or 512 runs on the
   // tensor-memory kernel: blocks of 128 query columns (any power-of-two group
   // up to 128 query heads per KV head), one CTA (head dim 512: a CTA pair)
-  // per block and partition.
-  const bool tc_path = varlen && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
+  // per block and partition; so do verify windows of at least
+  // kTcMinColumns query columns per KV head.
+  const bool many_rows =
+      varlen || (!windowed && qs.tokens >= 2 && (int64_t)qs.tokens * group >= kTcMinColumns);
+  const bool tc_path = many_rows && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
                        d.head_dim_k == d.head_dim_v &&
                        (d.head_dim_v == 256 || d.head_dim_v == 512) && group <= 128 &&
                        (group & (group - 1)) == 0 && aligned(d.k_pool, 16) &&
@@ -231,7 +241,8 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     t.q = q;
     t.page_tables = page_tables;
     t.seq_lens = seq_lens;
-    t.cu_q = qs.cu_q;
+    t.cu_q = varlen ? qs.cu_q : nullptr;
+    t.num_tokens = varlen ? 0 : qs.tokens;
     t.status = d.status;
     t.ws_m = a.ws_m;
     t.ws_l = a.ws_l;

@@ -128,13 +128,14 @@ struct PrepArgs {
 // (head dim 512: a pair of CTAs) per block of 128 query columns (tokens x the
 // KV group's heads) and partition.
 struct TcArgs {
-  const void *q;               // bf16 [rows][Hq][256]
+  const void *q;               // bf16 [rows][Hq][D]
   const int32_t *page_tables;  // [B][table_stride]
   const int32_t *seq_lens;     // [B]
-  const int32_t *cu_q;         // [B + 1] first query row of each table row
+  const int32_t *cu_q;         // [B + 1] first query row of each table row, or null:
+  int num_tokens;              //   then num_tokens rows per table row (a verify window)
   int32_t *status;
-  float *ws_m, *ws_l, *ws_o;   // partials [rows][Hq][P] (o: x 256) when not direct
-  void *out;                   // [rows][Hq][256] of out_dtype when direct
+  float *ws_m, *ws_l, *ws_o;   // partials [rows][Hq][P] (o: x D) when not direct
+  void *out;                   // [rows][Hq][D] of out_dtype when direct
   int out_dtype;
   int direct;
   long long num_pages;

@@ -111,3 +111,10 @@ def test_device_length_below_the_window_is_flagged():
     run(dc, q, 2, lens=i32([2]))
     torch.cuda.synchronize()
     assert dc.faults() & pskv.PSKV_FAULT_BAD_LENGTH
+
+
+@pytest.mark.parametrize("hd,hq,hkv,tokens", [(256, 32, 2, 4), (512, 32, 2, 3)])
+def test_wide_windows_of_large_groups(hd, hq, hkv, tokens):
+    """16 query heads per KV head: windows of 64 / 48 columns run on the
+    tensor-memory kernel (the split-KV kernels do not serve this group)."""
+    check(small(79 + tokens, [900, 333], hq, hkv, hd, 64), tokens, splits=(0, 1, 4))
