@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
+#include "attn_tc.h"
 #include "pskv_internal.cuh"
 #include "tc_ops.cuh"
 

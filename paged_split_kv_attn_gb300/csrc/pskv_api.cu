@@ -10,6 +10,7 @@
 #include <cstring>
 #include <new>
 
+#include "attn_tc.h"
 #include "pskv_internal.cuh"
 #include "pskv_plan.h"
 

@@ -123,28 +123,6 @@ struct PrepArgs {
   int32_t *status;
 };
 
-// Arguments of the tensor-memory (tcgen05) attention kernel: paged prefill at
-// head dim 256 or 512 over bf16 split pools; grid (qblocks * P, Hkv, B), one CTA
-// (head dim 512: a pair of CTAs) per block of 128 query columns (tokens x the
-// KV group's heads) and partition.
-struct TcArgs {
-  const void *q;               // bf16 [rows][Hq][D]
-  const int32_t *page_tables;  // [B][table_stride]
-  const int32_t *seq_lens;     // [B]
-  const int32_t *cu_q;         // [B + 1] first query row of each table row, or null:
-  int num_tokens;              //   then num_tokens rows per table row (a verify window)
-  int32_t *status;
-  float *ws_m, *ws_l, *ws_o;   // partials [rows][Hq][P] (o: x D) when not direct
-  void *out;                   // [rows][Hq][D] of out_dtype when direct
-  int out_dtype;
-  int direct;
-  long long num_pages;
-  int table_stride, page_size, num_kv_heads, num_q_heads;
-  int group_shift;             // log2 of the query heads per KV head
-  int num_splits, qblocks, total_rows, window;
-  int box_rows;                // rows per tensor copy: 64 when a page holds whole tiles, else 16
-  float scale_log2;
-};
 
 // Host-side launchers (one per kernel family).  They return a CUDA error code.
 // The tensor-core family takes `nt` n-tiles of 8 query columns (group x tokens <= 8 nt).
@@ -160,10 +138,6 @@ cudaError_t occupancy_partial_simt_bf16(int head_dim, int group, int *ctas);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
-// Encodes the pools' tensor maps (rows = num_pages * Hkv * page_size < 2^31) and launches:
-// head dim 256 one CTA per (query block, partition) of `grid`, head dim 512 a pair of CTAs.
-cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, int head_dim,
-                           dim3 grid, cudaStream_t s);
 
 // Launch `kernel` with programmatic dependent launch allowed: it may start
 // while the previous kernel on the stream is still running, and must execute
