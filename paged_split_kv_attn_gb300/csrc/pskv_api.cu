@@ -82,7 +82,7 @@ constexpr int kMaxGroups = 64;
 // Verify windows with at least this many query columns per KV head (tokens x
 // query heads per KV head) run on the tensor-memory kernel: a block of 128
 // columns costs the same whatever its real columns, and at 40,002 keys (head
-// dim 512, 8 query heads per KV head) it took ~128 us against 109 / 160 us for
+// dim 512, 8 query heads per KV head) it took ~115 us against 109 / 160 us for
 // 4 / 6 tokens on the split-KV kernels.
 constexpr int64_t kTcMinColumns = 40;
 

@@ -119,7 +119,7 @@ int pick_kernel(int kv_dtype, int head_dim, int group, int format) {
 int plan_tc_splits(int64_t units, int slots, int64_t max_tiles) {
   if (units < 1 || slots < 1 || units >= slots) return 1;
   int64_t cap = max_tiles / 4;
-  if (cap > 16) cap = 16;
+  if (cap > 32) cap = 32;
   if (cap < 1) cap = 1;
   const int64_t p = (slots + units - 1) / units;  // one wave at least
   return (int)(p < cap ? p : cap);

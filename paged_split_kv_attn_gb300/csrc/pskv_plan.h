@@ -49,7 +49,7 @@ constexpr int kFillBytes32 = 27;
 // query columns (x KV heads x rows) over `slots` concurrent units (SMs, or SM
 // pairs at head dim 512), each block holding up to max_tiles 64-key tiles.
 // Splits the keys only when the blocks alone leave slots idle: P = ceil(slots /
-// units), at most 16 and at least 4 tiles per partition; with a wave or more
+// units), at most 32 and at least 4 tiles per partition; with a wave or more
 // of blocks, P = 1 (a block's fixed costs and the merge outweigh balancing the
 // last wave).
 int plan_tc_splits(int64_t units, int slots, int64_t max_tiles);

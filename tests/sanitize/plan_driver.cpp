@@ -80,7 +80,8 @@ int main() {
   CHECK(plan_tc_splits(128, 76, 166) == 1);
   CHECK(plan_tc_splits(32, 152, 1000) == 5);   // ceil(152 / 32)
   CHECK(plan_tc_splits(32, 152, 8) == 2);      // at most 8 / 4 partitions
-  CHECK(plan_tc_splits(5, 152, 100000) == 16); // capped at 16
+  CHECK(plan_tc_splits(5, 152, 100000) == 31); // ceil(152 / 5)
+  CHECK(plan_tc_splits(2, 152, 100000) == 32); // capped at 32
   CHECK(plan_tc_splits(0, 152, 10) == 1);
 
   std::vector<int32_t> rows = {0, 1}, pos = {3, 600}, lease = {1, 2};
