@@ -158,7 +158,8 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"pskv_clocks_rank{device_index}.csv")
 
     def start(self):
         try:
@@ -505,7 +506,7 @@ def parse():
                     help="skip timing the step with the fused K/V prep beside the headline step")
     ap.add_argument("--folded-contexts", type=int, nargs="*", default=[40002],
                     help="contexts of the folded-format decode timed beside the step")
-    ap.add_argument("--verify-tokens", type=int, nargs="*", default=[2, 4],
+    ap.add_argument("--verify-tokens", type=int, nargs="*", default=[2, 4, 8],
                     help="verify-window lengths of the multi-row decode timed beside the step")
     ap.add_argument("--verify-context", type=int, default=40002,
                     help="context of those verify windows (global-layer shape)")
