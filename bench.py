@@ -78,7 +78,7 @@ def measured_peak():
 
 
 def measured_tensor_peak() -> float:
-    """Dense bf16 TFLOP/s measured on this machine (burst), else the fallback figure."""
+    """Dense bf16 TFLOP/s from the measured-peaks file (burst), else the fallback figure."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             return float(json.load(f)["bf16_tflops"])
