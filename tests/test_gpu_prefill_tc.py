@@ -248,3 +248,33 @@ def test_large_groups(hd, hq, hkv, lens, counts, window):
     case = W.make_paged_case(214 + hq // hkv, lens, num_q_heads=hq, num_kv_heads=hkv,
                              head_dim=hd, page_size=64, dtype="bf16")
     check(case, counts, window=window, splits=(0, 1, 3))
+
+
+def test_random_shapes_against_the_oracle():
+    """Forty seeded random prefills (head dim 256 / 512, 1-16 query heads per
+    KV head, pages of 16-256, 1-3 rows with chunks of any length including
+    empty ones, windows, one to five partitions) against the oracle."""
+    rng = np.random.default_rng(2024)
+    for it in range(40):
+        hd = int(rng.choice([256, 512]))
+        g = int(rng.choice([1, 2, 4, 8, 16]))
+        hkv = int(rng.choice([1, 2]))
+        ps = int(rng.choice([16, 32, 64, 128, 256]))
+        lens = [int(rng.integers(1, 700)) for _ in range(int(rng.integers(1, 4)))]
+        counts = [int(rng.integers(0, n + 1)) for n in lens]
+        if sum(counts) == 0:
+            counts[0] = lens[0]
+        window = int(rng.choice([0, 0, int(rng.integers(1, 300))]))
+        splits = int(rng.choice([0, 1, 2, 5]))
+        case = W.make_paged_case(int(rng.integers(1 << 30)), lens, num_q_heads=g * hkv,
+                                 num_kv_heads=hkv, head_dim=hd, page_size=ps, dtype="bf16")
+        dc = DevCase(case)
+        qn = _q(case, counts, seed=it)
+        cu = _cu(counts)
+        ref = oracle.prefill_direct(qn, cu, case.k_pool, case.v_pool, case.page_tables,
+                                    case.seq_lens, case.scale, window)
+        out = run(dc, to_dev(qn, "bf16"), cu, window, splits)
+        torch.cuda.synchronize()
+        err = max_err(out, ref)
+        assert err <= TOL and dc.faults() == 0, (it, hd, g, hkv, ps, lens, counts, window,
+                                                  splits, err)
