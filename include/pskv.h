@@ -287,14 +287,17 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
  *               head (query heads per KV head x num_tokens) are served 8 per
  *               CTA when they fit in 8, else 16 per CTA, the CTAs of one
  *               partition reading the same keys (the later ones mostly from L2);
- *               from 40 columns on (bf16 split pools, head dim 256 or 512) by
- *               the tensor-memory kernel, 128 columns per CTA (pair)
+ *               on bf16 split pools of head dim 256 or 512, 17 to 64 columns
+ *               by the key-major tensor-memory kernel (128 keys per tile as
+ *               the MMA's M, the columns as its N, one CTA per partition
+ *               streaming the keys once) and from 65 columns on by the
+ *               query-major tensor-memory kernel, 128 columns per CTA (pair)
  *   seq_lens    every length at least num_tokens
  *   workspace   decode_attn_workspace_bytes(batch * num_tokens, num_q_heads, ...)
  *               bytes; its partials are laid out as for batch * num_tokens rows
  *               (row b * num_tokens + t)
  * bf16 pools with 1/2/4/8 query heads per KV head (any power of two up to
- * 128 when the window has 40 columns or more on a split pool); no key window.
+ * 128 when the window has more than 16 columns on a split pool); no key window.
  * num_tokens = 1 gives decode_attn_splitkv's bits.
  * Errors: INVALID_ARG (also a host length below num_tokens), UNSUPPORTED,
  * WORKSPACE_TOO_SMALL, CUDA. */

@@ -32,11 +32,19 @@
 
 #include "attn_tc.h"
 #include "pskv_internal.cuh"
+#include "tc_common.cuh"
 #include "tc_ops.cuh"
 
 namespace pskv {
 
 namespace {
+
+using tc::elect_one;
+using tc::ex2;
+using tc::make_map;
+using tc::PageCache;
+using tc::tc_wait;
+using tc::warp_wait;
 
 constexpr int kD = 256;                     // head-dim columns per CTA
 constexpr int kRows = 128;                  // query rows per CTA (MMA M)
@@ -167,52 +175,6 @@ __device__ __forceinline__ TcPlan make_plan(const TcArgs &a, int x) {
   pl.n = hi - lo;
   return pl;
 }
-
-
-// Bounded wait that gives up at once when another thread of the CTA already has.
-__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                        int32_t *status) {
-  if (*abort_flag) return false;
-  if (mbar_wait(bar, parity)) return true;
-  *abort_flag = 1;
-  raise_fault(status, PSKV_FAULT_WAIT_TIMEOUT);
-  return false;
-}
-
-// The same wait taken by a whole warp: one answer for all lanes.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
-  const bool ok = tc_wait(bar, parity, abort_flag, status);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
-// 2^x by the special-function unit (inputs of -inf give 0; results below the
-// smallest normal flush to 0, far below what a weight can contribute).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Page ids of 32 consecutive table slots held across the copy warp's lanes.
-struct PageCache {
-  int base = -1, val = -1;
-  __device__ int get(const int32_t *tbl, int slot, int n_slots, int lane) {
-    if (base < 0 || slot < base || slot >= base + 32) {
-      base = slot;
-      val = slot + lane < n_slots ? __ldg(tbl + slot + lane) : -1;
-    }
-    return __shfl_sync(0xffffffffu, val, slot - base);
-  }
-};
 
 
 // ---- the CTA pair: distributed shared memory and cluster-scope barriers
@@ -910,33 +872,6 @@ __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
 
 
 namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// The pool region as a 2-D tensor of `rows` rows of `dt` bf16, read in boxes
-// of 64 columns x box_rows rows in the 128-byte swizzled layout.
-bool make_map(CUtensorMap *m, const void *region, long long rows, int dt, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)dt, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)dt * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  const cuuint32_t elem[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(region), dims, strides,
-             box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <bool kPair>
 cudaError_t launch_tc(const TcArgs &a, const void *k_pool, const void *v_pool, dim3 grid,

@@ -35,4 +35,10 @@ struct TcArgs {
 cudaError_t launch_attn_tc(const TcArgs &a, const void *k_pool, const void *v_pool, int head_dim,
                            dim3 grid, cudaStream_t s);
 
+// Verify windows of 17 to 64 query columns per KV head (num_tokens rows per
+// table row, qblocks 1, no offsets, no window): the key-major kernel, one CTA
+// per (partition, KV head, row) of `grid`; partitions of whole 16-key groups.
+cudaError_t launch_attn_verify(const TcArgs &a, const void *k_pool, const void *v_pool,
+                               int head_dim, dim3 grid, cudaStream_t s);
+
 }  // namespace pskv

@@ -79,12 +79,18 @@ int merge_group_of(const pskv_decode_opts *opts, int *group) {
 // Level 2 folds at most this many group results per row.
 constexpr int kMaxGroups = 64;
 
-// Verify windows with at least this many query columns per KV head (tokens x
-// query heads per KV head) run on the tensor-memory kernel: a block of 128
-// columns costs the same whatever its real columns, and at 40,002 keys (head
-// dim 512, 8 query heads per KV head) it took ~115 us against 109 / 160 us for
-// 4 / 6 tokens on the split-KV kernels.
-constexpr int64_t kTcMinColumns = 40;
+// Verify windows of 17 to 64 query columns per KV head (tokens x query heads
+// per KV head) on bf16 split pools run on the key-major tensor-memory kernel
+// (keys as the MMA's M, the columns zero-padded to an N of 32 or 64): one CTA
+// per (partition, KV head, row) streams the keys once.  At 40,002 keys (head
+// dim 512, 8 query heads per KV head) 3 / 4 / 5 / 8 tokens took 78 / 80 / 94 /
+// 98 us there against ~108 / 108 / 160 / 117 us on the split-KV or
+// query-major kernels; 2 tokens (16 columns) stay on the split-KV kernels
+// (61 us against 76).  Wider windows run on the query-major kernel, whose
+// blocks of 128 columns cost the same whatever their real columns.
+constexpr int64_t kVerifyMinColumns = 17;
+constexpr int64_t kVerifyMaxColumns = 64;
+constexpr int64_t kTcMinColumns = kVerifyMaxColumns + 1;
 
 // The query side of a call: a uniform number of tokens per row (single-token
 // decode, verify windows), or variable-length chunks given by row offsets
@@ -119,19 +125,23 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const bool varlen = qs.cu_q_host != nullptr;
   if (varlen && !qs.cu_q) return PSKV_ERR_INVALID_ARG;
   // Prefill of bf16 split pools at head dim 256 or 512 runs on the
-  // tensor-memory kernel: blocks of 128 query columns (any power-of-two group
-  // up to 128 query heads per KV head), one CTA (head dim 512: a CTA pair)
-  // per block and partition; so do verify windows of at least
-  // kTcMinColumns query columns per KV head.
-  const bool many_rows =
-      varlen || (!windowed && qs.tokens >= 2 && (int64_t)qs.tokens * group >= kTcMinColumns);
-  const bool tc_path = many_rows && !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
-                       d.head_dim_k == d.head_dim_v &&
-                       (d.head_dim_v == 256 || d.head_dim_v == 512) && group <= 128 &&
-                       (group & (group - 1)) == 0 && aligned(d.k_pool, 16) &&
-                       aligned(d.v_pool, 16) &&
-                       (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
-  if (kernel < 0 && !tc_path) return PSKV_ERR_UNSUPPORTED;
+  // query-major tensor-memory kernel: blocks of 128 query columns (any
+  // power-of-two group up to 128 query heads per KV head), one CTA (head dim
+  // 512: a CTA pair) per block and partition; so do verify windows of at
+  // least kTcMinColumns query columns per KV head, and narrower ones from
+  // kVerifyMinColumns on run on the key-major kernel.
+  const bool tc_pools = !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
+                        d.head_dim_k == d.head_dim_v &&
+                        (d.head_dim_v == 256 || d.head_dim_v == 512) && group <= 128 &&
+                        (group & (group - 1)) == 0 && aligned(d.k_pool, 16) &&
+                        aligned(d.v_pool, 16) &&
+                        (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
+  const int64_t window_cols = (int64_t)qs.tokens * group;
+  const bool verify_tc = tc_pools && !varlen && !windowed && qs.tokens >= 2 &&
+                         window_cols >= kVerifyMinColumns && window_cols <= kVerifyMaxColumns;
+  const bool many_rows = varlen || (!windowed && qs.tokens >= 2 && window_cols >= kTcMinColumns);
+  const bool tc_path = many_rows && tc_pools;
+  if (kernel < 0 && !tc_path && !verify_tc) return PSKV_ERR_UNSUPPORTED;
   const bool append = opts && opts->append_k;
   if (append) {
     if (!opts->append_v || !opts->append_pages) return PSKV_ERR_INVALID_ARG;
@@ -160,7 +170,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   // Query columns per KV head (heads x tokens): one n-tile of 8 when they fit,
   // else blocks of two n-tiles, one CTA per block (several tokens only on the
   // tensor-core family).
-  if ((max_t > 1 || varlen) && !tc_path && (kernel != kKernelMma || windowed))
+  if ((max_t > 1 || varlen) && !tc_path && !verify_tc && (kernel != kKernelMma || windowed))
     return PSKV_ERR_UNSUPPORTED;
   const int64_t columns = group * max_t;
   const int nt = columns > 8 ? 2 : 1;
@@ -173,7 +183,13 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const int64_t tc_qblocks = (columns + 127) / 128;
   if (tc_path && tc_qblocks * PSKV_MAX_SPLITS > INT32_MAX) return PSKV_ERR_INVALID_ARG;
   int P = num_splits;
-  if (P == 0 && tc_path) {
+  if (P == 0 && verify_tc) {
+    int n_sm = 0;
+    if ((rc = sm_count(&n_sm))) return rc;
+    int64_t max_len = 1;
+    for (int32_t b = 0; b < batch; ++b) max_len = seq_lens_host[b] > max_len ? seq_lens_host[b] : max_len;
+    P = plan_verify_splits((int64_t)d.num_kv_heads * batch, n_sm, (max_len + 127) / 128);
+  } else if (P == 0 && tc_path) {
     int n_sm = 0;
     if ((rc = sm_count(&n_sm))) return rc;
     int64_t max_len = 1;
@@ -190,7 +206,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
                     bytes_bound ? kFillBytes32 : 32);
   }
   // one partition on the tensor-core kernels: the partial is the output
-  const bool direct = P == 1 && (kernel == kKernelMma || tc_path);
+  const bool direct = P == 1 && (kernel == kKernelMma || tc_path || verify_tc);
   WorkspacePlan w;
   if ((rc = plan_workspace(rows, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
@@ -237,7 +253,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts->partial_begin), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (tc_path) {
+  if (tc_path || verify_tc) {
     TcArgs t;
     t.q = q;
     t.page_tables = page_tables;
@@ -258,13 +274,17 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     t.num_q_heads = num_q_heads;
     t.group_shift = __builtin_ctz((unsigned)group);
     t.num_splits = P;
-    t.qblocks = (int)tc_qblocks;
+    t.qblocks = verify_tc ? 1 : (int)tc_qblocks;
     t.total_rows = (int)rows;
     t.window = qs.window;
     t.box_rows = d.page_size % 64 == 0 ? 64 : 16;
     t.scale_log2 = scale * kLog2e;
-    e = launch_attn_tc(t, d.k_pool, d.v_pool, d.head_dim_v,
-                       dim3((unsigned)(tc_qblocks * P), d.num_kv_heads, batch), s);
+    if (verify_tc)
+      e = launch_attn_verify(t, d.k_pool, d.v_pool, d.head_dim_v,
+                             dim3((unsigned)P, d.num_kv_heads, batch), s);
+    else
+      e = launch_attn_tc(t, d.k_pool, d.v_pool, d.head_dim_v,
+                         dim3((unsigned)(tc_qblocks * P), d.num_kv_heads, batch), s);
   } else if (kernel == kKernelMma)
     e = launch_partial_mma(a, d.head_dim_v, group, folded, nt, grid, s);
   else if (d.kv_dtype == PSKV_DTYPE_F32)

@@ -125,4 +125,12 @@ int plan_tc_splits(int64_t units, int slots, int64_t max_tiles) {
   return (int)(p < cap ? p : cap);
 }
 
+int plan_verify_splits(int64_t units, int slots, int64_t max_tiles) {
+  if (units < 1 || slots < 1 || units >= slots) return 1;
+  int64_t p = slots / units;
+  const int64_t cap = max_tiles / 2 < PSKV_MAX_SPLITS ? max_tiles / 2 : PSKV_MAX_SPLITS;
+  if (p > cap) p = cap;
+  return p < 1 ? 1 : (int)p;
+}
+
 }  // namespace pskv

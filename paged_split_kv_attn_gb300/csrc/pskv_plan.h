@@ -53,6 +53,11 @@ constexpr int kFillBytes32 = 27;
 // of blocks, P = 1 (a block's fixed costs and the merge outweigh balancing the
 // last wave).
 int plan_tc_splits(int64_t units, int slots, int64_t max_tiles);
+// Partitions per (row, KV head) for the key-major verify kernel: `units`
+// (KV heads x rows) CTAs per partition over `slots` SMs, rows of at most
+// max_tiles 128-key tiles.  One wave: P = floor(slots / units), at least 1,
+// at most max_tiles / 2 (two tiles per partition) and PSKV_MAX_SPLITS.
+int plan_verify_splits(int64_t units, int slots, int64_t max_tiles);
 int plan_splits(int slots, int32_t batch, int32_t num_kv_heads, const int32_t *seq_lens_host,
                 int fill32 = 32);
 

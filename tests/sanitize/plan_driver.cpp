@@ -83,6 +83,13 @@ int main() {
   CHECK(plan_tc_splits(5, 152, 100000) == 31); // ceil(152 / 5)
   CHECK(plan_tc_splits(2, 152, 100000) == 32); // capped at 32
   CHECK(plan_tc_splits(0, 152, 10) == 1);
+  CHECK(plan_verify_splits(4, 152, 313) == 38);   // one wave: floor(152 / 4)
+  CHECK(plan_verify_splits(5, 152, 313) == 30);   // 150 CTAs, not a second wave of 3
+  CHECK(plan_verify_splits(4, 152, 20) == 10);    // two tiles per partition at least
+  CHECK(plan_verify_splits(4, 152, 1) == 1);
+  CHECK(plan_verify_splits(152, 152, 313) == 1);
+  CHECK(plan_verify_splits(1, 152, 100000) == 152);
+  CHECK(plan_verify_splits(0, 152, 10) == 1);
 
   std::vector<int32_t> rows = {0, 1}, pos = {3, 600}, lease = {1, 2};
   CHECK(check_append_host(&lay, 2, 4, 2, rows.data(), pos.data(), lease.data()) ==
