@@ -81,18 +81,24 @@ enum : int {
 };
 
 // Shared memory and tensor memory of head dim DT and NC query columns per CTA
-// (offsets from a 1,024-byte aligned base).  P^T is K-major: row n holds
-// column n's weights of 64 keys per 128-byte slab, two slabs per tile.
+// (offsets from a 1,024-byte aligned base).  A P^T buffer is K-major with 2 NC
+// rows: row n holds column n's hi weights, row NC + n its lo weights, 64 keys
+// per 128-byte slab, two slabs per tile.  Where tensor memory allows, one value
+// product of N = 2 NC takes both halves (O^T keeps a hi and a lo block of NC
+// columns each, summed at the end), so V is read once per tile.
 template <int DT, int NC>
 struct VLay {
   static constexpr int kChunks = DT / 128;    // chunks per K or V tile
   static constexpr int kQSlab = NC * 128;     // 64 head-dim columns of Q (or 64 keys of P^T)
   static constexpr int kQBytes = (DT / 64) * kQSlab;
-  static constexpr int kPlane = 2 * kQSlab;   // P^T hi or lo of a tile
-  static constexpr int kPBufs = DT == 512 && NC == 64 ? 1 : 2;  // P^T buffers (hi + lo each)
+  static constexpr int kPSlab = 2 * NC * 128;  // 64 keys of the hi and lo rows
+  static constexpr int kPBuf = 2 * kPSlab;     // a tile's P^T
+  static constexpr int kPBufs = DT == 512 && NC == 64 ? 1 : 2;  // P^T buffers
+  static constexpr bool kMerged = !(DT == 512 && NC == 64);     // one value product of 2 NC
+  static constexpr int kOBlock = kMerged ? 2 * NC : NC;         // O^T columns per block
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kOffQ + kQBytes;
-  static constexpr int kOffK = kOffP + kPBufs * 2 * kPlane;
+  static constexpr int kOffK = kOffP + kPBufs * kPBuf;
   static constexpr int kRingK = 2;  // K stages (the score products take them at once)
   static constexpr int kRingV = (kDataBytes - kOffK) / kChunkBytes - kRingK;  // V stages
   static constexpr int kOffV = kOffK + kRingK * kChunkBytes;
@@ -107,6 +113,7 @@ struct VLay {
   static constexpr int kOffA = kOffM + NC * 4;             // float[NC]: rescale factor, then sum
   static constexpr int kOffFlag = kOffA + NC * 4;          // int[2][4] votes, int[4] rescale
   static constexpr int kOffSlot = kOffFlag + 16 * 4;
+  static constexpr int kOffCOff = kOffP;  // size_t[NC] output row offsets, once P^T is done
   static constexpr int kOffAbort = kOffSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment of the dynamic base
   static_assert(kRingV >= 2 && kOffBar <= kDataBytes, "stages");
@@ -114,10 +121,10 @@ struct VLay {
   static_assert(kOffRed % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0, "16-byte reads");
   // tensor memory: S^T regions, O^T blocks, then the per-row shares of the sums
   static constexpr int kOCol = 2 * NC;
-  static constexpr int kLCol = kOCol + NC * kChunks;
+  static constexpr int kLCol = kOCol + kOBlock * kChunks;
   static_assert(kLCol + NC <= kTmemCols, "tensor memory");
   static constexpr uint32_t kIdescS = tc::instr_desc(kKeys, NC, false, false);
-  static constexpr uint32_t kIdescPV = tc::instr_desc(128, NC, true, false);
+  static constexpr uint32_t kIdescPV = tc::instr_desc(128, kOBlock, true, false);
 };
 
 // What a copy warp found for a tile: rows [vlo, vhi) lie in the CTA's keys;
@@ -335,7 +342,7 @@ struct PVIssuer {
     for (int j = 0; j < n; ++j) {
       const int pb = j % L::kPBufs;
       if (!wait(kPFull + pb, (j / L::kPBufs) & 1)) return false;
-      const uint32_t p0 = smem_u32(sm + L::kOffP + pb * 2 * L::kPlane);
+      const uint32_t p0 = smem_u32(sm + L::kOffP + pb * L::kPBuf);
       uint32_t live = 0;  // 16-key groups that meet the values
       bool ragged_lo = false, ragged_hi = false;
       int vlo = 0, vhi = 0;
@@ -374,16 +381,21 @@ struct PVIssuer {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             if (!((live >> kk) & 1u)) continue;
-            // A = V^T (128 head-dim columns x 16 keys, MN-major), B = P^T (NC columns x 16
-            // keys, K-major)
+            // A = V^T (128 head-dim columns x 16 keys, MN-major), B = P^T (the hi and lo
+            // rows x 16 keys, K-major): one product of 2 NC rows, or hi then lo
             const uint64_t da = tc::smem_desc(v0 + kk * 2048, kSlab, 1024);
+            const uint32_t pk = p0 + (kk >> 2) * L::kPSlab + (kk & 3) * 32;
+            if (L::kMerged) {
+              tc::mma(tmem + L::kOCol + L::kOBlock * c, da, tc::smem_desc(pk, 16, 1024),
+                      L::kIdescPV, !first);
+            } else {
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint64_t db = tc::smem_desc(
-                  p0 + part * L::kPlane + (kk >> 2) * L::kQSlab + (kk & 3) * 32, 16, 1024);
-              tc::mma(tmem + L::kOCol + NC * c, da, db, L::kIdescPV, !first);
-              first = false;
+              for (int part = 0; part < 2; ++part)
+                tc::mma(tmem + L::kOCol + L::kOBlock * c,
+                        da, tc::smem_desc(pk + part * NC * 128, 16, 1024), L::kIdescPV,
+                        !first || part > 0);
             }
+            first = false;
           }
           tc::commit(bars + L::kEmptyV + st);
         }
@@ -492,7 +504,7 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
   const int lim0 = pl.len - pl.T + 1;  // token t sees the keys below lim0 + t
   // this thread's key in P^T's K-major rows: slab, then the 2-byte slot inside the
   // row's swizzled 16-byte chunk (the chunk index is XORed with the row's low bits)
-  const int p_slab = (kr >> 6) * L::kQSlab, p_chunk = (kr & 63) >> 3, p_byte = 2 * (kr & 7);
+  const int p_slab = (kr >> 6) * L::kPSlab, p_chunk = (kr & 63) >> 3, p_byte = 2 * (kr & 7);
   auto wait_all = [&](int slot, uint32_t parity) {
     return warp_wait(bars + slot, parity, abort_flag, a.status);
   };
@@ -582,20 +594,19 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
       } else {
         if (!wait_all(kPvDone + (j - 1) % L::kPBufs, ((j - 1) / L::kPBufs) & 1)) return false;
         tc::fence_after_sync();
+        // the O^T blocks (hi and lo halves), then the sums: column q of them belongs to
+        // query column q % NC
 #pragma unroll 1
-        for (int blk = 0; blk <= L::kChunks; ++blk) {  // the O^T blocks, then the sums
-#pragma unroll 1
-          for (int h = 0; h < NC / 32; ++h) {
-            uint32_t v[32];
-            const uint32_t addr = lane_base + L::kOCol + NC * blk + 32 * h;
-            tc::ld32(addr, v);
-            tc::wait_ld();
-            tc::reg_fence(v);
+        for (int g = 0; g < (L::kOBlock * L::kChunks + NC) / 32; ++g) {
+          uint32_t v[32];
+          const uint32_t addr = lane_base + L::kOCol + 32 * g;
+          const float *al = a_sm + (32 * g) % NC;
+          tc::ld32(addr, v);
+          tc::wait_ld();
+          tc::reg_fence(v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              v[c] = __float_as_uint(__uint_as_float(v[c]) * a_sm[32 * h + c]);
-            tc::st32(addr, v);
-          }
+          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * al[c]);
+          tc::st32(addr, v);
         }
       }
       tc::wait_st();
@@ -607,7 +618,7 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
     if (j >= L::kPBufs &&
         !wait_all(kPvDone + pb, ((j - L::kPBufs) / L::kPBufs) & 1))
       return false;
-    unsigned char *ph_hi = sm + L::kOffP + pb * 2 * L::kPlane + p_slab + p_byte;
+    unsigned char *ph_hi = sm + L::kOffP + pb * L::kPBuf + p_slab + p_byte;
 #pragma unroll
     for (int h = 0; h < NC / 32; ++h) {
       uint32_t lv[32];
@@ -625,7 +636,7 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
         const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
         unsigned char *at = ph_hi + n * 128 + ((p_chunk ^ (n & 7)) << 4);
         *reinterpret_cast<__nv_bfloat16 *>(at) = hi;
-        *reinterpret_cast<__nv_bfloat16 *>(at + L::kPlane) = lo;
+        *reinterpret_cast<__nv_bfloat16 *>(at + NC * 128) = lo;  // row NC + n
       }
       tc::st32(laddr, lv);
     }
@@ -638,58 +649,17 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
   return true;
 }
 
-// Write the CTA's columns: O / sum to `out` (direct) or the partial (m, l, o).
-// Thread kr holds head-dim row kr of every O^T block; a warp's 32 lanes write
-// 32 consecutive head-dim columns of one query column.  With `have_o` false
-// (no tile) every column is empty and only m and l (or zeros) are written.
+// The (m, l) of the CTA's columns (partial), or the empty-row flag (direct).
 template <int DT, int NC>
-__device__ __forceinline__ void write_cols(const TcArgs &a, const VPlan &pl, unsigned char *sm,
-                                           uint32_t tmem, bool have_o) {
+__device__ __forceinline__ void write_ml(const TcArgs &a, const VPlan &pl, const unsigned char *sm,
+                                         bool have_o) {
   using L = VLay<DT, NC>;
-  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, kr = 32 * w + lane;
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * w) << 16);
-  const float *m_sm = reinterpret_cast<const float *>(sm + L::kOffM);
-  const float *l_sm = reinterpret_cast<const float *>(sm + L::kOffA);      // column sums
-  const float *inv_sm = reinterpret_cast<const float *>(sm + L::kOffRed);  // 1 / sum, or 0
-  const int gmask = (1 << a.group_shift) - 1;
-#pragma unroll 1
-  for (int blk = 0; blk < L::kChunks; ++blk) {
-#pragma unroll 1
-    for (int h = 0; h < NC / 32; ++h) {
-      uint32_t v[32];
-      if (have_o) {
-        tc::ld32(lane_base + L::kOCol + NC * blk + 32 * h, v);
-        tc::wait_ld();
-        tc::reg_fence(v);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = 0u;
-      }
-      const int dim = 128 * blk + kr;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int col = 32 * h + c;
-        if (col >= pl.ncols) break;
-        const size_t qrow = (size_t)(pl.r0 + (col >> a.group_shift)) * a.num_q_heads +
-                            (pl.g << a.group_shift) + (col & gmask);
-        // a column that met no key holds no value product (its O may never have been written)
-        const bool seen = have_o && m_sm[col] != -CUDART_INF_F;
-        const float o = seen ? __uint_as_float(v[c]) : 0.f;
-        if (a.direct) {
-          const float y = o * (seen ? inv_sm[col] : 0.f);
-          if (a.out_dtype == PSKV_DTYPE_BF16)
-            static_cast<__nv_bfloat16 *>(a.out)[qrow * DT + dim] = __float2bfloat16_rn(y);
-          else
-            static_cast<float *>(a.out)[qrow * DT + dim] = y;
-        } else if (have_o) {
-          a.ws_o[(qrow * a.num_splits + pl.p) * DT + dim] = o;
-        }
-      }
-    }
-  }
+  const int kr = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31);
   if (kr >= pl.ncols) return;
+  const float *m_sm = reinterpret_cast<const float *>(sm + L::kOffM);
+  const float *l_sm = reinterpret_cast<const float *>(sm + L::kOffA);  // column sums
   const size_t qrow = (size_t)(pl.r0 + (kr >> a.group_shift)) * a.num_q_heads +
-                      (pl.g << a.group_shift) + (kr & gmask);
+                      (pl.g << a.group_shift) + (kr & ((1 << a.group_shift) - 1));
   const bool empty = !have_o || m_sm[kr] == -CUDART_INF_F;
   if (a.direct) {
     if (empty) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
@@ -698,6 +668,94 @@ __device__ __forceinline__ void write_cols(const TcArgs &a, const VPlan &pl, uns
     a.ws_m[prow] = empty ? -CUDART_INF_F : m_sm[kr] * kLn2;
     a.ws_l[prow] = empty ? 0.f : l_sm[kr];
   }
+}
+
+// Output row of query column c (direct: [rows][Hq][DT]) or partial row
+// ([rows][Hq][P][DT]), in elements.
+__device__ __forceinline__ size_t col_offset(const TcArgs &a, const VPlan &pl, int c, int dt) {
+  const size_t qrow = (size_t)(pl.r0 + (c >> a.group_shift)) * a.num_q_heads +
+                      (pl.g << a.group_shift) + (c & ((1 << a.group_shift) - 1));
+  return (a.direct ? qrow : qrow * a.num_splits + pl.p) * dt;
+}
+
+// A partition with no tile: the empty state (partial), or zeros flagged as
+// empty rows (direct).
+template <int DT, int NC>
+__device__ __forceinline__ void write_empty(const TcArgs &a, const VPlan &pl,
+                                            const unsigned char *sm) {
+  const int kr = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31);
+  if (a.direct) {
+    for (int e = kr; e < pl.ncols * (DT / 4); e += 128) {
+      const int c = e / (DT / 4), q = e % (DT / 4);
+      const size_t off = col_offset(a, pl, c, DT) + 4 * q;
+      if (a.out_dtype == PSKV_DTYPE_BF16)
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) + off) = make_uint2(0, 0);
+      else
+        *reinterpret_cast<float4 *>(static_cast<float *>(a.out) + off) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  write_ml<DT, NC>(a, pl, sm, false);
+}
+
+// Write the CTA's columns: O / sum to `out` (direct) or the partial (m, l, o).
+// Thread kr holds head-dim row kr of every O^T block: it first puts its rows,
+// scaled per column (1 / sum direct, 1 partial, 0 for a column that met no
+// key), into a [column][head dim] f32 block of the (drained) K/V rings; after
+// the softmax warps meet, every thread writes 16-byte pieces of whole rows.
+template <int DT, int NC>
+__device__ __forceinline__ bool write_cols(const TcArgs &a, const VPlan &pl, unsigned char *sm,
+                                           uint64_t *bars, uint32_t tmem, int &ph,
+                                           volatile int *abort_flag) {
+  using L = VLay<DT, NC>;
+  static_assert(NC * DT * 4 <= L::kRingK * kChunkBytes + L::kRingV * kChunkBytes, "staging");
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, kr = 32 * w + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * w) << 16);
+  const float *scale = reinterpret_cast<const float *>(sm + L::kOffRed) + NC;
+  float *stage = reinterpret_cast<float *>(sm + L::kOffK);
+#pragma unroll 1
+  for (int blk = 0; blk < L::kChunks; ++blk) {
+#pragma unroll 1
+    for (int h = 0; h < NC / 32; ++h) {
+      // both loads in flight before the one wait
+      uint32_t v[32], u[32];
+      const uint32_t addr = lane_base + L::kOCol + L::kOBlock * blk + 32 * h;
+      tc::ld32(addr, v);
+      if (L::kMerged) tc::ld32(addr + NC, u);  // O = the hi products + the lo products
+      tc::wait_ld();
+      tc::reg_fence(v);
+      if (L::kMerged) {
+        tc::reg_fence(u);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          v[c] = __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(u[c]));
+      }
+      const int dim = 128 * blk + kr;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int col = 32 * h + c;
+        // (a column that met no key may hold no value product at all: scale 0 by selection)
+        const float sc = scale[col];
+        stage[col * DT + dim] = sc == 0.f ? 0.f : __uint_as_float(v[c]) * sc;
+      }
+    }
+  }
+  if (!meet(bars, ph, abort_flag, a.status)) return false;
+  const size_t *coff = reinterpret_cast<const size_t *>(sm + L::kOffCOff);
+  for (int e = kr; e < pl.ncols * (DT / 4); e += 128) {
+    const int c = e / (DT / 4), q = e % (DT / 4);
+    const float4 y = *reinterpret_cast<const float4 *>(stage + c * DT + 4 * q);
+    const size_t off = coff[c] + 4 * q;
+    if (!a.direct)
+      *reinterpret_cast<float4 *>(a.ws_o + off) = y;
+    else if (a.out_dtype == PSKV_DTYPE_BF16)
+      *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) + off) =
+          make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+    else
+      *reinterpret_cast<float4 *>(static_cast<float *>(a.out) + off) = y;
+  }
+  write_ml<DT, NC>(a, pl, sm, true);
+  return true;
 }
 
 }  // namespace
@@ -724,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const VPlan pl = make_plan(a);
   if (!pl.ok && threadIdx.x == 64) raise_fault(a.status, PSKV_FAULT_BAD_LENGTH);
   if (pl.n <= 0) {  // a partition past the row's keys: the empty state
-    if (warp >= 2 && warp < 6) write_cols<DT, NC>(a, pl, sm, 0u, false);
+    if (warp >= 2 && warp < 6) write_empty<DT, NC>(a, pl, sm);
     return;
   }
 
@@ -807,13 +865,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < NC / 32; ++i) red[NC * (warp & 3) + (NC / 32) * lane + i] = sum[i];
       ok = meet(bars, ph, abort_flag, a.status);
     }
+    // column sums and output scales (the folds are read before the meet below)
+    float t = 0.f;
+    if (ok && kr < NC) t = (red[kr] + red[NC + kr]) + (red[2 * NC + kr] + red[3 * NC + kr]);
+    ok = ok && meet(bars, ph, abort_flag, a.status);
     if (ok && kr < NC) {
-      const float t = (red[kr] + red[NC + kr]) + (red[2 * NC + kr] + red[3 * NC + kr]);
       a_sm[kr] = t;
-      red[kr] = t > 0.f ? 1.f / t : 0.f;
+      const bool seen = m_sm[kr] != -CUDART_INF_F;
+      red[NC + kr] = !seen ? 0.f : (a.direct ? (t > 0.f ? 1.f / t : 0.f) : 1.f);
+      reinterpret_cast<size_t *>(sm + L::kOffCOff)[kr] = col_offset(a, pl, kr, DT);
     }
     ok = ok && meet(bars, ph, abort_flag, a.status);
-    if (ok) write_cols<DT, NC>(a, pl, sm, tmem, true);
+    if (ok) write_cols<DT, NC>(a, pl, sm, bars, tmem, ph, abort_flag);
   }
   tc::fence_before_sync();
   __syncthreads();
