@@ -624,12 +624,23 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
       uint32_t lv[32];
       const uint32_t laddr = lane_base + L::kLCol + 32 * h;
       tc::ld32(laddr, lv);
+      // the reference maxima in registers first (read between the P stores below,
+      // each would wait for the store before it)
+      float mr[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 m4 = *reinterpret_cast<const float4 *>(m_sm + 32 * h + c);
+        mr[c] = m4.x;
+        mr[c + 1] = m4.y;
+        mr[c + 2] = m4.z;
+        mr[c + 3] = m4.w;
+      }
       tc::wait_ld();
       tc::reg_fence(lv);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const int n = 32 * h + c;
-        const float mc = m_sm[n];
+        const float mc = mr[c];
         const float p = ex2(x[n] - (mc == -CUDART_INF_F ? 0.f : mc));
         lv[c] = __float_as_uint(__uint_as_float(lv[c]) + p);
         const __nv_bfloat16 hi = __float2bfloat16_rn(p);
@@ -731,17 +742,27 @@ __device__ __forceinline__ bool write_cols(const TcArgs &a, const VPlan &pl, uns
           v[c] = __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(u[c]));
       }
       const int dim = 128 * blk + kr;
+      // the scales in registers first: read between the stores below, each would
+      // wait for the store before it (the compiler cannot tell them apart)
+      float sc[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(scale + 32 * h + c);
+        sc[c] = s4.x;
+        sc[c + 1] = s4.y;
+        sc[c + 2] = s4.z;
+        sc[c + 3] = s4.w;
+      }
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int col = 32 * h + c;
         // (a column that met no key may hold no value product at all: scale 0 by selection)
-        const float sc = scale[col];
-        stage[col * DT + dim] = sc == 0.f ? 0.f : __uint_as_float(v[c]) * sc;
+        stage[(32 * h + c) * DT + dim] = sc[c] == 0.f ? 0.f : __uint_as_float(v[c]) * sc[c];
       }
     }
   }
   if (!meet(bars, ph, abort_flag, a.status)) return false;
   const size_t *coff = reinterpret_cast<const size_t *>(sm + L::kOffCOff);
+#pragma unroll 4
   for (int e = kr; e < pl.ncols * (DT / 4); e += 128) {
     const int c = e / (DT / 4), q = e % (DT / 4);
     const float4 y = *reinterpret_cast<const float4 *>(stage + c * DT + 4 * q);
