@@ -81,16 +81,27 @@ constexpr int kMaxGroups = 64;
 
 // Verify windows of 17 to 64 query columns per KV head (tokens x query heads
 // per KV head) on bf16 split pools run on the key-major tensor-memory kernel
-// (keys as the MMA's M, the columns zero-padded to an N of 32 or 64): one CTA
-// per (partition, KV head, row) streams the keys once.  At 40,002 keys (head
-// dim 512, 8 query heads per KV head) 3 / 4 / 5 / 8 tokens took 78 / 80 / 94 /
-// 98 us there against ~108 / 108 / 160 / 117 us on the split-KV or
-// query-major kernels; 2 tokens (16 columns) stay on the split-KV kernels
-// (61 us against 76).  Wider windows run on the query-major kernel, whose
-// blocks of 128 columns cost the same whatever their real columns.
-constexpr int64_t kVerifyMinColumns = 17;
+// (keys as the MMA's M, the columns zero-padded to an N of 32 or 64) when the
+// longest row has at least kVerifyMinKeys keys: one CTA per (partition, KV
+// head, row) streams the keys once.  At 40,002 keys (head dim 512, 8 query
+// heads per KV head) 3 / 4 / 5 / 8 tokens took 74 / 75 / 89 / 91 us there
+// against ~108 / 108 / 160 / 117 us on the split-KV or query-major kernels, at
+// 20,000 keys 51 / 53 / 63 / 65 against 59 / 60 / 85 / 108 us, at 10,602 keys
+// 39 / 39 / 48 / 49 against 37 / 38 / 51 / 63 us; below that a CTA's first
+// tile (its K tile through two stages, then the softmax, then the values),
+// ~10 us, outweighs the few tiles behind it (4,096 keys: 29 / 29 / 34 / 35
+// against 23 / 22 / 27 / 32 us).  2 tokens (16 columns) stay on the split-KV
+// kernels (61 against 76 us at 40,002 keys).  Otherwise windows of at least
+// kTcMinColumns columns run on the query-major kernel, whose blocks of 128
+// columns cost the same whatever their real columns (at 40,002 keys ~115 us
+// against 109 / 160 us for 4 / 6 tokens on the split-KV kernels).
+#ifndef PSKV_VERIFY_MIN_COLUMNS
+#define PSKV_VERIFY_MIN_COLUMNS 17  // compile-time tuning knob (65 routes no window there)
+#endif
+constexpr int64_t kVerifyMinColumns = PSKV_VERIFY_MIN_COLUMNS;
 constexpr int64_t kVerifyMaxColumns = 64;
-constexpr int64_t kTcMinColumns = kVerifyMaxColumns + 1;
+constexpr int64_t kVerifyMinKeys = 8192;
+constexpr int64_t kTcMinColumns = 40;
 
 // The query side of a call: a uniform number of tokens per row (single-token
 // decode, verify windows), or variable-length chunks given by row offsets
@@ -128,8 +139,8 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   // query-major tensor-memory kernel: blocks of 128 query columns (any
   // power-of-two group up to 128 query heads per KV head), one CTA (head dim
   // 512: a CTA pair) per block and partition; so do verify windows of at
-  // least kTcMinColumns query columns per KV head, and narrower ones from
-  // kVerifyMinColumns on run on the key-major kernel.
+  // least kTcMinColumns query columns per KV head that the key-major kernel
+  // does not take.
   const bool tc_pools = !folded && d.kv_dtype == PSKV_DTYPE_BF16 &&
                         d.head_dim_k == d.head_dim_v &&
                         (d.head_dim_v == 256 || d.head_dim_v == 512) && group <= 128 &&
@@ -137,10 +148,14 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
                         aligned(d.v_pool, 16) &&
                         (int64_t)d.num_pages * d.num_kv_heads * d.page_size <= INT32_MAX;
   const int64_t window_cols = (int64_t)qs.tokens * group;
+  int64_t longest = 0;  // the host lengths (checked below); the routing only reads them
+  for (int32_t b = 0; b < batch; ++b)
+    longest = seq_lens_host[b] > longest ? seq_lens_host[b] : longest;
   const bool verify_tc = tc_pools && !varlen && !windowed && qs.tokens >= 2 &&
-                         window_cols >= kVerifyMinColumns && window_cols <= kVerifyMaxColumns;
+                         window_cols >= kVerifyMinColumns && window_cols <= kVerifyMaxColumns &&
+                         longest >= kVerifyMinKeys;
   const bool many_rows = varlen || (!windowed && qs.tokens >= 2 && window_cols >= kTcMinColumns);
-  const bool tc_path = many_rows && tc_pools;
+  const bool tc_path = many_rows && tc_pools && !verify_tc;
   if (kernel < 0 && !tc_path && !verify_tc) return PSKV_ERR_UNSUPPORTED;
   const bool append = opts && opts->append_k;
   if (append) {
