@@ -288,9 +288,10 @@ int decode_attn_windowed(const pskv_layout *layout, const void *q, const int32_t
  *               CTA when they fit in 8, else 16 per CTA, the CTAs of one
  *               partition reading the same keys (the later ones mostly from L2);
  *               on bf16 split pools of head dim 256 or 512, 17 to 64 columns
- *               by the key-major tensor-memory kernel (128 keys per tile as
- *               the MMA's M, the columns as its N, one CTA per partition
- *               streaming the keys once) and from 65 columns on by the
+ *               by the key-major tensor-memory kernel when the longest row
+ *               has at least 8,192 keys (128 keys per tile as the MMA's M,
+ *               the columns as its N, one CTA per partition streaming the
+ *               keys once), and otherwise from 40 columns on by the
  *               query-major tensor-memory kernel, 128 columns per CTA (pair)
  *   seq_lens    every length at least num_tokens
  *   workspace   decode_attn_workspace_bytes(batch * num_tokens, num_q_heads, ...)
