@@ -53,6 +53,7 @@ constexpr int kKVSlab = kKeys * 128;        // bytes of one 64-column slab of a 
 constexpr int kKVBytes = 4 * kKVSlab;       // 32 KB
 constexpr int kStages = 3;                  // most K or V stages (barrier and record slots)
 constexpr int kXBytes = kRows * kKeys * 4;  // one block of partial scores (32 KB)
+constexpr int kQSlab = kRows * 128;         // 64 columns of Q's 128 rows (16 KB)
 constexpr int kTmemCols = 512;
 constexpr int kQCol = 0;                    // Q: 256 bf16 = 128 columns
 constexpr int kSCol = 128;                  // score / P region r at kSCol + 64 r
@@ -78,7 +79,8 @@ enum : int {
   kXFull = kQReady + 1,           // [2] the peer's partial scores arrived (CTA pair)
   kXFree = kXFull + 2,            // [2] the peer read the partial scores sent to it
   kSReady = kXFree + 2,           // [2] the full scores of region r are in place (CTA pair)
-  kNumBars = kSReady + 2
+  kQFull = kSReady + 2,           // Q's tensor copy landed (head dim 256)
+  kNumBars = kQFull + 1
 };
 
 // Head dim 256: one CTA.  Head dim 512: a cluster of two CTAs, rank c holding
@@ -324,12 +326,13 @@ struct Loader {
     issued = j + 1;
   }
 
-  __device__ bool wait(int slot, uint32_t parity) {
-    return warp_wait(bars + slot, parity, abort_flag, a.status);
-  }
-
-  __device__ void prologue(bool is_v) {
-    for (int j = 0; j < (is_v ? L::kStagesV : L::kStagesK) && j < pl.n; ++j) load(j, is_v);
+  __device__ bool prologue(bool is_v) {
+    for (int j = 0; j < (is_v ? L::kStagesV : L::kStagesK) && j < pl.n; ++j) {
+      // (head dim 256: V stages 1 and 2 hold Q's tensor copy until Q is in tensor memory)
+      if (!kPair && is_v && j == 1 && !wait(kQReady, 0)) return false;
+      load(j, is_v);
+    }
+    return true;
   }
 
   __device__ bool run(bool is_v) {
@@ -345,6 +348,10 @@ struct Loader {
       load(j, is_v);
     }
     return true;
+  }
+
+  __device__ bool wait(int slot, uint32_t parity) {
+    return warp_wait(bars + slot, parity, abort_flag, a.status);
   }
 
   // Wait (bounded) for the last copy issued into each stage.
@@ -441,11 +448,37 @@ __device__ __forceinline__ size_t query_row(const TcArgs &a, const TcPlan &pl, i
   return ((size_t)pl.r0 + (*real ? t : 0)) * a.num_q_heads + h;
 }
 
-// Q into tensor memory: this thread's row (zeros past the chunk), 256 bf16 as
-// 128 columns of pairs.  All 32 loads are in flight before the first store.
+// Q into tensor memory: this thread's row, 256 bf16 as 128 columns of pairs.
+// Head dim 256 reads it from the block's tensor copy (rows past the chunk hold
+// other rows' queries or zeros, and see no key); the pair loads it row by row
+// (zeros past the chunk), all 32 loads in flight before the first store.
 template <bool kPair>
-__device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint32_t tmem, int col0) {
+__device__ __forceinline__ bool stage_q(const TcArgs &a, const TcPlan &pl, unsigned char *sm,
+                                        uint64_t *bars, uint32_t tmem, int col0,
+                                        volatile int *abort_flag) {
   const int w = (threadIdx.x >> 5) & 3, i = 32 * w + (threadIdx.x & 31);
+  const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
+  if constexpr (!kPair) {
+    // the block's 128 rows arrived by one tensor copy into V stages 1 and 2:
+    // four 64-column slabs of 128 rows, 128-byte swizzled
+    if (!warp_wait(bars + kQFull, 0, abort_flag, a.status)) return false;
+    const unsigned char *qs = sm + Lay<kPair>::kOffV + kKVBytes + i * 128;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t v[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(qs + b * kQSlab + ((c ^ (i & 7)) << 4));
+        v[4 * c] = x.x;
+        v[4 * c + 1] = x.y;
+        v[4 * c + 2] = x.z;
+        v[4 * c + 3] = x.w;
+      }
+      tc::st32(lane_base + kQCol + 32 * b, v);
+    }
+    tc::wait_st();
+    return true;
+  }
   bool real;
   const size_t qrow = query_row(a, pl, i, &real);
   const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
@@ -453,7 +486,6 @@ __device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint3
   uint4 q[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) q[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-  const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     uint32_t v[32];
@@ -467,6 +499,7 @@ __device__ __forceinline__ void stage_q(const TcArgs &a, const TcPlan &pl, uint3
     tc::st32(lane_base + kQCol + 32 * b, v);
   }
   tc::wait_st();
+  return true;
 }
 
 // Multiply this warp's rows of O in tensor memory by alpha (1 keeps a row).
@@ -770,7 +803,8 @@ __device__ __forceinline__ void write_empty(const TcArgs &a, const TcPlan &pl, i
 template <bool kPair>
 __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
     pskv_attn_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap) {
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap qmap) {
   using L = Lay<kPair>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -815,8 +849,18 @@ __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
       }
       mbar_init(&bars[kDrain], 1);
       mbar_init(&bars[kQReady], 4);
+      mbar_init(&bars[kQFull], 1);
       *abort_flag = 0;
       mbar_fence_init();
+      if (!kPair) {
+        // head dim 256: the block's Q rows (tokens t_first .., the KV group's heads) by
+        // one tensor copy of four 64-column slabs into V stages 1 and 2
+        const int t_first = (pl.qb * kRows) >> a.group_shift;
+        mbar_arrive_expect_tx(bars + kQFull, 4 * kQSlab);
+        for (int b = 0; b < 4; ++b)
+          tc::tma_load_3d(sm + L::kOffV + kKVBytes + b * kQSlab, &qmap, 64 * b,
+                          pl.g << a.group_shift, pl.r0 + t_first, bars + kQFull);
+      }
     }
     __syncwarp();
     ld.prologue(false);
@@ -835,8 +879,7 @@ __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
     is.drain();  // every MMA done before the memory is released
   } else if (warp == 1 || warp == 6) {
     const bool is_v = warp == 6;
-    if (is_v) ld.prologue(true);
-    ld.run(is_v);
+    if (!is_v || ld.prologue(true)) ld.run(is_v);
     ld.drain(is_v);  // every copy landed before the CTA leaves
   } else if (warp >= 7) {
     if constexpr (kPair) {
@@ -844,14 +887,14 @@ __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
       if (lane == 0) bulk_wait_read();  // no send still reads this CTA's memory
     }
   } else {
-    stage_q<kPair>(a, pl, tmem, col0);
+    const bool q_ok = stage_q<kPair>(a, pl, sm, bars, tmem, col0, abort_flag);
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + kQReady);
     RowState st;
     st.m = -CUDART_INF_F;
     st.l = 0.f;
-    if (softmax_loop<kPair>(a, pl, sm, bars, info, tmem, abort_flag, st, rank)) {
+    if (q_ok && softmax_loop<kPair>(a, pl, sm, bars, info, tmem, abort_flag, st, rank)) {
       // PV(n - 1); PV(n - 3) is known done, as S(n - 1) waited for it
       const bool ok =
           tc_wait(bars + kPvDone + ((pl.n - 1) & 1), ((pl.n - 1) >> 1) & 1, abort_flag, a.status);
@@ -888,9 +931,11 @@ cudaError_t launch_tc(const TcArgs &a, const void *k_pool, const void *v_pool, d
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const long long rows = a.num_pages * a.num_kv_heads * a.page_size;
-  CUtensorMap km, vm;
+  const int group = 1 << a.group_shift;
+  CUtensorMap km, vm, qm;
   if (!make_map(&km, k_pool, rows, L::kDT, a.box_rows) ||
-      !make_map(&vm, v_pool, rows, L::kDT, a.box_rows))
+      !make_map(&vm, v_pool, rows, L::kDT, a.box_rows) ||
+      !tc::make_q_map(&qm, a.q, a.total_rows, a.num_q_heads, L::kDT, group, kRows / group))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -906,7 +951,7 @@ cudaError_t launch_tc(const TcArgs &a, const void *k_pool, const void *v_pool, d
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = kPair ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, pskv_attn_tc_kernel<kPair>, a, km, vm);
+  return cudaLaunchKernelEx(&cfg, pskv_attn_tc_kernel<kPair>, a, km, vm, qm);
 }
 
 }  // namespace

@@ -87,5 +87,21 @@ inline bool make_map(CUtensorMap *m, const void *region, long long rows, int dt,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Queries [rows][heads][dt] bf16 as a 3-D tensor read in boxes of 64 columns x
+// `heads_box` heads x `rows_box` rows (128-byte swizzled): a box holds the
+// query columns (row, head) of one KV group in row-major order.
+inline bool make_q_map(CUtensorMap *m, const void *q, long long rows, int heads, int dt,
+                       int heads_box, int rows_box) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)dt, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)dt * 2, (cuuint64_t)heads * dt * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)heads_box, (cuuint32_t)rows_box};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 }  // namespace pskv
