@@ -5,38 +5,41 @@
 // Serves decode_attn_multirow (TensorFold #1619, description "Reads" and the
 // review thread: drafted verify windows and tree-attention rows read their keys
 // through the page table) when a KV head's query columns (tokens x the query
-// heads of the KV head) number 16 to 64.  A block of 64 columns (zero-padded)
-// is too narrow for the query-major kernel's M of 128, and at head dim 512
-// that kernel needs a CTA pair exchanging partial scores; here the roles turn
-// around.  One CTA takes one (row, KV head, partition); per tile j of 128 keys:
-//   S^T = K Q^T        M = 128 keys, N = 64 columns, K = head dim
-//                      (A = the K tile, B = Q, both K-major in shared memory)
-//   softmax            one thread per key reads its 64 scores, masks them
-//                      (keys past the row, causality inside the window, pages
-//                      outside the pool) and checks them against each column's
-//                      reference max (exp2 units, moved only past a slack of 8,
-//                      as in the other kernels); when some column's max moves,
-//                      the four softmax warps reduce the tile's column maxima
-//                      and rescale that column's sums and O.  P^T goes to shared
-//                      memory as a bf16 hi + lo pair; each thread keeps its
-//                      keys' share of every column's sum until the end
-//   O^T += V^T P^T     per 128 head-dim columns: M = 128, N = 64, K = 128 keys
-//                      (A = the V tile read MN-major, B = P^T MN-major), hi
-//                      then lo
-// Tensor memory: S^T regions at columns [0, 64) and [64, 128) (tile j uses
-// region j % 2), O^T block c (head-dim columns [128 c, 128 c + 128) as lanes,
-// query columns as columns) at [128 + 64 c, 192 + 64 c), then 64 columns of
-// per-key-row shares of the column sums (lane = the tile row that gathered
-// them).  K and V tiles move in chunks of 128 keys x 128 head-dim columns
-// (32 KB), K and V each through a ring of its own: the score products take a
-// K chunk as soon as it lands (S of tile j + 1 overlaps tile j's softmax), the
-// value products take V chunks once P^T of their tile is written.  Warp 0
-// issues the score MMAs, warp 7 the value MMAs, warps 1 and 6 the K and V
-// copies; warps 2-5 stage Q and run the softmax and the epilogue (warp w owns
-// tensor-memory lanes 32 (w % 4) .. + 31).  The softmax warps meet on a
-// barrier of their own (bounded waits, like every wait here); on expiry the
-// CTA flags PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its
-// tensor memory.
+// heads of the KV head) number 17 to 64 and the rows are long.  Such a block is
+// too narrow for the query-major kernel's M of 128 (and at head dim 512 that
+// kernel needs a CTA pair exchanging partial scores); here the roles turn
+// around: the columns, zero-padded to NC = 32 or 64, are the MMA's N.  One CTA
+// takes one (row, KV head, partition of 16-key groups); per tile j of 128 keys:
+//   S^T = K Q^T        M = 128 keys, N = NC, K = head dim in chunks of 128
+//                      (A = the K chunk, B = Q, both K-major in shared memory)
+//   softmax            one thread per key reads its NC scores, masks them
+//                      (keys outside the CTA's range, causality inside the
+//                      window, pages outside the pool) and checks them against
+//                      each column's reference max (exp2 units, moved only past
+//                      a slack of 8, as in the other kernels); when some
+//                      column's max moves, the four softmax warps fold the
+//                      tile's column maxima and rescale that column's sums and
+//                      O.  P^T goes to shared memory as bf16 hi and lo rows of
+//                      one K-major operand; each thread keeps its key row's
+//                      share of every column's sum in tensor memory until the end
+//   O^T += V^T P^T     per 128 head-dim columns: M = 128, K = 128 keys in 16-key
+//                      steps, A = the V chunk read MN-major, B = the hi and lo
+//                      rows (one product of N = 2 NC, or hi then lo where
+//                      tensor memory holds only one O^T)
+// Tensor memory: two S^T regions of NC columns (tile j uses region j % 2), the
+// O^T blocks (head dim as lanes, query columns as columns; hi and lo halves),
+// then NC columns of per-key-row shares of the column sums.  K and V tiles move
+// in chunks of 128 keys x 128 head-dim columns (32 KB), each through a ring of
+// its own: the score products take a K chunk as soon as it lands (S of tile
+// j + 1 overlaps tile j's softmax), the value products take V chunks once P^T
+// of their tile is written (P^T double-buffered where shared memory allows).
+// Warp 0 issues the score MMAs, warp 7 the value MMAs, warps 1 and 6 the K and
+// V copies; warps 2-5 stage Q and run the softmax and the epilogue (warp w
+// owns tensor-memory lanes 32 (w % 4) .. + 31), which stages O through the
+// drained rings and writes whole rows.  The softmax warps meet on an mbarrier
+// of their own; every wait is bounded, and on expiry the CTA flags
+// PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its tensor
+// memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
