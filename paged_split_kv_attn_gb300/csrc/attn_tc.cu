@@ -79,7 +79,7 @@ enum : int {
   kXFull = kQReady + 1,           // [2] the peer's partial scores arrived (CTA pair)
   kXFree = kXFull + 2,            // [2] the peer read the partial scores sent to it
   kSReady = kXFree + 2,           // [2] the full scores of region r are in place (CTA pair)
-  kQFull = kSReady + 2,           // Q's tensor copy landed (head dim 256)
+  kQFull = kSReady + 2,           // Q's tensor copy landed
   kNumBars = kQFull + 1
 };
 
@@ -95,6 +95,9 @@ struct Lay {
   static constexpr int kStagesK = kPair ? 2 : 3;
   static constexpr int kStagesV = kPair ? 2 : 3;
   static constexpr int kOffV = kOffK + kStagesK * kKVBytes;  // V stage s at kOffV + s * kKVBytes
+  // the first of the two V stages that take Q's tensor copy at the start (the
+  // pair's V stages are all it has; head dim 256 keeps stage 0 for V(0))
+  static constexpr int kQStage = kPair ? 0 : 1;
   static constexpr int kOffX = kOffV + kStagesV * kKVBytes;  // received partial scores [2]
   static constexpr int kOffXs = kOffX + (kPair ? 2 * kXBytes : 0);  // partial scores to send
   static constexpr int kOffBar = kOffXs + (kPair ? kXBytes : 0);
@@ -328,8 +331,8 @@ struct Loader {
 
   __device__ bool prologue(bool is_v) {
     for (int j = 0; j < (is_v ? L::kStagesV : L::kStagesK) && j < pl.n; ++j) {
-      // (head dim 256: V stages 1 and 2 hold Q's tensor copy until Q is in tensor memory)
-      if (!kPair && is_v && j == 1 && !wait(kQReady, 0)) return false;
+      // (V stages kQStage and on hold Q's tensor copy until Q is in tensor memory)
+      if (is_v && j == L::kQStage && !wait(kQReady, 0)) return false;
       load(j, is_v);
     }
     return true;
@@ -448,21 +451,21 @@ __device__ __forceinline__ size_t query_row(const TcArgs &a, const TcPlan &pl, i
   return ((size_t)pl.r0 + (*real ? t : 0)) * a.num_q_heads + h;
 }
 
-// Q into tensor memory: this thread's row, 256 bf16 as 128 columns of pairs.
-// Head dim 256 reads it from the block's tensor copy (rows past the chunk hold
-// other rows' queries or zeros, and see no key); the pair loads it row by row
-// (zeros past the chunk), all 32 loads in flight before the first store.
+// Q into tensor memory: this thread's row (its CTA's 256 columns) as 128
+// columns of bf16 pairs, read from the block's tensor copy (rows past the
+// chunk hold other rows' queries or zeros, and see no key).
 template <bool kPair>
 __device__ __forceinline__ bool stage_q(const TcArgs &a, const TcPlan &pl, unsigned char *sm,
                                         uint64_t *bars, uint32_t tmem, int col0,
                                         volatile int *abort_flag) {
   const int w = (threadIdx.x >> 5) & 3, i = 32 * w + (threadIdx.x & 31);
   const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
-  if constexpr (!kPair) {
-    // the block's 128 rows arrived by one tensor copy into V stages 1 and 2:
-    // four 64-column slabs of 128 rows, 128-byte swizzled
+  {
+    // the block's 128 rows (this CTA's columns) arrived by one tensor copy into
+    // two V stages: four 64-column slabs of 128 rows, 128-byte swizzled
     if (!warp_wait(bars + kQFull, 0, abort_flag, a.status)) return false;
-    const unsigned char *qs = sm + Lay<kPair>::kOffV + kKVBytes + i * 128;
+    const unsigned char *qs =
+        sm + Lay<kPair>::kOffV + Lay<kPair>::kQStage * kKVBytes + i * 128;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       uint32_t v[32];
@@ -479,27 +482,6 @@ __device__ __forceinline__ bool stage_q(const TcArgs &a, const TcPlan &pl, unsig
     tc::wait_st();
     return true;
   }
-  bool real;
-  const size_t qrow = query_row(a, pl, i, &real);
-  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
-                                                     qrow * Lay<kPair>::kDT + col0);
-  uint4 q[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) q[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    uint32_t v[32];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      v[4 * c] = q[8 * b + c].x;
-      v[4 * c + 1] = q[8 * b + c].y;
-      v[4 * c + 2] = q[8 * b + c].z;
-      v[4 * c + 3] = q[8 * b + c].w;
-    }
-    tc::st32(lane_base + kQCol + 32 * b, v);
-  }
-  tc::wait_st();
-  return true;
 }
 
 // Multiply this warp's rows of O in tensor memory by alpha (1 keeps a row).
@@ -852,14 +834,15 @@ __global__ void __launch_bounds__(Lay<kPair>::kThreads, 1)
       mbar_init(&bars[kQFull], 1);
       *abort_flag = 0;
       mbar_fence_init();
-      if (!kPair) {
-        // head dim 256: the block's Q rows (tokens t_first .., the KV group's heads) by
-        // one tensor copy of four 64-column slabs into V stages 1 and 2
+      {
+        // the block's Q rows (tokens t_first .., the KV group's heads; this CTA's
+        // columns) by one tensor copy of four 64-column slabs into two V stages
         const int t_first = (pl.qb * kRows) >> a.group_shift;
         mbar_arrive_expect_tx(bars + kQFull, 4 * kQSlab);
         for (int b = 0; b < 4; ++b)
-          tc::tma_load_3d(sm + L::kOffV + kKVBytes + b * kQSlab, &qmap, 64 * b,
-                          pl.g << a.group_shift, pl.r0 + t_first, bars + kQFull);
+          tc::tma_load_3d(sm + L::kOffV + L::kQStage * kKVBytes + b * kQSlab, &qmap,
+                          col0 + 64 * b, pl.g << a.group_shift, pl.r0 + t_first,
+                          bars + kQFull);
       }
     }
     __syncwarp();
