@@ -98,7 +98,7 @@ __device__ __forceinline__ void combine_chunk(float4 &acc, const float4 (&v)[kCh
   }
 }
 
-// Both levels in one launch, one block per (row, 64 output columns).  Every
+// Both levels in one launch, one block per (row, 64 or 128 output columns).  Every
 // block computes the row's level-1 weights (warp w takes groups w, w + 4, ...)
 // and the level-2 weights over the group states; its threads fold, for their
 // column, each group of partials in index order into a shared-memory group
@@ -106,10 +106,11 @@ __device__ __forceinline__ void combine_chunk(float4 &acc, const float4 (&v)[kCh
 // in index order and normalises (level 2).  The group results never leave the
 // chip, and the arithmetic and its order are those of two separate levels.
 // The first group's numerators are loaded before any weight is known.
-constexpr int kColsPerBlock = 16;                              // float4 columns per block
-constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;     // threads per column
-
+// kCols float4 columns per block (16, or 32 when a row has at most 4 groups:
+// then no thread of the block idles), kMergeThreads / kCols threads per column.
+template <int kColsPerBlock>
 __global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
+  constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;  // threads per column
   __shared__ float w_s[PSKV_MAX_SPLITS];             // level-1 weights, by partial
   __shared__ float m_s[PSKV_MAX_SPLITS], l_s[PSKV_MAX_SPLITS];  // the row's partial (m, l)
   __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates], wg_s[kMaxStates];  // group states
@@ -195,9 +196,13 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
   *launches = 0;
   const int ng = (a.count + a.group - 1) / a.group;
   if (ng > kMaxStates || a.count > PSKV_MAX_SPLITS || a.group > kChunk) return cudaErrorInvalidValue;
-  const int chunks = (a.dv / 4 + kColsPerBlock - 1) / kColsPerBlock;
   *launches = 1;
-  return launch_pdl(pskv_merge_cols, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
+  if (ng <= kMergeThreads / 32) {  // every group lane busy with 32 columns per block
+    const int chunks = (a.dv / 4 + 31) / 32;
+    return launch_pdl(pskv_merge_cols<32>, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
+  }
+  const int chunks = (a.dv / 4 + 15) / 16;
+  return launch_pdl(pskv_merge_cols<16>, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
 }
 
 }  // namespace pskv
