@@ -3,26 +3,34 @@
 One step is one pass of the whole decode hot path over one batch of
 synthetic input, as a Gemma-4-31B-shaped decode step runs it:
   * the global-layer decode (32 query heads on 4 KV heads, head dim 512,
-    bf16 K/V in shuffled pages of 256) at the two contexts 10,602 and
-    40,002: append the step's new K/V row into its page, then the split-KV
-    partial kernel and the two-level merge;
+    bf16 K/V in shuffled pages of 256) at each of the contexts 10,602,
+    40,002, 81,653 and 163,336: the step's new K/V row is written into its
+    page by the decode's own partial kernel, which then computes the
+    split-KV partials, and the two-level merge combines them;
   * the sliding-window decode (32 query heads on 16 KV heads, head dim 256,
-    window 1,024, pages of 64, resident length window + one page): append,
-    then the windowed partial kernel and merge.
+    window 1,024, pages of 64, resident length window + one page), the
+    same way.
 value = algorithmic bytes (K and V of every attended key) / step time, GB/s.
 
 Timing: W untimed warm-up steps, then K steps between CUDA events on the
 launching stream, with a barrier and a device synchronize on both sides;
-consecutive steps read three rotating copies of the pools (433 MB of K/V a
-step, > 3x the 129 MB L2), so no call finds its data in L2.  The timed steps
-are replays of CUDA graphs captured once (one per pool copy) from the same
-library calls, as a decode engine runs its step; the eager (stream-launched)
-time of the same K steps is reported beside it.  The partial kernels'
+consecutive steps read three rotating copies of the pools (2.4 GB of K/V a
+step, far beyond the 129 MB L2), so no call finds its data in L2.  The timed
+steps are replays of CUDA graphs captured once (one per pool copy) from the
+same library calls, as a decode engine runs its step.  The partial kernels'
 durations for the roofline come from a further pass of K eager steps with
-CUDA events recorded around each partial launch.
+CUDA events recorded around each partial launch.  Per call (each call alone,
+replayed from its own graphs, a 256 MB read between calls so that L2 is
+cold): microseconds, GB/s, the fraction of 8 TB/s and of the measured copy
+bandwidth; the split count swept over 8..256 at every global context with
+the best one reported.  e2e: the same step through the library's C entry
+points (eager calls, no graphs), with each step's inputs copied in from
+pinned host memory and its outputs copied back inside the timed region.
 
---impl reference times the CPU oracle (the only reference there is: the
-pages ship no runnable code) on the same workload; see the design doc.
+--impl reference times the CPU oracle (an fp64 direct softmax over the
+paged pool, run on the host's cores) on the same workload: the pages this
+method comes from ship no runnable code, so the oracle is the only
+reference implementation there is.
 """
 from __future__ import annotations
 
@@ -44,7 +52,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "decode attn µs/call & effective HBM GB/s (% of 8 TB/s) at 10.6K–163K ctx"
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_CONTEXTS = (10602, 40002)
+DEFAULT_CONTEXTS = (10602, 40002, 81653, 163336)
+DEFAULT_SWEEP = (8, 16, 32, 64, 128, 256)
+NOMINAL_HBM_GBS = 8000.0  # the metric's denominator (GB300 HBM3e, nominal)
 WINDOW_RESIDENCY = W.WINDOW + 64
 ROTATE = 3
 PARTIAL_SOURCES = ("paged_split_kv_attn_gb300/csrc/partial_kernel.cuh",
@@ -201,6 +211,25 @@ class ClockSampler:
 
 
 # ---- the workload ----------------------------------------------------------------
+
+_CASES: dict = {}
+
+
+def global_case(ctx: int):
+    """The global-layer decode case at `ctx` keys (made once per process)."""
+    key = ("global", ctx)
+    if key not in _CASES:
+        _CASES[key] = W.global_case(ctx, seed=ctx)
+    return _CASES[key]
+
+
+def window_case():
+    """The sliding-window decode case at residency window + one page."""
+    key = ("window", WINDOW_RESIDENCY)
+    if key not in _CASES:
+        _CASES[key] = W.window_case(WINDOW_RESIDENCY, seed=7)
+    return _CASES[key]
+
 
 class Call:
     """One decode call of the step: a pool (and rotating copies), its inputs and outputs.
@@ -455,10 +484,10 @@ def make_extra_calls(args, dev):
 def make_calls(args, dev):
     calls, prep, fused = [], args.append == "prep", args.append == "fused"
     for ctx in args.contexts:
-        calls.append(Call(f"global_{ctx}", W.global_case(ctx, seed=ctx), False, args.splits, dev,
+        calls.append(Call(f"global_{ctx}", global_case(ctx), False, args.splits, dev,
                           ROTATE, prep=prep, fused=fused))
     if not args.no_window:
-        calls.append(Call(f"window_{WINDOW_RESIDENCY}", W.window_case(WINDOW_RESIDENCY, seed=7),
+        calls.append(Call(f"window_{WINDOW_RESIDENCY}", window_case(),
                           True, args.window_splits, dev, ROTATE, prep=prep, fused=fused))
     return calls
 
@@ -479,9 +508,9 @@ def cpu_baseline(cases, budget_s: float):
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{reps} pass(es) of the step's {len(cases)} decode calls "
-                      f"({', '.join(str(int(c.seq_lens.sum())) + ' keys' for c in cases)}), "
-                      f"fp64 direct softmax over the paged pool, {dt:.1f} s"}
+            "sample": f"{reps} passes of the step's {len(cases)} calls "
+                      f"({'/'.join(str(int(c.seq_lens.sum())) for c in cases)} keys), "
+                      f"fp64 direct softmax, {dt:.1f} s"}
 
 
 # ---- main ----------------------------------------------------------------------------
@@ -517,8 +546,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="time eager stream launches instead of CUDA graph replays")
-    ap.add_argument("--sweep", type=int, nargs="*", default=None,
-                    help="also time each global context alone at these split counts")
+    ap.add_argument("--sweep", type=int, nargs="*", default=list(DEFAULT_SWEEP),
+                    help="split counts each global context is also timed at alone "
+                         "(the automatic plan is always added); none to skip")
+    ap.add_argument("--detail", default=None,
+                    help="also write every per-call figure (unrounded) to this JSON file")
     return ap.parse_args()
 
 
@@ -527,9 +559,9 @@ def reference_arm(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     import oracle
-    cases = [W.global_case(ctx, seed=ctx) for ctx in args.contexts]
+    cases = [global_case(ctx) for ctx in args.contexts]
     if not args.no_window:
-        cases.append(W.window_case(WINDOW_RESIDENCY, seed=7))
+        cases.append(window_case())
     nbytes = sum(c.kv_bytes() for c in cases)
     for _ in range(min(args.warmup, 1)):
         for c in cases:
@@ -556,25 +588,23 @@ def reference_arm(args):
 
 
 def config_dict(args):
-    return {"workload": "gemma4-31b decode step: global-layer split-KV decode at contexts "
-                        + "/".join(str(c) for c in args.contexts)
-                        + ("" if args.no_window else
-                           f" + sliding-window decode at residency {WINDOW_RESIDENCY}"),
-            "global": {"batch": 1, "num_q_heads": 32, "num_kv_heads": 4, "head_dim": 512,
-                       "page_size": 256, "contexts": list(args.contexts),
-                       "splits": args.splits or "auto"},
-            "window": None if args.no_window else
-            {"batch": 1, "num_q_heads": 32, "num_kv_heads": 16, "head_dim": 256,
-             "page_size": 64, "window": W.WINDOW, "residency": WINDOW_RESIDENCY,
-             "splits": args.window_splits or "auto"},
-            "new_tokens": {"prep": "projection rows through the fused K/V prep (RMS norm, "
-                                   "rotation, page write, prepared query) in one launch",
-                           "copy": "K/V rows copied into the pages (kv_append_rows)",
-                           "fused": "K/V rows written into the pages by the decode's own "
-                                    "partial kernel (two launches per call)"}[args.append],
-            "kv_dtype": "bf16", "accumulate": "f32", "out_dtype": "bf16",
-            "l2": f"inputs larger than L2: {ROTATE} rotating pool copies, >400 MB of K/V per step",
+    """The workload, named by what it is (kept short: the line must fit a log tail)."""
+    wl = ("gemma4-31b decode step: global layer (32q/4kv, hd512, pages 256) at "
+          + "/".join(str(c) for c in args.contexts)
+          + ("" if args.no_window else
+             f" + sliding layer (32q/16kv, hd256, W{W.WINDOW}, pages 64) at {WINDOW_RESIDENCY}"))
+    return {"workload": wl, "batch": 1, "splits": args.splits or "auto",
+            "new_tokens": {"prep": "fused K/V prep (norm, rotation, page write) per call",
+                           "copy": "kv_append_rows per call",
+                           "fused": "row written by the decode's own partial kernel"}[args.append],
+            "kv": "bf16, f32 accumulate, bf16 out",
+            "l2": f"inputs larger than L2: {ROTATE} rotating pool copies",
             "parallelism": "replicas"}
+
+
+def r1(x):
+    """Round for the printed line (full precision goes to --detail)."""
+    return None if x is None else round(float(x), 1)
 
 
 def main():
@@ -595,6 +625,7 @@ def main():
     packed = Packed(calls, dev)
     stream = torch.cuda.current_stream()
     step_bytes = sum(c.bytes for c in calls)
+    peak, peak_kind = measured_peak()
 
     # per-call partial-kernel events (recorded by the library around the partial launch)
     ev = {c.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -639,22 +670,20 @@ def main():
     graphs = None
     if not args.eager:
         graphs, launches_per_step = capture(calls)
-        packed.bind(1)  # the same step over the second set of input/output buffers
-        graphs_b, _ = capture(calls)
-        packed.bind(0)
 
-    def timed(run_step):
+    def timed(run_step, steps=None):
         """K steps between events on the stream, barrier and synchronize on both sides."""
+        steps = args.steps if steps is None else steps
         dist.barrier()
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for it in range(args.steps):
+        for it in range(steps):
             run_step(it)
         t1.record(stream)
         torch.cuda.synchronize()
         dist.barrier()
-        return dist.max(t0.elapsed_time(t1) / args.steps)
+        return dist.max(t0.elapsed_time(t1) / steps)
 
     def eager_step(it):
         for c in calls:
@@ -666,7 +695,7 @@ def main():
         t_end = time.perf_counter() + seconds
         it = 0
         while time.perf_counter() < t_end:
-            for _ in range(64):
+            for _ in range(16):
                 if graphs is not None:
                     graphs[it % ROTATE].replay()
                 else:
@@ -686,121 +715,18 @@ def main():
         launches = pskv.pskv_kernel_launches() - launches0
     keep_busy(0.2)
     clock_info = clocks.stop()
-    clock_info["window"] = "sampled every 100 ms while the step ran: 0.4 s before the timed region, then it, then 0.2 s"
+    clock_info["window"] = "every 100 ms: 0.4 s before the timed steps, them, 0.2 s after"
     value = whole_job_gbps(step_bytes, dist.world, ms)
     eager_ms = ms if graphs is None else timed(eager_step)
 
-    # ---- the partial kernels' durations: a second pass of K eager steps with CUDA
-    # events recorded by the library right around each partial launch
-    for it in range(args.steps):
-        for c in calls:
-            c.run(it, events=ev[c.name][it])
-    torch.cuda.synchronize()
-    per_call = {}
-    for c in calls:
-        part = [b.elapsed_time(e) for b, e in ev[c.name]]
-        per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
-                            "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9}
-
-    # per-call µs/call (append + partial + merge), each call timed alone with a cold L2:
-    # a 256 MB buffer is READ between calls (reads leave no dirty lines to write back)
-    extra = make_extra_calls(args, dev)
-    for c in extra:
-        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for it in range(args.warmup):
-            c.run(it)
-        for it in range(args.steps):
-            c.run(it, events=pe[it])
-        torch.cuda.synchronize()
-        part = [b.elapsed_time(e) for b, e in pe]
-        per_call[c.name] = {"kv_bytes": c.bytes, "partial_us_mean": 1e3 * statistics.mean(part),
-                            "partial_GBps": c.bytes / (statistics.mean(part) * 1e-3) / 1e9,
-                            "note": ("16-row ragged batch (lengths log-uniform up to 131,072)"
-                                     if c.name == "ragged16" else "folded format"
-                                     if c.tokens == 1 else f"verify window of {c.tokens} tokens")
-                            + ", measured beside the step (not in value)"}
-    # each call replayed from its own graphs, so host launch overhead stays out
-    flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
-    for c in calls + extra:
-        cg, _ = capture([c])
-        times = []
-        for it in range(max(5, min(args.steps, 30))):
-            flush.sum()
-            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            b.record(stream)
-            cg[it % ROTATE].replay()
-            e.record(stream)
-            torch.cuda.synchronize()
-            times.append(b.elapsed_time(e) * 1e3)
-        del cg
-        per_call[c.name]["us_per_call_median"] = statistics.median(times)
-        per_call[c.name]["GBps_per_call"] = c.bytes / (statistics.median(times) * 1e-6) / 1e9
-        per_call[c.name]["splits"] = c.splits or (
-            pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads, c.lens_host)
-            if c.tokens == 1 else "auto")
-
-    # optional split sweep of the global contexts (each call alone, cold L2)
-    sweep = None
-    if args.sweep:
-        sweep = {}
-        for c in calls:
-            if c.windowed:
-                continue
-            res = {}
-            ws0 = c.ws  # the step's graphs point at this workspace: keep it alive and restore it
-            for p in args.sweep + [0]:
-                c.splits = p
-                c.ws = pskv.workspace(1, 32, 512, p, dev)
-                cg, _ = capture([c])  # each split count replayed from its own graphs
-                times = []
-                for it in range(10):
-                    flush.sum()
-                    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    b.record(stream)
-                    cg[it % ROTATE].replay()
-                    e.record(stream)
-                    torch.cuda.synchronize()
-                    times.append(b.elapsed_time(e) * 1e3)
-                del cg
-                key = p if p else "auto(%d)" % pskv.pskv_plan_splits(c.layouts[0], 32, c.lens_host)
-                res[key] = statistics.median(times)
-            sweep[c.name] = res
-            c.splits = args.splits
-            c.ws = ws0
-    del flush
-
-    # the same step with the fused K/V prep in place of the row copy (projection
-    # rows in, normalised and rotated K/V written into the pages, queries out)
-    prep_step = None
-    if args.append != "prep" and not args.no_prep_step and graphs is not None:
-        pargs = argparse.Namespace(**{**vars(args), "append": "prep"})
-        pcalls = make_calls(pargs, dev)
-        for it in range(args.warmup):
-            for c in pcalls:
-                c.run(it)
-        pgraphs, plaunch = capture(pcalls)
-        pms = timed(lambda it: pgraphs[it % ROTATE].replay())
-        for c in pcalls:
-            if c.status[0].item() != 0:
-                raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
-        prep_step = {"ms_per_step": pms, "unit": "GB/s",
-                     "value": whole_job_gbps(step_bytes, dist.world, pms),
-                     "launches_per_step": plaunch,
-                     "note": "the step with kv_prep_append (projection rows: RMS norm, rotation, "
-                             "page write, prepared queries) in place of kv_append_rows"}
-        del pgraphs, pcalls
-
-    # end-to-end through the public calls: each step copies its inputs in from
-    # pinned host memory (one copy) and its outputs back (one copy); the copies
-    # of neighbouring steps overlap the step in between (two buffer sets)
+    # ---- end to end through the C entry points: eager library calls each step
+    # (no graphs), each step's inputs copied in from pinned host memory (one
+    # packed copy) and its outputs copied back (one copy), inside the timed
+    # region; the copies of neighbouring steps overlap the step in between
     def run_e2e(it, parity):
-        if graphs is not None:
-            (graphs, graphs_b)[parity][it % ROTATE].replay()
-        else:
-            packed.bind(parity)
-            for c in calls:
-                c.run(it)
+        packed.bind(parity)
+        for c in calls:
+            c.run(it)
 
     def timed_e2e(steps):
         dist.barrier()
@@ -818,13 +744,103 @@ def main():
     timed_e2e(max(args.warmup, 2))
     e2e_ms = timed_e2e(args.steps)
     packed.bind(0)
-
     for c in calls:
         if c.status[0].item() != 0:
             raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
 
-    # paged prefills beside the step, last (tensor-core work: FLOP/s against the
-    # bf16 peak; heavy enough to move the clocks, so nothing is timed after them)
+    # ---- the partial kernels' durations: a pass of K eager steps with CUDA
+    # events recorded by the library right around each partial launch
+    for it in range(args.steps):
+        for c in calls:
+            c.run(it, events=ev[c.name][it])
+    torch.cuda.synchronize()
+    detail = {}
+    for c in calls:
+        part = statistics.mean([b.elapsed_time(e) for b, e in ev[c.name]])
+        detail[c.name] = {"kv_bytes": c.bytes, "partial_us": 1e3 * part,
+                          "partial_GBps": c.bytes / (part * 1e-3) / 1e9}
+
+    # ---- calls timed beside the step (not in value): partial kernel alone by events
+    extra = make_extra_calls(args, dev)
+    for c in extra:
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for it in range(args.warmup):
+            c.run(it)
+        for it in range(args.steps):
+            c.run(it, events=pe[it])
+        torch.cuda.synchronize()
+        part = statistics.mean([b.elapsed_time(e) for b, e in pe])
+        detail[c.name] = {"kv_bytes": c.bytes, "partial_us": 1e3 * part,
+                          "partial_GBps": c.bytes / (part * 1e-3) / 1e9}
+
+    # ---- each call alone, replayed from its own graphs with a cold L2 (a 256 MB
+    # buffer is READ between calls: reads leave no dirty lines to write back)
+    flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def per_call_us(c, reps):
+        cg, _ = capture([c])
+        times = []
+        for it in range(reps):
+            flush.sum()
+            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b.record(stream)
+            cg[it % ROTATE].replay()
+            e.record(stream)
+            torch.cuda.synchronize()
+            times.append(b.elapsed_time(e) * 1e3)
+        del cg
+        return statistics.median(times)
+
+    reps = max(5, min(args.steps, 30))
+    for c in calls + extra:
+        us = per_call_us(c, reps)
+        gbps = c.bytes / (us * 1e-6) / 1e9
+        detail[c.name].update({
+            "us_per_call": us, "GBps_per_call": gbps,
+            "frac_of_8TBs": gbps / NOMINAL_HBM_GBS, "frac_of_measured": gbps / peak,
+            "splits": c.splits or (pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads,
+                                                         c.lens_host)
+                                   if c.tokens == 1 else "auto")})
+
+    # ---- the split-count sweep of every global context (each call alone, cold L2)
+    sweep = {}
+    if args.sweep:
+        for c in calls:
+            if c.windowed:
+                continue
+            res = {}
+            ws0, s0 = c.ws, c.splits  # the step's graphs point at this workspace: keep it alive
+            for p in args.sweep:
+                c.splits = p
+                c.ws = pskv.workspace(1, 32, 512, p, dev)
+                res[p] = per_call_us(c, 10)
+            c.splits, c.ws = s0, ws0
+            best = min(res, key=res.get)
+            sweep[c.name] = {"us": res, "best_splits": best, "best_us": res[best],
+                             "auto_splits": detail[c.name]["splits"],
+                             "auto_us": detail[c.name]["us_per_call"]}
+    del flush
+
+    # ---- the same step with the fused K/V prep in place of the row copy
+    # (projection rows in, normalised and rotated K/V written into the pages,
+    # queries out)
+    prep_ms = None
+    if args.append != "prep" and not args.no_prep_step and graphs is not None:
+        pargs = argparse.Namespace(**{**vars(args), "append": "prep"})
+        pcalls = make_calls(pargs, dev)
+        for it in range(args.warmup):
+            for c in pcalls:
+                c.run(it)
+        pgraphs, _ = capture(pcalls)
+        prep_ms = timed(lambda it: pgraphs[it % ROTATE].replay())
+        for c in pcalls:
+            if c.status[0].item() != 0:
+                raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
+        del pgraphs, pcalls
+
+    # ---- paged prefills beside the step, last (tensor-core work: FLOP/s against
+    # the bf16 peak; heavy enough to move the clocks, so nothing is timed after them)
     prefill = {}
     for c in make_prefill_calls(args, dev):
         cg, _ = capture([c])
@@ -840,50 +856,62 @@ def main():
             raise RuntimeError(f"{c.name}: device fault word {c.status[0].item()}")
         us = statistics.median(times)
         tf = c.flops / (us * 1e-6) / 1e12
-        prefill[c.name] = {"tokens": c.tokens, "us_per_call_median": us,
-                           "tokens_per_s": c.tokens / (us * 1e-6), "tflops": tf,
-                           "tflops_frac_of_bf16_peak": tf / measured_tensor_peak()}
+        prefill[c.name] = {"tokens": c.tokens, "us": us, "tflops": tf,
+                           "frac_of_bf16_peak": tf / measured_tensor_peak()}
         del cg, c
 
-    peak, peak_kind = measured_peak()
     glob = [c for c in calls if not c.windowed]
     part_bytes = sum(c.bytes for c in glob)
-    part_s = sum(statistics.mean([b.elapsed_time(e) for b, e in ev[c.name]]) * 1e-3 for c in glob)
+    part_s = sum(detail[c.name]["partial_us"] * 1e-6 for c in glob)
     achieved = part_bytes / part_s / 1e9
     traffic_per_key = recorded_traffic()
     keys_per_launch = statistics.mean(int(c.case.seq_lens.sum()) for c in glob)
     roofline = {"bound": "hbm", "kernel": "pskv_partial_kernel<MmaConsumer<512, 8>>",
-                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
-                "measured" else "fallback 6.8 TB/s",
+                "achieved": r1(achieved), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "peak_source": "measured hbm_gbs" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": part_bytes / len(glob),
-                "traffic": None if traffic_per_key is None else traffic_per_key * keys_per_launch}
+                "traffic": None if traffic_per_key is None
+                else round(traffic_per_key * keys_per_launch)}
 
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+    # per call: us, GB/s, % of 8 TB/s, % of the measured copy peak, splits, partial us
+    per_call = {"cols": ["us", "GBps", "pct_8TBs", "pct_meas", "P", "partial_us"]}
+    for name, d in detail.items():
+        per_call[name] = [r1(d["us_per_call"]), round(d["GBps_per_call"]),
+                          r1(100 * d["frac_of_8TBs"]), r1(100 * d["frac_of_measured"]),
+                          d["splits"], r1(d["partial_us"])]
+    line = {"metric": METRIC, "value": r1(value), "unit": "GB/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_dict(args), "roofline": roofline,
-            "e2e": {"value": whole_job_gbps(step_bytes, dist.world, e2e_ms), "unit": "GB/s",
-                    "ms_per_step": e2e_ms,
+            "data": "synthetic", "config": config_dict(args), "gpu_launches": int(launches),
+            "roofline": roofline,
+            "e2e": {"value": r1(whole_job_gbps(step_bytes, dist.world, e2e_ms)), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5),
                     "h2d_bytes_per_step": packed.host_in.numel(),
                     "d2h_bytes_per_step": packed.host_out[0].numel(),
-                    "copies": "one packed copy in and one out per step, each on its own "
-                              "stream, overlapping the neighbouring steps' compute"},
-            "gpu_launches": int(launches), "clocks": clock_info, "calls": per_call}
-    if sweep is not None:
-        line["split_sweep_us"] = sweep
-    if prep_step is not None:
-        line["prep_step"] = prep_step
+                    "how": "eager C-ABI calls; one packed copy in, one out per step"},
+            "clocks": clock_info,
+            "step_ms": {"graph": round(ms, 5), "eager": round(eager_ms, 5),
+                        "prep": None if prep_ms is None else round(prep_ms, 5)},
+            "per_call": per_call}
+    if sweep:
+        line["sweep_us"] = {"P": list(args.sweep)}
+        for name, sw in sweep.items():
+            line["sweep_us"][name] = [r1(sw["us"][p]) for p in args.sweep] + [sw["best_splits"]]
     if prefill:
-        line["prefill"] = prefill
-    line["step_launch"] = ("CUDA graph replay (one graph per pool copy, captured once)"
-                           if graphs is not None else "eager stream launches")
-    line["eager"] = {"ms_per_step": eager_ms, "unit": "GB/s",
-                     "value": whole_job_gbps(step_bytes, dist.world, eager_ms)}
+        line["prefill_tflops"] = {k.replace("prefill_", ""): round(v["tflops"]) for k, v in
+                                  prefill.items()}
     if dist.rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline([c.case for c in calls], args.cpu_seconds)
+        cb = cpu_baseline([c.case for c in calls], args.cpu_seconds)
+        cb["value"] = round(cb["value"], 3)
+        line["cpu_baseline"] = cb
     if dist.rank == 0:
-        print(json.dumps(line), flush=True)
+        if args.detail:
+            with open(args.detail, "w") as f:
+                json.dump({"line": line, "calls": detail, "sweep": sweep, "prefill": prefill,
+                           "prep_step_ms": prep_ms, "eager_ms": eager_ms}, f, indent=1)
+        print(json.dumps(line, separators=(",", ":"), ensure_ascii=False), flush=True)
     dist.close()
 
 

@@ -405,7 +405,9 @@ int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_hea
  *     PSKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call before any
- *     stream capture on the device.
+ *     stream capture on the device.  The kept address is not looked up
+ *     again: calling this entry point after cudaDeviceReset on that device
+ *     is not supported.
  *   - All calls share the array.  Calls that may run at the same time on the
  *     GPU (other streams or host threads without ordering) overwrite each
  *     other's partials: order them.  Nothing in the array needs clearing;

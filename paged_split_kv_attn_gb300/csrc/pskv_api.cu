@@ -69,6 +69,28 @@ int partial_slots(int kv_dtype, int head_dim, int group, int format, int nt, int
   return PSKV_OK;
 }
 
+// The automatic split count of the split-KV partial kernels for a call whose
+// rows carry `columns` query columns per KV head (query heads per KV head x
+// tokens): one n-tile of 8 columns when they fit, else CTAs of two n-tiles,
+// `col_blocks` of them per partition.  decode_attn_* (num_splits = 0) and
+// pskv_plan_splits both take their plan from here.
+int auto_partial_splits(const pskv_layout_desc &d, int32_t batch, int group, int64_t columns,
+                        const int32_t *seq_lens_host, int *P) {
+  const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
+  if (kernel < 0) return PSKV_ERR_UNSUPPORTED;
+  const int nt = columns > 8 ? 2 : 1;
+  const int64_t col_blocks = (columns + 8 * nt - 1) / (8 * nt);
+  int slots = 0;
+  const int rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots);
+  if (rc) return rc;
+  // every partition launches col_blocks CTAs
+  const int64_t per = slots / col_blocks;
+  const bool bytes_bound = kernel == kKernelMma && d.format != PSKV_FORMAT_FOLDED && columns <= 8;
+  *P = plan_splits(per > 0 ? (int)per : 1, batch, d.num_kv_heads, seq_lens_host,
+                   bytes_bound ? kFillBytes32 : 32);
+  return PSKV_OK;
+}
+
 int merge_group_of(const pskv_decode_opts *opts, int *group) {
   int g = (opts && opts->merge_group) ? opts->merge_group : PSKV_MERGE_GROUP;
   if (g < 1 || g > PSKV_MERGE_GROUP) return PSKV_ERR_INVALID_ARG;
@@ -212,13 +234,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     P = plan_tc_splits(tc_qblocks * d.num_kv_heads * batch, d.head_dim_v == 512 ? n_sm / 2 : n_sm,
                        (max_len + 63) / 64);
   } else if (P == 0) {
-    int slots = 0;
-    if ((rc = partial_slots(d.kv_dtype, d.head_dim_v, group, d.format, nt, &slots))) return rc;
-    // every partition launches col_blocks CTAs
-    const int64_t per = slots / col_blocks;
-    const bool bytes_bound = kernel == kKernelMma && !folded && columns <= 8;
-    P = plan_splits(per > 0 ? (int)per : 1, batch, d.num_kv_heads, seq_lens_host,
-                    bytes_bound ? kFillBytes32 : 32);
+    if ((rc = auto_partial_splits(d, batch, group, columns, seq_lens_host, &P))) return rc;
   }
   // one partition on the tensor-core kernels: the partial is the output
   const bool direct = P == 1 && (kernel == kKernelMma || tc_path || verify_tc);
@@ -613,16 +629,12 @@ int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_hea
   if (!layout || !seq_lens_host || !num_splits || batch < 1 || num_q_heads < 1)
     return PSKV_ERR_INVALID_ARG;
   if (num_q_heads % layout->d.num_kv_heads != 0) return PSKV_ERR_UNSUPPORTED;
-  int slots = 0;
-  const int rc = partial_slots(layout->d.kv_dtype, layout->d.head_dim_v,
-                               num_q_heads / layout->d.num_kv_heads, layout->d.format, 1, &slots);
+  const int group = num_q_heads / layout->d.num_kv_heads;
+  // single-token decode: one column per query head of the KV group
+  int P = 0;
+  const int rc = auto_partial_splits(layout->d, batch, group, group, seq_lens_host, &P);
   if (rc) return rc;
-  const bool bytes_bound =
-      pick_kernel(layout->d.kv_dtype, layout->d.head_dim_v, num_q_heads / layout->d.num_kv_heads,
-                  layout->d.format) == kKernelMma &&
-      layout->d.format != PSKV_FORMAT_FOLDED;
-  *num_splits = plan_splits(slots, batch, layout->d.num_kv_heads, seq_lens_host,
-                            bytes_bound ? kFillBytes32 : 32);
+  *num_splits = P;
   return PSKV_OK;
 }
 

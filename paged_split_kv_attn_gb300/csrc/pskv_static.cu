@@ -14,7 +14,10 @@
 // which cudaGetSymbolAddress returns per device.  This file looks that address
 // up the first time the entry point runs on a device (with that device
 // current) and caches it; that first call should therefore happen before any
-// stream capture begins on that device.
+// stream capture begins on that device.  The cached address belongs to the
+// device's primary context as it was then: after cudaDeviceReset on that
+// device the module is loaded again and the address may change, so calling
+// this entry point after a reset is not supported.
 //
 // Every call uses the same array and the array keeps whatever the previous
 // call left in it.  Nothing in it has to start at zero: each decode writes

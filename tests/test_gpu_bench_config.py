@@ -1,7 +1,7 @@
 """The benchmark's own step, at full size and in the launch configuration it
 times (automatic plans, the new K/V row written by the decode itself, bf16
-output), against the oracle: the global-layer calls at 10,602 and 40,002 keys
-and the sliding-window call at residency 1,088."""
+output), against the oracle: the global-layer calls at 10,602, 40,002, 81,653
+and 163,336 keys and the sliding-window call at residency 1,088."""
 import numpy as np
 import pytest
 import torch
@@ -28,6 +28,8 @@ BF16_TOL = TOL + 2.0 ** -7
 @pytest.mark.parametrize("name,make", [
     ("global_10602", lambda: W.global_case(10602, seed=10602)),
     ("global_40002", lambda: W.global_case(40002, seed=40002)),
+    ("global_81653", lambda: W.global_case(81653, seed=81653)),
+    ("global_163336", lambda: W.global_case(163336, seed=163336)),
     ("window_1088", lambda: W.window_case(1088, seed=7)),
 ])
 def test_bench_step_call(name, make):
