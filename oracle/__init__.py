@@ -76,6 +76,7 @@ def _load():
         lib.orc_decode_online.argtypes = [P, P, P, I, P, P, P, I, I, D, I, I, I, P]
         lib.orc_decode_multirow_direct.argtypes = [P, P, P, I, P, I, I, I, D, P]
         lib.orc_prefill_direct.argtypes = [P, P, P, P, I, P, I, I, I, D, P]
+        lib.orc_decode_tree_direct.argtypes = [P, P, P, I, P, P, I, I, I, D, P]
         lib.orc_partial_scratch_bytes.argtypes = [I64, I64, I64, I64, P, P, P, P]
         lib.orc_num_threads.argtypes = []
         lib.orc_prep_head.argtypes = [P, I, D, P, I, P, P, P]
@@ -237,6 +238,25 @@ def decode_multirow_direct(q, k_pool, v_pool, page_tables, seq_lens, scale):
                                               tables.shape[1], _ptr(lens), q.shape[0], q.shape[1],
                                               q.shape[2], scale, _ptr(out)),
            "decode_multirow_direct")
+    return out
+
+
+def decode_tree_direct(q, k_pool, v_pool, page_tables, seq_lens, tree_mask, scale):
+    """q [batch, tokens, num_q_heads, key width] -> out [batch, tokens, num_q_heads, dv]:
+    the row's last `tokens` keys are a drafted tree in topological order;
+    token t attends every key before the window and the window tokens whose
+    bit is set in tree_mask[b, t] (uint64: its ancestors and itself)."""
+    pool, keep = _pool(k_pool, v_pool)
+    q, _ = _data(q)
+    tables, lens = _c(page_tables, np.int32), _c(seq_lens, np.int32)
+    mask = _c(tree_mask, np.uint64)
+    if mask.shape != q.shape[:2]:
+        raise ValueError("tree_mask must be [batch, tokens]")
+    out = np.zeros((q.shape[0], q.shape[1], q.shape[2], pool.head_dim_v), np.float64)
+    _check(_load().orc_decode_tree_direct(ctypes.byref(pool), _ptr(q), _ptr(tables),
+                                          tables.shape[1], _ptr(lens), _ptr(mask), q.shape[0],
+                                          q.shape[1], q.shape[2], scale, _ptr(out)),
+           "decode_tree_direct")
     return out
 
 

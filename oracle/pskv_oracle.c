@@ -447,6 +447,87 @@ static int decode_direct_tokens(const orc_pool *pool, const void *q, const int32
   return rc_all;
 }
 
+/* softmax(scale q.k_i) v_i over the n keys listed in keys[] (increasing key
+ * indices) of (row b, kv head g), into dst[dv].  s is caller scratch of n doubles. */
+static void attend_paged_keys(const orc_pool *pool, const double *qd, const int32_t *page_tables,
+                              int table_stride, int b, int g, const int *keys, int n,
+                              double scale, double *s, double *dst) {
+  const int dk = pool->head_dim_k, dv = pool->head_dim_v, kw = key_width(pool);
+  double mx = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    const size_t kr = paged_row(pool, dk, page_tables, table_stride, b, g, keys[j]);
+    const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, keys[j]);
+    double acc = 0.0;
+    for (int d = 0; d < kw; ++d) acc += qd[d] * key_elem(pool, kr, vr, d);
+    s[j] = scale * acc;
+    if (s[j] > mx) mx = s[j];
+  }
+  double z = 0.0;
+  for (int j = 0; j < n; ++j) {
+    s[j] = exp(s[j] - mx);
+    z += s[j];
+  }
+  for (int d = 0; d < dv; ++d) dst[d] = 0.0;
+  for (int j = 0; j < n; ++j) {
+    const double w = s[j] / z;
+    const size_t vr = paged_row(pool, dv, page_tables, table_stride, b, g, keys[j]);
+    for (int d = 0; d < dv; ++d) dst[d] += w * load_elem(pool->v, pool->dtype, vr + d);
+  }
+}
+
+/* Tree attention over a drafted window: the window's T tokens are the row's
+ * last T keys, in an order where every token comes after its ancestors.
+ * Token t sees every key before the window and the window tokens j <= t
+ * whose bit j is set in tree_mask[b * T + t] (its ancestors and itself). */
+int orc_decode_tree_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                           int table_stride, const int32_t *seq_lens, const uint64_t *tree_mask,
+                           int batch, int num_tokens, int num_q_heads, double scale,
+                           double *out) {
+  int rc = decode_args_ok(pool, q, page_tables, table_stride, seq_lens, NULL, NULL, batch,
+                          num_q_heads, out);
+  if (rc) return rc;
+  const int T = num_tokens;
+  if (!tree_mask || T < 1 || T > 64) return ORC_ERR_INVALID;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens[b] < T) return ORC_ERR_INVALID;
+    for (int t = 0; t < T; ++t) {
+      const uint64_t m = tree_mask[(size_t)b * T + t];
+      const uint64_t later = t == 63 ? 0 : ~((((uint64_t)1) << (t + 1)) - 1);
+      /* a token sees itself and none of the tokens after it */
+      if (!((m >> t) & 1) || (m & later)) return ORC_ERR_INVALID;
+    }
+  }
+  const int dv = pool->head_dim_v, kw = key_width(pool);
+  const int G = num_q_heads / pool->num_kv_heads;
+  int rc_all = ORC_OK;
+  const int jobs = batch * T * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int job = 0; job < jobs; ++job) {
+    const int h = job % num_q_heads, bt = job / num_q_heads, b = bt / T, t = bt % T, g = h / G;
+    const int w0 = seq_lens[b] - T; /* the window's first key */
+    const uint64_t m = tree_mask[(size_t)bt];
+    double *qd = (double *)malloc(sizeof(double) * (size_t)kw);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(w0 + t + 1));
+    int *keys = (int *)malloc(sizeof(int) * (size_t)(w0 + t + 1));
+    if (!qd || !s || !keys) {
+#pragma omp critical
+      rc_all = ORC_ERR_INVALID;
+    } else {
+      int n = 0;
+      for (int i = 0; i < w0; ++i) keys[n++] = i;
+      for (int j = 0; j <= t; ++j)
+        if ((m >> j) & 1) keys[n++] = w0 + j;
+      for (int d = 0; d < kw; ++d) qd[d] = load_elem(q, pool->dtype, ((size_t)bt * num_q_heads + h) * kw + d);
+      attend_paged_keys(pool, qd, page_tables, table_stride, b, g, keys, n, scale, s,
+                        out + ((size_t)bt * num_q_heads + h) * dv);
+    }
+    free(qd);
+    free(s);
+    free(keys);
+  }
+  return rc_all;
+}
+
 int orc_prefill_direct(const orc_pool *pool, const void *q, const int32_t *cu_q,
                        const int32_t *page_tables, int table_stride, const int32_t *seq_lens,
                        int window, int batch, int num_q_heads, double scale, double *out) {

@@ -147,6 +147,22 @@ int orc_decode_multirow_direct(const orc_pool *pool, const void *q, const int32_
                                int table_stride, const int32_t *seq_lens, int batch,
                                int num_tokens, int num_q_heads, double scale, double *out);
 
+/* Direct fp64 tree attention over a drafted window read through the page
+ * table (TensorFold #1619, description "Reads" and review thread: tree
+ * attention rows read their keys from a page table).  The window's
+ * num_tokens (1..64) tokens are row b's last keys, ordered so that every
+ * token comes after its ancestors; token t sits at key w0 + t, w0 =
+ * seq_lens[b] - num_tokens, and attends keys [0, w0) and the keys w0 + j,
+ * j <= t, whose bit j is set in tree_mask[b * num_tokens + t].  q and out as
+ * in orc_decode_multirow_direct.  Fails closed (ORC_ERR_INVALID) unless every
+ * mask has its own bit t set and no bit above t, and every row holds at least
+ * num_tokens keys.  A chain (mask of token t = bits 0..t) is
+ * orc_decode_multirow_direct. */
+int orc_decode_tree_direct(const orc_pool *pool, const void *q, const int32_t *page_tables,
+                           int table_stride, const int32_t *seq_lens, const uint64_t *tree_mask,
+                           int batch, int num_tokens, int num_q_heads, double scale,
+                           double *out);
+
 /* Direct fp64 paged prefill over variable-length chunks (pegainfer #1057,
  * Description: prompt rows read through a windowed varlen kernel with a
  * window lower bound; pegainfer #1055, Description: the generated prefill

@@ -239,6 +239,37 @@ def ragged_case(seed: int = 0, n: int = 16, hi: int = 131072) -> PagedCase:
     return make_paged_case(seed, ragged_lengths(seed, n, hi), dtype="bf16", **GLOBAL_SHAPE)
 
 
+# ---- drafted token trees ---------------------------------------------------------
+
+def random_tree_parents(seed: int, tokens: int, roots: float = 0.1) -> np.ndarray:
+    """Parent index of each of `tokens` drafted tokens in topological order:
+    token 0 is a root (-1: it hangs off the accepted prefix); token t > 0 is
+    another root with probability `roots`, else the child of a uniformly
+    drawn earlier token."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tokens, 5])))
+    parents = np.full(tokens, -1, np.int64)
+    for t in range(1, tokens):
+        parents[t] = -1 if rng.random() < roots else int(rng.integers(0, t))
+    return parents
+
+
+def chain_parents(tokens: int) -> np.ndarray:
+    """A chain: token t's parent is t - 1 (a plain causal verify window)."""
+    return np.arange(-1, tokens - 1, dtype=np.int64)
+
+
+def tree_masks(parents) -> np.ndarray:
+    """uint64 ancestor masks: bit j of mask[t] is set iff window token j is t
+    itself or one of its ancestors."""
+    parents = np.asarray(parents, np.int64)
+    masks = np.zeros(len(parents), np.uint64)
+    for t, p in enumerate(parents):
+        if not (-1 <= p < t):
+            raise ValueError("parents must precede their children")
+        masks[t] = np.uint64(1 << t) | (masks[p] if p >= 0 else np.uint64(0))
+    return masks
+
+
 # ---- K/V prep inputs -----------------------------------------------------------
 
 @dataclasses.dataclass
