@@ -215,11 +215,12 @@ class ClockSampler:
 _CASES: dict = {}
 
 
-def global_case(ctx: int):
+def global_case(ctx: int, seed: int | None = None):
     """The global-layer decode case at `ctx` keys (made once per process)."""
-    key = ("global", ctx)
+    seed = ctx if seed is None else seed
+    key = ("global", ctx, seed)
     if key not in _CASES:
-        _CASES[key] = W.global_case(ctx, seed=ctx)
+        _CASES[key] = W.global_case(ctx, seed=seed)
     return _CASES[key]
 
 
@@ -240,7 +241,7 @@ class Call:
     copied into the pages as they are (kv_append_rows) and ``q`` is given."""
 
     def __init__(self, name, case, windowed, splits, dev, rotate, tokens=1, prep=False,
-                 fused=False):
+                 fused=False, tree=False):
         import torch
         import paged_split_kv_attn_gb300 as pskv
         self.name, self.case, self.windowed = name, case, windowed
@@ -258,6 +259,10 @@ class Call:
         self.layouts = [pskv.paged_kv_layout_create(k, v, self.status)
                         for k, v in zip(self.k, self.v)]
         self.q = bf(case.q if tokens == 1 else W.window_queries(case, tokens))
+        # a drafted tree over the window (one seeded tree per row), else a causal window
+        self.tree_mask = None if not tree else torch.from_numpy(np.ascontiguousarray(np.stack(
+            [W.tree_masks(W.random_tree_parents(b, tokens)) for b in range(case.batch)]))
+            .view(np.int64)).to(dev)
         self.tables = torch.from_numpy(case.page_tables).to(dev)
         self.lens = torch.from_numpy(case.seq_lens).to(dev)
         self.lens_host = case.seq_lens.copy()
@@ -315,7 +320,11 @@ class Call:
             pskv.kv_append_rows(layout, self.k_new, self.v_new, self.row_of, self.pos_of,
                                 self.tables, self.pages_of_row)
         app = (self.k_new, self.v_new, self.pages_of_row) if self.fused else None
-        if self.tokens > 1:
+        if self.tree_mask is not None:
+            pskv.decode_attn_tree(layout, self.q, self.tables, self.lens, self.lens_host,
+                                  self.tree_mask, self.case.scale, num_splits=self.splits,
+                                  workspace=self.ws, out=self.out, events=events)
+        elif self.tokens > 1:
             pskv.decode_attn_multirow(layout, self.q, self.tables, self.lens, self.lens_host,
                                       self.case.scale, num_splits=self.splits, workspace=self.ws,
                                       out=self.out, events=events)
@@ -473,8 +482,12 @@ def make_extra_calls(args, dev):
                   ROTATE, prep=prep, fused=fused) for ctx in args.folded_contexts]
     for t in args.verify_tokens:
         ctx = args.verify_context
-        calls.append(Call(f"verify_{ctx}x{t}", W.global_case(ctx, seed=ctx + 2), False,
+        calls.append(Call(f"verify_{ctx}x{t}", global_case(ctx, ctx + 2), False,
                           args.splits, dev, ROTATE, tokens=t, prep=prep))
+    for t in args.tree_tokens:
+        ctx = args.verify_context
+        calls.append(Call(f"tree_{ctx}x{t}", global_case(ctx, ctx + 3), False,
+                          args.splits, dev, ROTATE, tokens=t, prep=prep, tree=True))
     if not args.no_ragged:
         calls.append(Call("ragged16", W.ragged_case(0), False, args.splits, dev, ROTATE,
                           prep=prep, fused=fused))
@@ -537,6 +550,8 @@ def parse():
                     help="contexts of the folded-format decode timed beside the step")
     ap.add_argument("--verify-tokens", type=int, nargs="*", default=[2, 4, 8],
                     help="verify-window lengths of the multi-row decode timed beside the step")
+    ap.add_argument("--tree-tokens", type=int, nargs="*", default=[8],
+                    help="drafted-tree sizes (tree attention) timed beside the step")
     ap.add_argument("--verify-context", type=int, default=40002,
                     help="context of those verify windows (global-layer shape)")
     ap.add_argument("--prefill", nargs="*",

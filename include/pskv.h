@@ -74,6 +74,7 @@ typedef struct CUevent_st *pskv_event_t;
 #define PSKV_FAULT_EMPTY_ROW 16u    /* a row had no attended key: its output was written as zeros */
 #define PSKV_FAULT_BAD_STATE 32u    /* merge input with m = -inf but l != 0, or a NaN m: treated as empty */
 #define PSKV_FAULT_BAD_POSITION 64u /* a prep token whose rotation position is outside the table: skipped */
+#define PSKV_FAULT_BAD_MASK 128u    /* a tree mask without its own bit or with a later one: later bits ignored */
 
 /* ---- limits ---------------------------------------------------------------- */
 #define PSKV_MAX_SPLITS 1024       /* most partitions one decode call may use */
@@ -308,6 +309,36 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
                          int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
                          size_t workspace_bytes, void *out, int32_t out_dtype,
                          const pskv_decode_opts *opts, pskv_stream_t stream);
+
+/* Tree attention over a drafted window read through the page table
+ * (TensorFold #1619, description "Reads" and review thread: tree-attention
+ * rows read their keys from a page table, next to drafted verify windows).
+ * The window's num_tokens drafted tokens are row b's last keys (already
+ * appended), ordered so that every token comes after its ancestors.  Token t
+ * sits at key w0 + t, w0 = seq_lens[b] - num_tokens, and attends every key
+ * before the window and the window keys w0 + j, j <= t, whose bit j is set in
+ * its mask.  As decode_attn_multirow, except:
+ *   tree_mask   device uint64[batch][num_tokens]: bit j of the mask of token t
+ *               of row b marks window token j as visible to it; a valid mask
+ *               holds bit t (the token itself) and no bit above t.  A mask
+ *               without bit t or with a later bit sets PSKV_FAULT_BAD_MASK
+ *               (the later bits are ignored; the token attends what the
+ *               remaining bits and the prefix give it)
+ * A chain (the mask of token t = bits 0..t) gives decode_attn_multirow's
+ * causal window.  Routing as for decode_attn_multirow, except that windows
+ * the query-major tensor-memory kernel would take run on the split-KV
+ * kernels instead: bf16 (or folded) pools with 1/2/4/8 query heads per KV
+ * head, 8 or 16 columns per CTA; on bf16 split pools of head dim 256 or 512,
+ * 17 to 64 columns per KV head on the key-major kernel when the longest row
+ * has at least 8,192 keys (there also with 16 to 64 query heads per KV head).
+ * Errors: INVALID_ARG (also a host length below num_tokens, a null mask),
+ * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+int decode_attn_tree(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                     int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
+                     const uint64_t *tree_mask, int32_t batch, int32_t num_tokens,
+                     int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
+                     size_t workspace_bytes, void *out, int32_t out_dtype,
+                     const pskv_decode_opts *opts, pskv_stream_t stream);
 
 /* Paged prefill over variable-length chunks (pegainfer #1057, Description:
  * the sliding family's prompt rows read through a windowed varlen kernel

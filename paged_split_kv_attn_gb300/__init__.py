@@ -6,6 +6,7 @@ entry-point names.  PyTorch provides device memory and streams only.
 """
 from ._binding import *  # noqa: F401,F403
 from ._binding import (EXPORTS, Layout, PskvError, decode_attn_multirow, decode_attn_splitkv,
+                       decode_attn_tree,
                        decode_attn_splitkv_static, decode_attn_windowed,
                        decode_attn_workspace_bytes, kv_append_rows, kv_prep_append, load_library,
                        merge_partials, merge_partials_workspace_bytes, paged_kv_layout_create,
@@ -15,6 +16,7 @@ from ._binding import (EXPORTS, Layout, PskvError, decode_attn_multirow, decode_
                        pskv_strerror, pskv_version, workspace)
 
 __all__ = ["EXPORTS", "Layout", "PskvError", "decode_attn_multirow", "decode_attn_splitkv",
+           "decode_attn_tree",
            "decode_attn_splitkv_static", "decode_attn_windowed",
            "decode_attn_workspace_bytes", "kv_append_rows", "kv_prep_append", "load_library",
            "merge_partials",

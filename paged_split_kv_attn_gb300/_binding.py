@@ -35,6 +35,7 @@ PSKV_FAULT_WAIT_TIMEOUT = 8
 PSKV_FAULT_EMPTY_ROW = 16
 PSKV_FAULT_BAD_STATE = 32
 PSKV_FAULT_BAD_POSITION = 64
+PSKV_FAULT_BAD_MASK = 128
 
 PSKV_MAX_SPLITS = 1024
 PSKV_AUTO_MAX_SPLITS = 256
@@ -46,7 +47,7 @@ PSKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 # Every function the header declares, in the header's order.
 EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows", "kv_prep_append",
            "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow",
-           "prefill_attn_paged", "merge_partials",
+           "decode_attn_tree", "prefill_attn_paged", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
            "pskv_check_flags", "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches",
@@ -108,6 +109,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                          I32, P, P]
     lib.decode_attn_multirow.argtypes = [P, P, P, I32, P, P, I32, I32, I32, F, I32, P, SZ, P, I32,
                                          P, P]
+    lib.decode_attn_tree.argtypes = [P, P, P, I32, P, P, P, I32, I32, I32, F, I32, P, SZ, P, I32,
+                                     P, P]
     lib.prefill_attn_paged.argtypes = [P, P, P, P, P, I32, P, P, I32, I32, I32, F, I32, P, SZ, P,
                                        I32, P, P]
     lib.merge_partials.argtypes = [P, P, P, I32, I32, I32, P, I32, P, SZ, P, P, P]
@@ -438,6 +441,41 @@ def decode_attn_multirow(layout: Layout, q, page_tables, seq_lens, seq_lens_host
         float(scale), num_splits, _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dev(out, "out"), _dtype_code(out.dtype),
         None if opts is None else ctypes.byref(opts), _stream(stream)), "decode_attn_multirow")
+    return out
+
+
+def decode_attn_tree(layout: Layout, q, page_tables, seq_lens, seq_lens_host, tree_mask, scale,
+                     num_splits: int = 0, workspace=None, out=None, out_dtype=None,
+                     merge_group: int = 0, events=None, stream=None) -> torch.Tensor:
+    """Tree attention over a drafted window: ``q`` is [batch, tokens, num_q_heads,
+    head_dim]; the row's last ``tokens`` keys are the drafted tokens in an order
+    where ancestors come first; ``tree_mask`` (device int64 or uint64 [batch,
+    tokens]) holds each token's ancestor bits (itself included).  Token t
+    attends every key before the window and the window tokens its mask marks.
+    Returns ``out`` [batch, tokens, num_q_heads, head_dim]."""
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, tokens, num_q_heads, head_dim]")
+    batch, tokens, hq = q.shape[0], q.shape[1], q.shape[2]
+    if tuple(tree_mask.shape) != (batch, tokens) or tree_mask.element_size() != 8:
+        raise ValueError("tree_mask must be a 64-bit [batch, tokens] tensor")
+    dv = layout.desc.head_dim_v
+    if out is None:
+        out = torch.empty((batch, tokens, hq, dv), device=q.device,
+                          dtype=out_dtype or torch.bfloat16)
+    if workspace is None:
+        workspace = _alloc_workspace(batch * tokens, hq, dv, num_splits, q.device)
+    lens_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if len(lens_h) != batch:
+        raise ValueError("seq_lens_host must have one entry per row")
+    opts = _opts(merge_group, events)
+    _check(lib.decode_attn_tree(
+        layout.handle, _dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
+        page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(tree_mask, "tree_mask"), batch, tokens, hq, float(scale), num_splits,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(out, "out"), _dtype_code(out.dtype), None if opts is None else ctypes.byref(opts),
+        _stream(stream)), "decode_attn_tree")
     return out
 
 

@@ -20,7 +20,8 @@ LIB = os.path.join(PKG, "libpskv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["attn_tc.cu", "attn_verify.cu", "partial_mma.cu", "partial_mma_nt2.cu", "partial_simt_f32.cu",
+SOURCES = ["attn_tc.cu", "attn_verify.cu", "partial_mma.cu", "partial_mma_nt2.cu",
+           "partial_mma_tree.cu", "partial_simt_f32.cu",
            "partial_simt_bf16.cu", "merge.cu", "append.cu", "prep.cu", "pskv_api.cu",
            "pskv_plan.cpp", "pskv_static.cu"]
 

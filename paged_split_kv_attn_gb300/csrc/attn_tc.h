@@ -28,6 +28,7 @@ struct TcArgs {
   int num_splits, qblocks, total_rows, window;
   int box_rows;                // rows per tensor copy: 64 when a page holds whole tiles, else 16
   float scale_log2;
+  const unsigned long long *tree_mask;  // [rows] drafted-tree ancestor masks (key-major kernel), or null
 };
 
 // Encodes the pools' tensor maps (rows = num_pages * Hkv * page_size < 2^31) and launches:

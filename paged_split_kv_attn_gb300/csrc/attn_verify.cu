@@ -491,10 +491,13 @@ namespace {
 // The softmax warps' loop over the partition's tiles (thread = key row kr of
 // the tile).  This thread's share of column c's sum gathers in its lane of
 // tensor-memory column kLCol + c.  Returns false on an abort.
+// In a drafted tree, `vt` holds, for the one window key this thread's row can
+// meet (key row kr of some tile), bit t set iff that key is visible to token t.
 template <int DT, int NC>
 __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, unsigned char *sm,
                                              uint64_t *bars, uint32_t tmem,
-                                             volatile int *abort_flag, int &ph) {
+                                             volatile int *abort_flag, int &ph,
+                                             unsigned long long vt) {
   using L = VLay<DT, NC>;
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, kr = 32 * w + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w) << 16);
@@ -505,6 +508,8 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
   volatile int *flags = reinterpret_cast<volatile int *>(sm + L::kOffFlag);
   const float sc = a.scale_log2;
   const int lim0 = pl.len - pl.T + 1;  // token t sees the keys below lim0 + t
+  const bool tree = a.tree_mask != nullptr;
+  const int win0 = lim0 - 1;  // the window's first key
   // this thread's key in P^T's K-major rows: slab, then the 2-byte slot inside the
   // row's swizzled 16-byte chunk (the chunk index is XORed with the row's low bits)
   const int p_slab = (kr >> 6) * L::kPSlab, p_chunk = (kr & 63) >> 3, p_byte = 2 * (kr & 7);
@@ -535,7 +540,17 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
     // ---- mask (by selection: rows never loaded may hold anything)
     const int key = (pl.t_begin + j) * kKeys + kr;
     const bool key_ok = kr >= inf.vlo && kr < inf.vhi && !((inf.bad >> (kr >> 4)) & 1u);
-    if (!(key_ok && key < lim0)) {
+    if (tree) {
+      // a window key (win0 <= key < win0 + T) is this thread's one window key
+      if (!(key_ok && key < win0)) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const int t = c >> a.group_shift;
+          const bool vis = key_ok && key < lim0 + t && (key < win0 || ((vt >> t) & 1ull));
+          x[c] = vis ? x[c] : -CUDART_INF_F;
+        }
+      }
+    } else if (!(key_ok && key < lim0)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const bool vis = key_ok && key < lim0 + (c >> a.group_shift);
@@ -853,6 +868,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     stage_q<DT, NC>(a, pl, sm);
     if (kr < NC) m_sm[kr] = -CUDART_INF_F;
+    // A drafted tree: the window keys are win0 .. win0 + T - 1 (T <= 64 < 128
+    // keys a tile), so the only one this thread's key row kr can meet is window
+    // key d = (kr - win0) mod 128 when d < T; bit t of vt: token t sees it
+    // (its mask holds bit d, and d <= t).  A mask with a later bit, or
+    // without its own, is flagged; the later bits are ignored.
+    unsigned long long vt = 0;
+    if (a.tree_mask != nullptr) {
+      const int win0 = pl.len - pl.T;
+      const int d = ((kr - win0) % kKeys + kKeys) % kKeys;
+      const unsigned long long *tm = a.tree_mask + pl.r0;
+      if (kr < pl.T) {
+        const unsigned long long mk = tm[kr];
+        const unsigned long long upto = kr >= 63 ? ~0ull : (2ull << kr) - 1;
+        if (!((mk >> kr) & 1ull) || (mk & ~upto)) raise_fault(a.status, PSKV_FAULT_BAD_MASK);
+      }
+      if (d < pl.T)
+        for (int t = d; t < pl.T; ++t) vt |= ((tm[t] >> d) & 1ull) << t;
+    }
     tc::fence_smem_for_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + kQReady);
@@ -866,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int ph = 0;
     bool ok = meet(bars, ph, abort_flag, a.status);  // the reference maxima are set
-    ok = ok && softmax_loop<DT, NC>(a, pl, sm, bars, tmem, abort_flag, ph);
+    ok = ok && softmax_loop<DT, NC>(a, pl, sm, bars, tmem, abort_flag, ph, vt);
     // the last values product (and with it every earlier one), then every column's
     // sum over the tile rows
     ok = ok && warp_wait(bars + kPvDone + (pl.n - 1) % L::kPBufs,

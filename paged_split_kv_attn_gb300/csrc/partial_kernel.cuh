@@ -180,7 +180,9 @@ struct RowPlan {
 // the folded row holds K only where the rotation touches it, V in full, with
 // K's norm weight folded into the query).  The warps scoring quarter 0 read
 // their operands from the K tile, the others from the V tile.
-template <int kD, int kG = 8, bool kFolded = false, int kNT = 1>
+// kTree: the query columns are tokens of a drafted tree; window keys are
+// visible to a column by its token's ancestor mask (held in shared memory).
+template <int kD, int kG = 8, bool kFolded = false, int kNT = 1, bool kTree = false>
 struct MmaConsumer {
   using Elem = __nv_bfloat16;
   static constexpr int D = kD;
@@ -202,7 +204,8 @@ struct MmaConsumer {
   static constexpr int KSP = DW / 16;              // m-tiles of a warp's PV product
   // score accumulator chains (two when the second n-tile's state needs the registers)
   static constexpr int CH = (KSQ % 4 == 0 && kNT == 1) ? 4 : 2;
-  static constexpr int kExtraSmem = 2 * kQuarters * NT * 32 * 16;  // double-buffered exchange
+  static constexpr int kXchgBytes = 2 * kQuarters * NT * 32 * 16;  // double-buffered exchange
+  static constexpr int kExtraSmem = kXchgBytes + (kTree ? kCols * 8 : 0);  // + tree masks
   static constexpr int kRowBytesK = (kFolded ? D / 4 : D) * 2;     // bytes of one stored K row
   static constexpr int kRowBytesV = D * 2;
   using Geom = RingGeom<kRowBytesK, kRowBytesV, 2, 1, PSKV_MMA_STAGES>;
@@ -220,6 +223,8 @@ struct MmaConsumer {
   int lo_fixed, window;    // and keys from lo_fixed on, or from lim - window on with a window
   float scale_log2;
   float4 *xchg;            // [2][kQuarters][NT][32] partial scores
+  const unsigned long long *tmask;  // [kCols] tree masks of the block's columns (kTree)
+  int win0;                // the window's first key (len - tokens)
   int r, c, warp, tokens, cbase, r0;
 
   __device__ int nt_scored() const { return warp % NT; }  // the n-tile this warp scores
@@ -239,6 +244,25 @@ struct MmaConsumer {
     cbase = cb * kCols;
     scale_log2 = a.scale_log2;
     xchg = reinterpret_cast<float4 *>(extra);
+    win0 = rp.len - rp.T;
+    if constexpr (kTree) {
+      unsigned long long *tm = reinterpret_cast<unsigned long long *>(extra + kXchgBytes);
+      tmask = tm;
+      // Column i of the block takes its token's mask, cut to the tokens up to
+      // itself; a mask without its own bit or with a later one is flagged.  The
+      // first tile's consumer barrier orders these stores before any read.
+      if (threadIdx.x < kCols) {
+        const int t = (cbase + (int)threadIdx.x) / G;
+        unsigned long long m = 0;
+        if (t < tokens) {
+          m = a.tree_mask[r0 + t];
+          const unsigned long long upto = t >= 63 ? ~0ull : (2ull << t) - 1;
+          if (!((m >> t) & 1ull) || (m & ~upto)) raise_fault(a.status, PSKV_FAULT_BAD_MASK);
+          m &= upto;
+        }
+        tm[threadIdx.x] = m;
+      }
+    }
     {
       const int jq = cbase + 8 * nt_scored() + r, tq = jq / G;  // the column this lane feeds
       const bool real = tq < tokens;
@@ -324,11 +348,19 @@ struct MmaConsumer {
       // a token's first visible key: lo_fixed, or (own + 1) - window with a window
       const int lo0 = window > 0 ? max(0, lim0[nt] - window) : lo_fixed;
       const int lo1 = window > 0 ? max(0, lim1[nt] - window) : lo_fixed;
-      auto vis = [&](int t, int lo, int lim) { return !skip && t >= lo && t < lim; };
-      s00[nt] = vis(tA, lo0, lim0[nt]) ? st.x * scale_log2 : -CUDART_INF_F;  // key tA, col 8nt+2c
-      s01[nt] = vis(tA, lo1, lim1[nt]) ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, col 8nt+2c+1
-      s10[nt] = vis(tB, lo0, lim0[nt]) ? st.z * scale_log2 : -CUDART_INF_F;  // key tB, col 8nt+2c
-      s11[nt] = vis(tB, lo1, lim1[nt]) ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, col 8nt+2c+1
+      // in a drafted tree, a window key (t >= win0) is visible to a column iff
+      // its bit is set in the column's mask (only tiles reaching the window look)
+      const bool in_tree = kTree && key0 + kKeyTile > win0;
+      auto vis = [&](int t, int lo, int lim, int col) {
+        const int dt = t - win0;
+        return !skip && t >= lo && t < lim &&
+               (!in_tree || dt < 0 || (dt < 64 && ((tmask[col] >> dt) & 1ull)));
+      };
+      const int ca = 8 * nt + 2 * c, cb1 = ca + 1;  // the block's columns of this lane
+      s00[nt] = vis(tA, lo0, lim0[nt], ca) ? st.x * scale_log2 : -CUDART_INF_F;   // key tA, col 8nt+2c
+      s01[nt] = vis(tA, lo1, lim1[nt], cb1) ? st.y * scale_log2 : -CUDART_INF_F;  // key tA, col 8nt+2c+1
+      s10[nt] = vis(tB, lo0, lim0[nt], ca) ? st.z * scale_log2 : -CUDART_INF_F;   // key tB, col 8nt+2c
+      s11[nt] = vis(tB, lo1, lim1[nt], cb1) ? st.w * scale_log2 : -CUDART_INF_F;  // key tB, col 8nt+2c+1
       x0[nt] = fmaxf(s00[nt], s10[nt]);
       x1[nt] = fmaxf(s01[nt], s11[nt]);
       need |= x0[nt] > m0[nt] + kSlack || x1[nt] > m1[nt] + kSlack;

@@ -5,14 +5,19 @@
 
 namespace pskv {
 
-template cudaError_t launch_partial_mma_nt<1>(const PartialArgs &, int, int, bool, dim3,
-                                              cudaStream_t);
+template cudaError_t launch_partial_mma_nt<1, false>(const PartialArgs &, int, int, bool, dim3,
+                                                     cudaStream_t);
 template cudaError_t occupancy_partial_mma_nt<1>(int, int, bool, int *);
 
 cudaError_t launch_partial_mma(const PartialArgs &a, int head_dim, int group, bool folded, int nt,
                                dim3 grid, cudaStream_t s) {
-  if (nt == 1) return launch_partial_mma_nt<1>(a, head_dim, group, folded, grid, s);
-  if (nt == 2) return launch_partial_mma_nt<2>(a, head_dim, group, folded, grid, s);
+  const bool tree = a.tree_mask != nullptr;
+  if (nt == 1)
+    return tree ? launch_partial_mma_nt<1, true>(a, head_dim, group, folded, grid, s)
+                : launch_partial_mma_nt<1, false>(a, head_dim, group, folded, grid, s);
+  if (nt == 2)
+    return tree ? launch_partial_mma_nt<2, true>(a, head_dim, group, folded, grid, s)
+                : launch_partial_mma_nt<2, false>(a, head_dim, group, folded, grid, s);
   return cudaErrorInvalidValue;
 }
 

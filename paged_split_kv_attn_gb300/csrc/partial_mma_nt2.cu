@@ -4,8 +4,8 @@
 
 namespace pskv {
 
-template cudaError_t launch_partial_mma_nt<2>(const PartialArgs &, int, int, bool, dim3,
-                                              cudaStream_t);
+template cudaError_t launch_partial_mma_nt<2, false>(const PartialArgs &, int, int, bool, dim3,
+                                                     cudaStream_t);
 template cudaError_t occupancy_partial_mma_nt<2>(int, int, bool, int *);
 
 }  // namespace pskv

@@ -133,6 +133,7 @@ struct QuerySpec {
   const int32_t *cu_q_host = nullptr;  // [B + 1] host copy of the offsets, or null
   const int32_t *cu_q = nullptr;       // [B + 1] device offsets
   int window = 0;
+  const uint64_t *tree_mask = nullptr;  // [B][tokens] ancestor masks of a drafted tree, or null
 };
 
 int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_tables,
@@ -173,11 +174,17 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int64_t longest = 0;  // the host lengths (checked below); the routing only reads them
   for (int32_t b = 0; b < batch; ++b)
     longest = seq_lens_host[b] > longest ? seq_lens_host[b] : longest;
+  const bool tree = qs.tree_mask != nullptr;
+  if (tree && (varlen || windowed)) return PSKV_ERR_INVALID_ARG;
+  // drafted trees run on the split-KV kernels and the key-major kernel (both
+  // take the tokens' masks), never on the query-major one
   const bool verify_tc = tc_pools && !varlen && !windowed && qs.tokens >= 2 &&
                          window_cols >= kVerifyMinColumns && window_cols <= kVerifyMaxColumns &&
                          longest >= kVerifyMinKeys;
   const bool many_rows = varlen || (!windowed && qs.tokens >= 2 && window_cols >= kTcMinColumns);
-  const bool tc_path = many_rows && tc_pools && !verify_tc;
+  const bool tc_path = !tree && many_rows && tc_pools && !verify_tc;
+  // the tensor-core split-KV consumer is the other kernel that takes tree masks
+  if (tree && !verify_tc && kernel != kKernelMma) return PSKV_ERR_UNSUPPORTED;
   if (kernel < 0 && !tc_path && !verify_tc) return PSKV_ERR_UNSUPPORTED;
   const bool append = opts && opts->append_k;
   if (append) {
@@ -276,6 +283,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.append_pages = append ? opts->append_pages : nullptr;
   a.k_row_bytes = layout->k_row_bytes;
   a.v_row_bytes = layout->v_row_bytes;
+  a.tree_mask = reinterpret_cast<const unsigned long long *>(qs.tree_mask);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)(P * col_blocks), d.num_kv_heads, batch);
@@ -310,6 +318,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
     t.window = qs.window;
     t.box_rows = d.page_size % 64 == 0 ? 64 : 16;
     t.scale_log2 = scale * kLog2e;
+    t.tree_mask = verify_tc ? reinterpret_cast<const unsigned long long *>(qs.tree_mask) : nullptr;
     if (verify_tc)
       e = launch_attn_verify(t, d.k_pool, d.v_pool, d.head_dim_v,
                              dim3((unsigned)P, d.num_kv_heads, batch), s);
@@ -518,6 +527,21 @@ int decode_attn_multirow(const pskv_layout *layout, const void *q, const int32_t
                          const pskv_decode_opts *opts, pskv_stream_t stream) {
   QuerySpec qs;
   qs.tokens = num_tokens;
+  return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
+                       nullptr, false, batch, qs, num_q_heads, scale, num_splits, workspace,
+                       workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int decode_attn_tree(const pskv_layout *layout, const void *q, const int32_t *page_tables,
+                     int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
+                     const uint64_t *tree_mask, int32_t batch, int32_t num_tokens,
+                     int32_t num_q_heads, float scale, int32_t num_splits, void *workspace,
+                     size_t workspace_bytes, void *out, int32_t out_dtype,
+                     const pskv_decode_opts *opts, pskv_stream_t stream) {
+  if (!tree_mask || (reinterpret_cast<uintptr_t>(tree_mask) & 7u)) return PSKV_ERR_INVALID_ARG;
+  QuerySpec qs;
+  qs.tokens = num_tokens;
+  qs.tree_mask = tree_mask;
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
                        nullptr, false, batch, qs, num_q_heads, scale, num_splits, workspace,
                        workspace_bytes, out, out_dtype, opts, stream);

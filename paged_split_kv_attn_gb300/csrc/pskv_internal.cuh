@@ -53,6 +53,9 @@ struct PartialArgs {
   const void *append_v;  // [B][Hkv][Dv]
   const int32_t *append_pages;  // [B] pages leased per row
   int k_row_bytes, v_row_bytes;  // bytes of one stored K / V row of one head
+  // [rows] ancestor mask of each query token of a drafted tree (bit j: the
+  // window's token j is visible), or null for causal windows
+  const unsigned long long *tree_mask;
 };
 
 // Arguments of the merge kernel: level 1 folds groups of `group` partials of
