@@ -21,163 +21,102 @@
 namespace pskv {
 
 constexpr int kMergeThreads = 128;
-constexpr int kMaxStates = 64;  // states one warp weighs: groups of a row, or partials of a group
-constexpr int kChunk = 16;      // states whose o is loaded together (all loads in flight at once)
+constexpr int kMaxStates = 64;  // group states of a row (level 2)
+constexpr int kChunk = 16;      // partials of a group, loaded together (all loads in flight at once)
 
-// One warp reads n <= 64 states' (m, l) in parallel and computes the weights
-// w_i = e^(m_i - M) (-1 marks an empty state, whose o is skipped), M and l.
-// Every lane returns M and L; the weights go to w_s[0..n).
-template <bool kCoherent = false>
-__device__ __forceinline__ void warp_state_weights(const float *m, const float *l, int n,
-                                                   float *w_s, float &M_out, float &L_out,
-                                                   int32_t *status, int lane) {
-  float mi[kMaxStates / 32], li[kMaxStates / 32];
+// Both levels in one launch, one block per (row, 64 or 128 output columns).
+// Thread (c, j) of a block owns float4 column c of the block's columns and folds
+// the groups j, j + L, ... of the row's partials (L = threads per column): it
+// loads a group's (m, l) and its column's numerators all at once (one memory
+// round trip; every thread of a group reads the same (m, l), which the
+// hardware serves as one broadcast), computes the group's weights
+// w_i = e^(m_i - M_g) itself and folds the group in index order (level 1) into
+// a shared-memory group state.  One thread per column then folds the group
+// states in index order and normalises (level 2).  The group states never
+// leave the chip, every step's order is fixed, and the weights and sums are
+// computed identically by every thread that needs them, so the result is
+// deterministic.  An empty state's o is loaded but never used.
+template <int kColsPerBlock>
+__global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
+  constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;  // threads per column
+  __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates];  // group states (m, l)
+  __shared__ int bad_s;
+  // the group numerators of the block's columns, [ng][kColsPerBlock]: sized by
+  // the launch (2 KB for four groups), so that a merge block launched early fits
+  // on an SM beside the partial kernel's CTAs
+  extern __shared__ float4 o1_s[];
+  const int row = blockIdx.x;
+  const int c = threadIdx.x % kColsPerBlock, j = threadIdx.x / kColsPerBlock;
+  const int dv4 = a.dv / 4, d4 = blockIdx.y * kColsPerBlock + c;
+  const int d4c = d4 < dv4 ? d4 : dv4 - 1;  // columns past dv load a real column, never stored
+  const int P = a.count, G = a.group, ng = (P + G - 1) / G;
+  const float *m = a.m + (size_t)row * P, *l = a.l + (size_t)row * P;
+  const float *o = a.o + (size_t)row * P * a.dv;
+  if (threadIdx.x == 0) bad_s = 0;
+  pdl_wait();
+  pdl_launch_dependents();
   bool bad = false;
-  float M = -CUDART_INF_F;
+  // ---- level 1: this thread's groups, each in one round trip
+  for (int g = j; g < ng; g += kGroupLanes) {
+    const int i0 = g * G, n = min(P, i0 + G) - i0;
+    float mi[kChunk], li[kChunk];
+    float4 v[kChunk];
 #pragma unroll
-  for (int k = 0; k < kMaxStates / 32; ++k) {
-    const int i = lane + 32 * k;
-    mi[k] = i < n ? (kCoherent ? __ldcg(m + i) : m[i]) : -CUDART_INF_F;
-    li[k] = i < n ? (kCoherent ? __ldcg(l + i) : l[i]) : 0.f;
-    if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
-      bad = true;
-      mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
-    }
-    M = fmaxf(M, mi[k]);
-  }
+    for (int k = 0; k < kChunk; ++k)
+      if (k < n) {
+        mi[k] = m[i0 + k];
+        li[k] = l[i0 + k];
+        v[k] = __ldg(reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * a.dv) + d4c);
+      }
+    float M = -CUDART_INF_F;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f;
+    for (int k = 0; k < kChunk; ++k)
+      if (k < n) {
+        if (isnan(mi[k]) || (mi[k] == -CUDART_INF_F && li[k] != 0.f)) {
+          bad = true;
+          mi[k] = -CUDART_INF_F;  // an invalid state counts as empty
+        }
+        M = fmaxf(M, mi[k]);
+      }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < kMaxStates / 32; ++k) {
-    const int i = lane + 32 * k;
-    const bool empty = mi[k] == -CUDART_INF_F;
-    const float w = empty ? 0.f : exp2f((mi[k] - M) * kLog2e);
-    if (i < n) w_s[i] = empty ? -1.f : w;
-    // fixed-order sum: lane partials, then a butterfly (same bits every run)
-    if (!empty) L = fmaf(li[k], w, L);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  if (__any_sync(0xffffffffu, bad) && lane == 0) raise_fault(status, PSKV_FAULT_BAD_STATE);
-  M_out = M;
-  L_out = L;
-}
-
-// Load o_i[d4] of states [i0, i0 + kChunk) (those below n), all in flight at once.
-// The values of empty states are loaded too but never used (their o may be
-// uninitialised); loading them keeps the loads independent of the weights, so
-// they overlap the (m, l) loads.  kCoherent reads through L2 only (for data
-// other blocks of this grid just wrote).
-template <bool kCoherent>
-__device__ __forceinline__ void load_chunk(const float *o, int n, int dv, int d4, int i0,
-                                           float4 (&v)[kChunk]) {
-#pragma unroll
-  for (int k = 0; k < kChunk; ++k)
-    if (i0 + k < n) {
-      const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(i0 + k) * dv) + d4;
-      v[k] = kCoherent ? __ldcg(src) : __ldg(src);
-    }
-}
-
-// acc += w_i v[i - i0] over the chunk's states, in index order; empty states
-// (w < 0) are skipped by selection, so whatever their o holds never reaches acc.
-__device__ __forceinline__ void combine_chunk(float4 &acc, const float4 (&v)[kChunk], int n,
-                                              int i0, const float *w_s) {
-#pragma unroll
-  for (int k = 0; k < kChunk; ++k) {
-    if (i0 + k < n) {
-      const float w = w_s[i0 + k];
-      if (w >= 0.f) {
+    for (int k = 0; k < kChunk; ++k)
+      if (k < n && mi[k] != -CUDART_INF_F) {  // empty states: skipped by selection
+        const float w = exp2f((mi[k] - M) * kLog2e);
+        L = fmaf(li[k], w, L);
         acc.x = fmaf(v[k].x, w, acc.x);
         acc.y = fmaf(v[k].y, w, acc.y);
         acc.z = fmaf(v[k].z, w, acc.z);
         acc.w = fmaf(v[k].w, w, acc.w);
       }
+    o1_s[g * kColsPerBlock + c] = acc;
+    if (c == 0) {
+      Mg_s[g] = M;
+      Lg_s[g] = L;
     }
   }
-}
-
-// Both levels in one launch, one block per (row, 64 or 128 output columns).  Every
-// block computes the row's level-1 weights (warp w takes groups w, w + 4, ...)
-// and the level-2 weights over the group states; its threads fold, for their
-// column, each group of partials in index order into a shared-memory group
-// accumulator (level 1), then one thread per column folds the group results
-// in index order and normalises (level 2).  The group results never leave the
-// chip, and the arithmetic and its order are those of two separate levels.
-// The first group's numerators are loaded before any weight is known.
-// kCols float4 columns per block (16, or 32 when a row has at most 4 groups:
-// then no thread of the block idles), kMergeThreads / kCols threads per column.
-template <int kColsPerBlock>
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
-  constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;  // threads per column
-  __shared__ float w_s[PSKV_MAX_SPLITS];             // level-1 weights, by partial
-  __shared__ float m_s[PSKV_MAX_SPLITS], l_s[PSKV_MAX_SPLITS];  // the row's partial (m, l)
-  __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates], wg_s[kMaxStates];  // group states
-  __shared__ float4 o1_s[kMaxStates][kColsPerBlock];  // group numerators of this block's columns
-  __shared__ float M_s, L_s;
-  const int row = blockIdx.x;
-  const int c = threadIdx.x % kColsPerBlock, j = threadIdx.x / kColsPerBlock;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int dv4 = a.dv / 4, d4 = blockIdx.y * kColsPerBlock + c;
-  const int P = a.count, G = a.group, ng = (P + G - 1) / G;
-  const float *m = a.m + (size_t)row * P, *l = a.l + (size_t)row * P;
-  const float *o = a.o + (size_t)row * P * a.dv;
-  pdl_wait();
-  pdl_launch_dependents();
-  float4 v[kChunk];
-  if (j < ng && d4 < dv4) load_chunk<false>(o, min(P, j * G + G), a.dv, d4, j * G, v);
-  // every (m, l) of the row in one round trip, staged in shared memory
-  for (int i = threadIdx.x; i < P; i += kMergeThreads) {
-    m_s[i] = m[i];
-    l_s[i] = l[i];
-  }
+  if (bad) bad_s = 1;
   __syncthreads();
-  // level-1 weights and group states
-  for (int g = warp; g < ng; g += kMergeThreads / 32) {
-    const int i0 = g * G, n = min(P, i0 + G) - i0;
-    float Mg, Lg;
-    warp_state_weights<false>(m_s + i0, l_s + i0, n, w_s + i0, Mg, Lg, a.status, lane);
-    if (lane == 0) {
-      Mg_s[g] = Mg;
-      Lg_s[g] = Lg;
-    }
-  }
-  __syncthreads();
-  // level-2 weights (warp 0) while every thread folds its groups (level 1)
-  if (warp == 0) {
-    float M, L;
-    warp_state_weights<false>(Mg_s, Lg_s, ng, wg_s, M, L, a.status, lane);
-    if (lane == 0) {
-      M_s = M;
-      L_s = L;
-    }
-  }
-  if (d4 < dv4) {
-    for (int g = j; g < ng; g += kGroupLanes) {
-      const int i0 = g * G, end = min(P, i0 + G);
-      if (g != j) load_chunk<false>(o, end, a.dv, d4, i0, v);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      combine_chunk(acc, v, end, i0, w_s);
-      o1_s[g][c] = acc;
-    }
-  }
-  __syncthreads();
-  // level 2 and normalisation, one thread per column
+  // ---- level 2 and normalisation, one thread per column
   if (j == 0 && d4 < dv4) {
+    float M = -CUDART_INF_F;
+    for (int g = 0; g < ng; ++g) M = fmaxf(M, Mg_s[g]);
+    float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int g = 0; g < ng; ++g) {
-      const float w = wg_s[g];
-      if (w >= 0.f) {
-        const float4 x = o1_s[g][c];
+      const float mg = Mg_s[g];
+      if (mg != -CUDART_INF_F) {
+        const float w = exp2f((mg - M) * kLog2e);
+        const float4 x = o1_s[g * kColsPerBlock + c];
+        L = fmaf(Lg_s[g], w, L);
         acc.x = fmaf(x.x, w, acc.x);
         acc.y = fmaf(x.y, w, acc.y);
         acc.z = fmaf(x.z, w, acc.z);
         acc.w = fmaf(x.w, w, acc.w);
       }
     }
-    const bool empty_row = (M_s == -CUDART_INF_F);
-    const float L = L_s;
+    const bool empty_row = (M == -CUDART_INF_F);
     const float4 r = empty_row ? make_float4(0.f, 0.f, 0.f, 0.f)
                                : make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
     if (a.out_dtype == PSKV_DTYPE_BF16) {
@@ -190,6 +129,7 @@ __global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs
     }
     if (empty_row && d4 == 0) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   }
+  if (threadIdx.x == 0 && bad_s) raise_fault(a.status, PSKV_FAULT_BAD_STATE);
 }
 
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
@@ -199,10 +139,12 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s, int *launches) {
   *launches = 1;
   if (ng <= kMergeThreads / 32) {  // every group lane busy with 32 columns per block
     const int chunks = (a.dv / 4 + 31) / 32;
-    return launch_pdl(pskv_merge_cols<32>, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
+    return launch_pdl(pskv_merge_cols<32>, dim3(a.rows, chunks), dim3(kMergeThreads),
+                      (size_t)ng * 32 * sizeof(float4), s, a);
   }
   const int chunks = (a.dv / 4 + 15) / 16;
-  return launch_pdl(pskv_merge_cols<16>, dim3(a.rows, chunks), dim3(kMergeThreads), 0, s, a);
+  return launch_pdl(pskv_merge_cols<16>, dim3(a.rows, chunks), dim3(kMergeThreads),
+                    (size_t)ng * 16 * sizeof(float4), s, a);
 }
 
 }  // namespace pskv

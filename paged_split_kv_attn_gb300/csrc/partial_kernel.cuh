@@ -782,6 +782,22 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
   pdl_wait();
   pdl_launch_dependents();
 
+  // ---- the page ids of the partition's first tiles, fetched by the producer
+  // from the host's copy of the length while the device length is read (plain
+  // rows: uniform tokens, no window, one column block); kept below only if the
+  // device length gives the same first slot and slot count
+  int hint_slot = -1, hint_slots = -1, hint_ids = -1;
+  if (warp == C::kWarps && b < kLenHints && a.len_hint[b] >= a.num_tokens && a.cu_q == nullptr &&
+      a.window_lo == nullptr && a.window == 0 && a.col_blocks == 1) {
+    const int hl = a.len_hint[b];
+    const int tiles = (hl + kKeyTile - 1) / kKeyTile, per = (tiles + P - 1) / P;
+    const int tb = p * per < tiles ? p * per : tiles;
+    hint_slot = tb * kKeyTile / a.page_size;
+    hint_slots = (hl + a.page_size - 1) / a.page_size;
+    const int sl = hint_slot + lane;
+    hint_ids = sl < hint_slots ? __ldg(a.page_tables + (size_t)b * a.table_stride + sl) : -1;
+  }
+
   // ---- this CTA's query tokens (row b's are query rows r0 .. r0 + T - 1)
   RowPlan rp;
   rp.b = b;
@@ -866,6 +882,10 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
     const int32_t *tbl = a.page_tables + (size_t)b * a.table_stride;
     const int n_slots = (k_hi + a.page_size - 1) / a.page_size;  // table entries in use
     int cache_base = -1, cached = -1;
+    if (hint_slots == n_slots && hint_slot == t_begin * kKeyTile / a.page_size) {
+      cache_base = hint_slot;  // the fetched ids are the ones this partition starts with
+      cached = hint_ids;
+    }
     int issued = 0;
     const uint64_t stream_policy = make_evict_first_policy();
     if (append_here) {

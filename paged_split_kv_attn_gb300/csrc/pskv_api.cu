@@ -284,6 +284,8 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   a.k_row_bytes = layout->k_row_bytes;
   a.v_row_bytes = layout->v_row_bytes;
   a.tree_mask = reinterpret_cast<const unsigned long long *>(qs.tree_mask);
+  for (int i = 0; i < kLenHints; ++i)
+    a.len_hint[i] = (i < batch && !varlen && !windowed && !tree) ? seq_lens_host[i] : -1;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)(P * col_blocks), d.num_kv_heads, batch);

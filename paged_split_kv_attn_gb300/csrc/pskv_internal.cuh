@@ -21,6 +21,8 @@ constexpr uint32_t kWaitPolls = 1u << 22;            // try_wait polls before gi
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr int kLenHints = 8;  // rows whose host length rides in the kernel arguments
+
 // Arguments of the split-KV partial kernels (one launch, grid (P, Hkv, B)).
 struct PartialArgs {
   const void *q;             // [B][Hq][D]
@@ -56,6 +58,11 @@ struct PartialArgs {
   // [rows] ancestor mask of each query token of a drafted tree (bit j: the
   // window's token j is visible), or null for causal windows
   const unsigned long long *tree_mask;
+  // Host copies of the first rows' lengths (-1: none): the producer warp
+  // fetches the page ids its partition starts with while the device length
+  // is still on its way, and keeps them only when the device length gives
+  // the same first table slot and slot count (plain uniform rows only).
+  int len_hint[kLenHints];
 };
 
 // Arguments of the merge kernel: level 1 folds groups of `group` partials of
