@@ -36,8 +36,10 @@ constexpr int kChunk = 16;      // partials of a group, loaded together (all loa
 // leave the chip, every step's order is fixed, and the weights and sums are
 // computed identically by every thread that needs them, so the result is
 // deterministic.  An empty state's o is loaded but never used.
+// Four blocks per SM (128 registers a thread, no spills): a call with many
+// rows (a verify window's tokens x query heads) runs its blocks in fewer waves.
 template <int kColsPerBlock>
-__global__ void __launch_bounds__(kMergeThreads) pskv_merge_cols(const MergeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 4) pskv_merge_cols(const MergeArgs a) {
   constexpr int kGroupLanes = kMergeThreads / kColsPerBlock;  // threads per column
   __shared__ float Mg_s[kMaxStates], Lg_s[kMaxStates];  // group states (m, l)
   __shared__ int bad_s;
