@@ -106,3 +106,27 @@ def test_device_lengths_rule_over_the_host_copy():
         ref = ref_direct(dataclasses.replace(c, seq_lens=np.array([dev_len], np.int32)))
         assert max_err(out, ref) <= TOL, dev_len
     assert dc.faults() == 0
+
+
+@pytest.mark.parametrize("host_len,dev_len,splits", [
+    (9000, 8500, 0),    # the plan from the host length, the keys from the device one
+    (9000, 8990, 16),   # the same table slots in use, shifted partition bounds
+    (9000, 9000, 64),   # agreeing copies (the page ids fetched from the host length kept)
+    (700, 9000, 0),     # a device length past the host's: planned for 700 keys
+])
+def test_device_lengths_rule_over_the_host_copy(host_len, dev_len, splits):
+    """The kernels take a row's keys from the device lengths; the host copy only
+    plans the call (split count, and the page ids fetched before the device
+    length arrives, kept only when the device length puts the partition on the
+    same table slots).  A graph replayed after the lengths advanced relies on it."""
+    import dataclasses
+    c = W.make_paged_case(131, [9000, 2000], **W.GLOBAL_SHAPE)
+    dc = DevCase(c)
+    lens_dev = i32([dev_len, 2000])
+    lens_host = np.array([host_len, 2000], np.int32)
+    out = pskv.decode_attn_splitkv(dc.layout, dc.q, dc.tables, lens_dev, lens_host, c.scale,
+                                   num_splits=splits, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = ref_direct(dataclasses.replace(c, seq_lens=np.array([dev_len, 2000], np.int32)))
+    assert max_err(out, ref) <= TOL
+    assert dc.faults() == 0
