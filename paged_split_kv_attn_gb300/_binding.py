@@ -457,8 +457,10 @@ def decode_attn_tree(layout: Layout, q, page_tables, seq_lens, seq_lens_host, tr
     if q.dim() != 4:
         raise ValueError("q must be [batch, tokens, num_q_heads, head_dim]")
     batch, tokens, hq = q.shape[0], q.shape[1], q.shape[2]
-    if tuple(tree_mask.shape) != (batch, tokens) or tree_mask.element_size() != 8:
-        raise ValueError("tree_mask must be a 64-bit [batch, tokens] tensor")
+    if tuple(tree_mask.shape) != (batch, tokens):
+        raise ValueError("tree_mask must be [batch, tokens]")
+    if tree_mask.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)):
+        raise TypeError("tree_mask must hold 64-bit integers (int64 or uint64 bit patterns)")
     dv = layout.desc.head_dim_v
     if out is None:
         out = torch.empty((batch, tokens, hq, dv), device=q.device,
