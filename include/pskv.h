@@ -418,6 +418,28 @@ int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_
 int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_heads,
                      const int32_t *seq_lens_host, int32_t *num_splits);
 
+/* The workspace a prefill_attn_paged call needs under its plan: the same
+ * arguments' host-visible parts (cu_q_host, seq_lens_host, table_stride,
+ * batch, num_q_heads, window, num_splits, 0 = automatic) are checked and
+ * planned exactly as the call does, and *bytes receives the bytes its
+ * partials take, or 0 when the plan has one partition (each CTA writes its
+ * output directly and no workspace is read).  Nothing is enqueued.  The
+ * answer depends on the device (its SM count) for automatic plans.
+ * Errors: as prefill_attn_paged's host-side checks. */
+int prefill_attn_workspace_bytes(const pskv_layout *layout, const int32_t *cu_q_host,
+                                 const int32_t *seq_lens_host, int32_t table_stride,
+                                 int32_t batch, int32_t num_q_heads, int32_t window,
+                                 int32_t num_splits, size_t *bytes);
+
+/* The workspace a decode_attn_multirow (tree = 0) or decode_attn_tree
+ * (tree = 1) call needs under its plan, with the same meaning as
+ * prefill_attn_workspace_bytes; the two calls can route a window to
+ * different kernels, so the flag selects whose plan. */
+int decode_attn_multirow_workspace_bytes(const pskv_layout *layout, const int32_t *seq_lens_host,
+                                         int32_t table_stride, int32_t batch, int32_t num_tokens,
+                                         int32_t num_q_heads, int32_t tree, int32_t num_splits,
+                                         size_t *bytes);
+
 /* Bytes of the scratch array that decode_attn_splitkv_static uses (16 MiB). */
 #define PSKV_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
 

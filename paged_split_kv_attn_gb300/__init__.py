@@ -12,7 +12,8 @@ from ._binding import (EXPORTS, Layout, PskvError, decode_attn_multirow, decode_
                        merge_partials, merge_partials_workspace_bytes, paged_kv_layout_create,
                        pskv_check_flags, pskv_kernel_launches, pskv_partial_scratch_bytes,
                        pskv_plan_splits,
-                       prefill_attn_paged,
+                       prefill_attn_paged, prefill_attn_workspace_bytes,
+                       decode_attn_multirow_workspace_bytes,
                        pskv_strerror, pskv_version, workspace)
 
 __all__ = ["EXPORTS", "Layout", "PskvError", "decode_attn_multirow", "decode_attn_splitkv",
@@ -23,5 +24,6 @@ __all__ = ["EXPORTS", "Layout", "PskvError", "decode_attn_multirow", "decode_att
            "merge_partials_workspace_bytes", "paged_kv_layout_create", "pskv_check_flags",
            "pskv_kernel_launches",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "pskv_strerror", "pskv_version",
-           "prefill_attn_paged",
+           "prefill_attn_paged", "prefill_attn_workspace_bytes",
+           "decode_attn_multirow_workspace_bytes",
            "workspace"]

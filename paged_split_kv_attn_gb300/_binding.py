@@ -49,6 +49,7 @@ EXPORTS = ("paged_kv_layout_create", "paged_kv_layout_destroy", "kv_append_rows"
            "decode_attn_splitkv", "decode_attn_windowed", "decode_attn_multirow",
            "decode_attn_tree", "prefill_attn_paged", "merge_partials",
            "decode_attn_workspace_bytes", "merge_partials_workspace_bytes",
+           "prefill_attn_workspace_bytes", "decode_attn_multirow_workspace_bytes",
            "pskv_partial_scratch_bytes", "pskv_plan_splits", "decode_attn_splitkv_static",
            "pskv_check_flags", "pskv_strerror", "pskv_last_cuda_error", "pskv_kernel_launches",
            "pskv_version")
@@ -116,6 +117,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.merge_partials.argtypes = [P, P, P, I32, I32, I32, P, I32, P, SZ, P, P, P]
     lib.decode_attn_workspace_bytes.argtypes = [I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.merge_partials_workspace_bytes.argtypes = [I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.prefill_attn_workspace_bytes.argtypes = [P, P, P, I32, I32, I32, I32, I32,
+                                                 ctypes.POINTER(SZ)]
+    lib.decode_attn_multirow_workspace_bytes.argtypes = [P, P, I32, I32, I32, I32, I32, I32,
+                                                         ctypes.POINTER(SZ)]
     lib.pskv_partial_scratch_bytes.argtypes = [I64, I64, I64, I64] + [ctypes.POINTER(SZ)] * 4
     lib.pskv_plan_splits.argtypes = [P, I32, I32, P, ctypes.POINTER(I32)]
     lib.decode_attn_splitkv_static.argtypes = [P, P, P, I32, P, P, I32, I32, F, I32, P, I32, P]
@@ -336,6 +341,33 @@ def merge_partials_workspace_bytes(rows: int, num_splits: int, head_dim_v: int) 
     return int(out.value)
 
 
+def prefill_attn_workspace_bytes(layout: Layout, cu_q_host, seq_lens_host, table_stride: int,
+                                 num_q_heads: int, window: int = 0, num_splits: int = 0) -> int:
+    """Workspace bytes a prefill call needs under its plan (0: one partition, none needed)."""
+    cu_h, lens_h = _host_i32(cu_q_host, "cu_q_host"), _host_i32(seq_lens_host, "seq_lens_host")
+    out = ctypes.c_size_t()
+    _check(load_library().prefill_attn_workspace_bytes(
+        layout.handle, cu_h, lens_h, table_stride, len(lens_h), num_q_heads, int(window),
+        num_splits, ctypes.byref(out)), "prefill_attn_workspace_bytes")
+    return int(out.value)
+
+
+def decode_attn_multirow_workspace_bytes(layout: Layout, seq_lens_host, table_stride: int,
+                                         num_tokens: int, num_q_heads: int, tree: bool = False,
+                                         num_splits: int = 0) -> int:
+    """Workspace bytes a verify-window (or drafted-tree) call needs under its plan."""
+    lens_h = _host_i32(seq_lens_host, "seq_lens_host")
+    out = ctypes.c_size_t()
+    _check(load_library().decode_attn_multirow_workspace_bytes(
+        layout.handle, lens_h, table_stride, len(lens_h), num_tokens, num_q_heads, int(tree),
+        num_splits, ctypes.byref(out)), "decode_attn_multirow_workspace_bytes")
+    return int(out.value)
+
+
+def _planned_workspace(nbytes: int, device):
+    return None if nbytes == 0 else torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
 def pskv_partial_scratch_bytes(batch: int, num_q_heads: int, head_dim_v: int, num_splits: int):
     vals = [ctypes.c_size_t() for _ in range(4)]
     _check(load_library().pskv_partial_scratch_bytes(batch, num_q_heads, head_dim_v, num_splits,
@@ -429,18 +461,20 @@ def decode_attn_multirow(layout: Layout, q, page_tables, seq_lens, seq_lens_host
     if out is None:
         out = torch.empty((batch, tokens, hq, dv), device=q.device,
                           dtype=out_dtype or torch.bfloat16)
-    if workspace is None:
-        workspace = _alloc_workspace(batch * tokens, hq, dv, num_splits, q.device)
     lens_h = _host_i32(seq_lens_host, "seq_lens_host")
     if len(lens_h) != batch:
         raise ValueError("seq_lens_host must have one entry per row")
+    if workspace is None:
+        workspace = _planned_workspace(decode_attn_multirow_workspace_bytes(
+            layout, lens_h, page_tables.shape[1], tokens, hq, False, num_splits), q.device)
     opts = _opts(merge_group, events)
     _check(lib.decode_attn_multirow(
         layout.handle, _dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
         page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32), batch, tokens, hq,
-        float(scale), num_splits, _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _dev(out, "out"), _dtype_code(out.dtype),
-        None if opts is None else ctypes.byref(opts), _stream(stream)), "decode_attn_multirow")
+        float(scale), num_splits, None if workspace is None else _dev(workspace, "workspace"),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(out, "out"), _dtype_code(out.dtype), None if opts is None else ctypes.byref(opts),
+        _stream(stream)), "decode_attn_multirow")
     return out
 
 
@@ -465,17 +499,19 @@ def decode_attn_tree(layout: Layout, q, page_tables, seq_lens, seq_lens_host, tr
     if out is None:
         out = torch.empty((batch, tokens, hq, dv), device=q.device,
                           dtype=out_dtype or torch.bfloat16)
-    if workspace is None:
-        workspace = _alloc_workspace(batch * tokens, hq, dv, num_splits, q.device)
     lens_h = _host_i32(seq_lens_host, "seq_lens_host")
     if len(lens_h) != batch:
         raise ValueError("seq_lens_host must have one entry per row")
+    if workspace is None:
+        workspace = _planned_workspace(decode_attn_multirow_workspace_bytes(
+            layout, lens_h, page_tables.shape[1], tokens, hq, True, num_splits), q.device)
     opts = _opts(merge_group, events)
     _check(lib.decode_attn_tree(
         layout.handle, _dev(q, "q", layout.dtype), _dev(page_tables, "page_tables", torch.int32),
         page_tables.shape[1], lens_h, _dev(seq_lens, "seq_lens", torch.int32),
         _dev(tree_mask, "tree_mask"), batch, tokens, hq, float(scale), num_splits,
-        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        None if workspace is None else _dev(workspace, "workspace"),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
         _dev(out, "out"), _dtype_code(out.dtype), None if opts is None else ctypes.byref(opts),
         _stream(stream)), "decode_attn_tree")
     return out
@@ -503,7 +539,8 @@ def prefill_attn_paged(layout: Layout, q, cu_q, cu_q_host, page_tables, seq_lens
     if len(cu_h) != batch + 1:
         raise ValueError("cu_q_host must have batch + 1 entries")
     if workspace is None and num_splits != 1:
-        workspace = _alloc_workspace(total, hq, dv, num_splits, q.device)
+        workspace = _planned_workspace(prefill_attn_workspace_bytes(
+            layout, cu_h, lens_h, page_tables.shape[1], hq, window, num_splits), q.device)
     opts = _opts(merge_group, events)
     _check(lib.prefill_attn_paged(
         layout.handle, _dev(q, "q", layout.dtype), cu_h, _dev(cu_q, "cu_q", torch.int32),

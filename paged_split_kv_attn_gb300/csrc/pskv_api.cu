@@ -134,17 +134,23 @@ struct QuerySpec {
   const int32_t *cu_q = nullptr;       // [B + 1] device offsets
   int window = 0;
   const uint64_t *tree_mask = nullptr;  // [B][tokens] ancestor masks of a drafted tree, or null
+  bool tree_plan = false;               // plan a drafted tree without its masks (size queries)
 };
 
+// Checks, plans and enqueues one call.  With `plan_bytes` set it only checks
+// the host-visible arguments and plans: *plan_bytes = the workspace the plan
+// needs (0 when one partition writes the output directly); device pointers
+// are not required and nothing is enqueued.
 int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_tables,
                   int32_t table_stride, const int32_t *seq_lens_host, const int32_t *seq_lens,
                   const int32_t *first_pos, const int32_t *window_lo, bool windowed,
                   int32_t batch, const QuerySpec &qs, int32_t num_q_heads, float scale,
                   int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
-                  int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream) {
-  if (!layout || !q || !page_tables || !seq_lens_host || !seq_lens || !out)
-    return PSKV_ERR_INVALID_ARG;
-  if (windowed && (!first_pos || !window_lo)) return PSKV_ERR_INVALID_ARG;
+                  int32_t out_dtype, const pskv_decode_opts *opts, pskv_stream_t stream,
+                  size_t *plan_bytes = nullptr) {
+  if (!layout || !seq_lens_host) return PSKV_ERR_INVALID_ARG;
+  if (!plan_bytes && (!q || !page_tables || !seq_lens || !out)) return PSKV_ERR_INVALID_ARG;
+  if (windowed && !plan_bytes && (!first_pos || !window_lo)) return PSKV_ERR_INVALID_ARG;
   if (batch < 1 || batch > 65535 || num_q_heads < 1 || table_stride < 1) return PSKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PSKV_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > PSKV_MAX_SPLITS) return PSKV_ERR_INVALID_ARG;
@@ -157,7 +163,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   const int kernel = pick_kernel(d.kv_dtype, d.head_dim_v, group, d.format);
   const bool folded = d.format == PSKV_FORMAT_FOLDED;
   const bool varlen = qs.cu_q_host != nullptr;
-  if (varlen && !qs.cu_q) return PSKV_ERR_INVALID_ARG;
+  if (varlen && !qs.cu_q && !plan_bytes) return PSKV_ERR_INVALID_ARG;
   // Prefill of bf16 split pools at head dim 256 or 512 runs on the
   // query-major tensor-memory kernel: blocks of 128 query columns (any
   // power-of-two group up to 128 query heads per KV head), one CTA (head dim
@@ -174,7 +180,7 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   int64_t longest = 0;  // the host lengths (checked below); the routing only reads them
   for (int32_t b = 0; b < batch; ++b)
     longest = seq_lens_host[b] > longest ? seq_lens_host[b] : longest;
-  const bool tree = qs.tree_mask != nullptr;
+  const bool tree = qs.tree_mask != nullptr || qs.tree_plan;
   if (tree && (varlen || windowed)) return PSKV_ERR_INVALID_ARG;
   // drafted trees run on the split-KV kernels and the key-major kernel (both
   // take the tokens' masks), never on the query-major one
@@ -248,6 +254,10 @@ int decode_common(const pskv_layout *layout, const void *q, const int32_t *page_
   WorkspacePlan w;
   if ((rc = plan_workspace(rows, num_q_heads, d.head_dim_v, P, mgroup, &w))) return rc;
   if (w.groups > kMaxGroups) return PSKV_ERR_INVALID_ARG;
+  if (plan_bytes) {
+    *plan_bytes = direct ? 0 : w.total;
+    return PSKV_OK;
+  }
   if (!direct && (!workspace || workspace_bytes < w.total)) return PSKV_ERR_WORKSPACE_TOO_SMALL;
 
   char *ws = static_cast<char *>(workspace);
@@ -563,6 +573,33 @@ int prefill_attn_paged(const pskv_layout *layout, const void *q, const int32_t *
   return decode_common(layout, q, page_tables, table_stride, seq_lens_host, seq_lens, nullptr,
                        nullptr, false, batch, qs, num_q_heads, scale, num_splits, workspace,
                        workspace_bytes, out, out_dtype, opts, stream);
+}
+
+int prefill_attn_workspace_bytes(const pskv_layout *layout, const int32_t *cu_q_host,
+                                 const int32_t *seq_lens_host, int32_t table_stride,
+                                 int32_t batch, int32_t num_q_heads, int32_t window,
+                                 int32_t num_splits, size_t *bytes) {
+  if (!bytes || !cu_q_host) return PSKV_ERR_INVALID_ARG;
+  QuerySpec qs;
+  qs.cu_q_host = cu_q_host;
+  qs.window = window;
+  return decode_common(layout, nullptr, nullptr, table_stride, seq_lens_host, nullptr, nullptr,
+                       nullptr,
+                       false, batch, qs, num_q_heads, 1.f, num_splits, nullptr, 0, nullptr,
+                       PSKV_DTYPE_BF16, nullptr, nullptr, bytes);
+}
+
+int decode_attn_multirow_workspace_bytes(const pskv_layout *layout, const int32_t *seq_lens_host,
+                                         int32_t table_stride, int32_t batch, int32_t num_tokens,
+                                         int32_t num_q_heads, int32_t tree, int32_t num_splits,
+                                         size_t *bytes) {
+  if (!bytes) return PSKV_ERR_INVALID_ARG;
+  QuerySpec qs;
+  qs.tokens = num_tokens;
+  qs.tree_plan = tree != 0;
+  return decode_common(layout, nullptr, nullptr, table_stride, seq_lens_host, nullptr, nullptr,
+                       nullptr, false, batch, qs, num_q_heads, 1.f, num_splits, nullptr, 0,
+                       nullptr, PSKV_DTYPE_BF16, nullptr, nullptr, bytes);
 }
 
 int merge_partials(const float *m, const float *l, const float *o, int32_t rows,

@@ -281,3 +281,38 @@ def test_merge_refusals(lib):
     assert lib.merge_partials(0x10, 0x10, 0x20, 4, 8, 512, 0x30, 0, None, 0, None,
                               ctypes.byref(opts), None) == B.PSKV_ERR_INVALID_ARG
     del P
+
+
+def test_workspace_size_queries_follow_the_plan(lib):
+    """With an explicit split count the planning is host-only: the size queries
+    answer the bytes of the plan's partials (0 for one partition, which writes
+    its output directly) and refuse what the call would refuse."""
+    h = _layout(lib)
+    out = ctypes.c_size_t()
+    try:
+        lh = (ctypes.c_int32 * 2)(900, 50)
+        ch = (ctypes.c_int32 * 3)(0, 40, 70)
+        for splits, rows_bytes in ((1, 0), (2, pskv.decode_attn_workspace_bytes(70, 32, 512, 2)),
+                                   (5, pskv.decode_attn_workspace_bytes(70, 32, 512, 5))):
+            assert lib.prefill_attn_workspace_bytes(h, ch, lh, 4, 2, 32, 0, splits,
+                                                    ctypes.byref(out)) == 0
+            assert out.value == rows_bytes
+        bad = (ctypes.c_int32 * 3)(0, 40, 91)  # the second row: 51 tokens on 50 keys
+        assert lib.prefill_attn_workspace_bytes(h, bad, lh, 4, 2, 32, 0, 2,
+                                                ctypes.byref(out)) == B.PSKV_ERR_INVALID_ARG
+        assert lib.prefill_attn_workspace_bytes(h, ch, lh, 4, 2, 32, 0, 2,
+                                                None) == B.PSKV_ERR_INVALID_ARG
+        # verify windows and drafted trees: batch x tokens rows of partials
+        for tree in (0, 1):
+            assert lib.decode_attn_multirow_workspace_bytes(h, lh, 4, 2, 3, 32, tree, 7,
+                                                            ctypes.byref(out)) == 0
+            assert out.value == pskv.decode_attn_workspace_bytes(6, 32, 512, 7)
+            assert lib.decode_attn_multirow_workspace_bytes(h, lh, 4, 2, 3, 32, tree, 1,
+                                                            ctypes.byref(out)) == 0
+            assert out.value == 0
+        assert lib.decode_attn_multirow_workspace_bytes(h, lh, 4, 2, 65, 32, 0, 7,
+                                                        ctypes.byref(out)) == B.PSKV_ERR_INVALID_ARG
+        assert lib.decode_attn_multirow_workspace_bytes(None, lh, 4, 2, 3, 32, 0, 7,
+                                                        ctypes.byref(out)) == B.PSKV_ERR_INVALID_ARG
+    finally:
+        lib.paged_kv_layout_destroy(h)

@@ -130,3 +130,28 @@ def test_device_lengths_rule_over_the_host_copy(host_len, dev_len, splits):
     ref = ref_direct(dataclasses.replace(c, seq_lens=np.array([dev_len, 2000], np.int32)))
     assert max_err(out, ref) <= TOL
     assert dc.faults() == 0
+
+
+def test_workspace_queries_give_the_automatic_plans_bytes():
+    """The size queries plan exactly as the calls: a long prefill chunk and a
+    verify window on the key-major kernel (one CTA per SM per KV head: 38
+    partitions on 152 SMs), answered on the device's own SM count."""
+    c = W.global_case(40002, seed=132)
+    dc = DevCase(c)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    cu = np.array([0, 512], np.int32)
+    assert pskv.prefill_attn_workspace_bytes(dc.layout, cu, c.seq_lens, c.page_tables.shape[1],
+                                             32) == 0  # the blocks fill the SM pairs: one partition
+    want = pskv.decode_attn_workspace_bytes(4, 32, 512, n_sm // 4)
+    assert pskv.decode_attn_multirow_workspace_bytes(dc.layout, c.seq_lens,
+                                                     c.page_tables.shape[1], 4, 32) == want
+    # and the call runs in exactly that workspace
+    q = torch.randn(1, 4, 32, 512, device="cuda").to(torch.bfloat16)
+    ws = torch.empty(want, dtype=torch.uint8, device="cuda")
+    pskv.decode_attn_multirow(dc.layout, q, dc.tables, dc.lens, c.seq_lens, c.scale, workspace=ws)
+    with pytest.raises(pskv.PskvError) as e:
+        pskv.decode_attn_multirow(dc.layout, q, dc.tables, dc.lens, c.seq_lens, c.scale,
+                                  workspace=ws[:want - 256])
+    assert e.value.code == pskv.PSKV_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert dc.faults() == 0
