@@ -622,6 +622,36 @@ def r1(x):
     return None if x is None else round(float(x), 1)
 
 
+LINE_BUDGET = 2900  # characters of the printed line: a log tail keeps about 3,000
+
+
+def make_line(args, world, value, ms, launches, roofline, e2e, clock_info, step_ms, detail,
+              sweep, prefill) -> dict:
+    """The printed JSON line: the contract's keys, then the per-call figures in
+    compact rows (alone, cold L2: us, GB/s, % of 8 TB/s, % of the measured copy
+    peak, splits, partial-kernel us; then us per call back to back), the split
+    sweep (us at each count, then the best count) and prefill TFLOP/s."""
+    per_call = {"cols": ["us", "GBps", "pct_8TBs", "pct_meas", "P", "partial_us", "us_b2b"]}
+    for name, d in detail.items():
+        per_call[name] = [r1(d["us_per_call"]), round(d["GBps_per_call"]),
+                          r1(100 * d["frac_of_8TBs"]), r1(100 * d["frac_of_measured"]),
+                          d["splits"], r1(d["partial_us"]), r1(d["us_stream"])]
+    line = {"metric": METRIC, "value": r1(value), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(args), "gpu_launches": int(launches),
+            "roofline": roofline, "e2e": e2e, "clocks": clock_info, "step_ms": step_ms,
+            "per_call": per_call}
+    if sweep:
+        line["sweep_us"] = {"P": list(args.sweep)}
+        for name, sw in sweep.items():
+            line["sweep_us"][name] = [r1(sw["us"][p]) for p in args.sweep] + [sw["best_splits"]]
+    if prefill:
+        line["prefill_tflops"] = {k.replace("prefill_", ""): round(v["tflops"]) for k, v in
+                                  prefill.items()}
+    return line
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -927,34 +957,15 @@ def main():
                 "traffic": None if traffic_per_key is None
                 else round(traffic_per_key * keys_per_launch)}
 
-    # per call (alone, cold L2): us, GB/s, % of 8 TB/s, % of the measured copy
-    # peak, splits, partial-kernel us; then us per call back to back (cold pools)
-    per_call = {"cols": ["us", "GBps", "pct_8TBs", "pct_meas", "P", "partial_us", "us_b2b"]}
-    for name, d in detail.items():
-        per_call[name] = [r1(d["us_per_call"]), round(d["GBps_per_call"]),
-                          r1(100 * d["frac_of_8TBs"]), r1(100 * d["frac_of_measured"]),
-                          d["splits"], r1(d["partial_us"]), r1(d["us_stream"])]
-    line = {"metric": METRIC, "value": r1(value), "unit": "GB/s", "n_gpus": dist.world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_dict(args), "gpu_launches": int(launches),
-            "roofline": roofline,
-            "e2e": {"value": r1(whole_job_gbps(step_bytes, dist.world, e2e_ms)), "unit": "GB/s",
-                    "ms_per_step": round(e2e_ms, 5),
-                    "h2d_bytes_per_step": packed.host_in.numel(),
-                    "d2h_bytes_per_step": packed.host_out[0].numel(),
-                    "how": "eager C-ABI calls; one packed copy in, one out per step"},
-            "clocks": clock_info,
-            "step_ms": {"graph": round(ms, 5), "eager": round(eager_ms, 5),
-                        "prep": None if prep_ms is None else round(prep_ms, 5)},
-            "per_call": per_call}
-    if sweep:
-        line["sweep_us"] = {"P": list(args.sweep)}
-        for name, sw in sweep.items():
-            line["sweep_us"][name] = [r1(sw["us"][p]) for p in args.sweep] + [sw["best_splits"]]
-    if prefill:
-        line["prefill_tflops"] = {k.replace("prefill_", ""): round(v["tflops"]) for k, v in
-                                  prefill.items()}
+    line = make_line(args, dist.world, value, ms, launches, roofline,
+                     {"value": r1(whole_job_gbps(step_bytes, dist.world, e2e_ms)), "unit": "GB/s",
+                      "ms_per_step": round(e2e_ms, 5),
+                      "h2d_bytes_per_step": packed.host_in.numel(),
+                      "d2h_bytes_per_step": packed.host_out[0].numel(),
+                      "how": "eager C-ABI calls; one packed copy in, one out per step"},
+                     clock_info, {"graph": round(ms, 5), "eager": round(eager_ms, 5),
+                                  "prep": None if prep_ms is None else round(prep_ms, 5)},
+                     detail, sweep, prefill)
     if dist.rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline([c.case for c in calls], args.cpu_seconds)
         cb["value"] = round(cb["value"], 3)
