@@ -182,3 +182,25 @@ def test_refusals():
     with pytest.raises(pskv.PskvError) as e:  # f32 pools run on the CUDA-core consumer
         run(dcf, qf, dev_masks(masks_of(f32, 2, 1)))
     assert e.value.code == pskv.PSKV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("tokens,length", [(8, 9092), (16, 9100), (5, 12419)])
+def test_key_major_window_across_two_tiles(tokens, length):
+    """The drafted window straddles a 128-key tile boundary (its first key at
+    row 124 or 126 of a tile): each softmax thread meets its window key in one
+    tile or the next, and chains still equal the causal window bit for bit."""
+    assert (length - tokens) % 128 > 128 - tokens
+    hq, hkv = (16, 2) if tokens == 8 else (8, 2) if tokens == 16 else (32, 4)
+    case = small(140 + tokens, [length, 9000], hq, hkv, 512, 256)
+    check(case, tokens, splits=(0, 3), seed=tokens)
+    dc, q, md = check(case, tokens, splits=(0,), chain=True)
+    a = run(dc, q, md, 0)
+    b = pskv.decode_attn_multirow(dc.layout, q, dc.tables, dc.lens, case.seq_lens, case.scale,
+                                  out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_widest_tree_on_the_key_major_kernel():
+    """64 drafted tokens of one query head per KV head: 64 columns per KV head."""
+    check(small(145, [8300, 9000], 4, 4, 256, 64), 64, splits=(0, 2), seed=9)
