@@ -418,7 +418,10 @@ int pskv_partial_scratch_bytes(int64_t batch, int64_t num_q_heads, int64_t head_
 int pskv_plan_splits(const pskv_layout *layout, int32_t batch, int32_t num_q_heads,
                      const int32_t *seq_lens_host, int32_t *num_splits);
 
-/* The workspace a prefill_attn_paged call needs under its plan: the same
+/* The workspace a prefill_attn_paged call needs under its plan.  A sizing
+ * helper: the pages give the workspace only as the partial buffer's byte
+ * contract (gem design, "Candidate ownership and storage"), which this
+ * applies to the plan's split count.  The same
  * arguments' host-visible parts (cu_q_host, seq_lens_host, table_stride,
  * batch, num_q_heads, window, num_splits, 0 = automatic) are checked and
  * planned exactly as the call does, and *bytes receives the bytes its
@@ -433,8 +436,9 @@ int prefill_attn_workspace_bytes(const pskv_layout *layout, const int32_t *cu_q_
 
 /* The workspace a decode_attn_multirow (tree = 0) or decode_attn_tree
  * (tree = 1) call needs under its plan, with the same meaning as
- * prefill_attn_workspace_bytes; the two calls can route a window to
- * different kernels, so the flag selects whose plan. */
+ * prefill_attn_workspace_bytes (the same sizing helper, no passage of its
+ * own); the two calls can route a window to different kernels, so the flag
+ * selects whose plan. */
 int decode_attn_multirow_workspace_bytes(const pskv_layout *layout, const int32_t *seq_lens_host,
                                          int32_t table_stride, int32_t batch, int32_t num_tokens,
                                          int32_t num_q_heads, int32_t tree, int32_t num_splits,
