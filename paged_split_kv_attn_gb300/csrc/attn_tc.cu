@@ -740,10 +740,13 @@ __device__ __forceinline__ void write_rows(const TcArgs &a, const TcPlan &pl, ui
       }
     } else {
       float4 *dst = reinterpret_cast<float4 *>(a.ws_o + prow * DT + col0 + 32 * c);
+      const uint64_t keep = make_evict_last_policy();
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        st_keep(dst + q,
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])),
+                keep);
     }
   }
   if (!real || col0 != 0) return;

@@ -694,8 +694,9 @@ __device__ __forceinline__ void write_ml(const TcArgs &a, const VPlan &pl, const
     if (empty) raise_fault(a.status, PSKV_FAULT_EMPTY_ROW);
   } else {
     const size_t prow = qrow * a.num_splits + pl.p;
-    a.ws_m[prow] = empty ? -CUDART_INF_F : m_sm[kr] * kLn2;
-    a.ws_l[prow] = empty ? 0.f : l_sm[kr];
+    const uint64_t keep = make_evict_last_policy();
+    st_keep(a.ws_m + prow, empty ? -CUDART_INF_F : m_sm[kr] * kLn2, keep);
+    st_keep(a.ws_l + prow, empty ? 0.f : l_sm[kr], keep);
   }
 }
 
@@ -780,13 +781,14 @@ __device__ __forceinline__ bool write_cols(const TcArgs &a, const VPlan &pl, uns
   }
   if (!meet(bars, ph, abort_flag, a.status)) return false;
   const size_t *coff = reinterpret_cast<const size_t *>(sm + L::kOffCOff);
+  const uint64_t keep = make_evict_last_policy();
 #pragma unroll 4
   for (int e = kr; e < pl.ncols * (DT / 4); e += 128) {
     const int c = e / (DT / 4), q = e % (DT / 4);
     const float4 y = *reinterpret_cast<const float4 *>(stage + c * DT + 4 * q);
     const size_t off = coff[c] + 4 * q;
     if (!a.direct)
-      *reinterpret_cast<float4 *>(a.ws_o + off) = y;
+      st_keep(reinterpret_cast<float4 *>(a.ws_o + off), y, keep);
     else if (a.out_dtype == PSKV_DTYPE_BF16)
       *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) + off) =
           make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));

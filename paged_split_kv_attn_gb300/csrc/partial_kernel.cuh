@@ -486,15 +486,16 @@ struct MmaConsumer {
         }
         const size_t row = qrow * P + p;
         float *dst = a.ws_o + row * D + d0 + r;
+        const uint64_t keep = make_evict_last_policy();
 #pragma unroll
         for (int j = 0; j < KSP; ++j) {
-          dst[16 * j] = o[nt][j][e];
-          dst[16 * j + 8] = o[nt][j][2 + e];
+          st_keep(dst + 16 * j, o[nt][j][e], keep);
+          st_keep(dst + 16 * j + 8, o[nt][j][2 + e], keep);
         }
         if (warp == 0 && r == 0) {
           const float mm = e ? m1[nt] : m0[nt];
-          a.ws_m[row] = mm == -CUDART_INF_F ? -CUDART_INF_F : mm * kLn2;
-          a.ws_l[row] = e ? l1[nt] : l0[nt];
+          st_keep(a.ws_m + row, mm == -CUDART_INF_F ? -CUDART_INF_F : mm * kLn2, keep);
+          st_keep(a.ws_l + row, e ? l1[nt] : l0[nt], keep);
         }
       }
     }
@@ -722,8 +723,9 @@ __device__ __forceinline__ void merge_warp_states(const C &cons, const PartialAr
       weight[w * G + h] = wt;
       L += wt * red_l[w * G + h];
     }
-    a.ws_m[row0 + (size_t)h * P] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * kLn2;
-    a.ws_l[row0 + (size_t)h * P] = L;
+    const uint64_t keep = make_evict_last_policy();
+    st_keep(a.ws_m + row0 + (size_t)h * P, (M == -CUDART_INF_F) ? -CUDART_INF_F : M * kLn2, keep);
+    st_keep(a.ws_l + row0 + (size_t)h * P, L, keep);
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += NT) {
@@ -734,7 +736,7 @@ __device__ __forceinline__ void merge_warp_states(const C &cons, const PartialAr
       const float wt = weight[w * G + h];
       if (wt != 0.f) acc = fmaf(o_s[(w * G + h) * D + d], wt, acc);
     }
-    a.ws_o[(row0 + (size_t)h * P) * D + d] = acc;
+    st_keep(a.ws_o + (row0 + (size_t)h * P) * D + d, acc, make_evict_last_policy());
   }
 }
 
@@ -868,8 +870,9 @@ __global__ void __launch_bounds__((C::kWarps + 1) * 32, C::kMinBlocks)
     }
     for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
       const size_t row = (((size_t)rp.r0 + i / G) * a.num_q_heads + h0 + i % G) * P + p;
-      a.ws_m[row] = -CUDART_INF_F;
-      a.ws_l[row] = 0.f;
+      const uint64_t keep = make_evict_last_policy();
+      st_keep(a.ws_m + row, -CUDART_INF_F, keep);
+      st_keep(a.ws_l + row, 0.f, keep);
     }
     return;
   }

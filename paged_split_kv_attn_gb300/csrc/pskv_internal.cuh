@@ -260,6 +260,25 @@ __device__ __forceinline__ uint64_t make_evict_first_policy() {
   return p;
 }
 
+// Partials (m, l, o) are read back by the merge right after the kernel that
+// writes them; stored with an L2 evict-last policy they stay in L2 while the
+// rest of the K/V stream passes (written plainly, most of them were written
+// back to DRAM before the merge ran, and the merge read them from DRAM).
+__device__ __forceinline__ uint64_t make_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_keep(float *p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_keep(float4 *p, float4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
                                         uint32_t &a3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
