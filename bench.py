@@ -19,11 +19,14 @@ step, far beyond the 129 MB L2), so no call finds its data in L2.  The timed
 steps are replays of CUDA graphs captured once (one per pool copy) from the
 same library calls, as a decode engine runs its step.  The partial kernels'
 durations for the roofline come from a further pass of K eager steps with
-CUDA events recorded around each partial launch.  Per call (each call alone,
-replayed from its own graphs, a 256 MB read between calls so that L2 is
-cold): microseconds, GB/s, the fraction of 8 TB/s and of the measured copy
-bandwidth; the split count swept over 8..256 at every global context with
-the best one reported.  e2e: the same step through the library's C entry
+CUDA events recorded around each partial launch.  Per call, with a cold L2
+(a 256 MB read before every call): microseconds -- one graph of ten (read,
+call) pairs less ten reads alone, per call; and the call's own graph replayed
+alone between two events (us_iso, which adds an idle GPU's event and launch
+latency) -- GB/s, the fraction of 8 TB/s and of the measured copy bandwidth,
+and the time per call back to back (a graph of calls over pool copies that
+hold more than twice the L2); the split count swept over 8..256 at every
+global context with the best one reported.  e2e: the same step through the library's C entry
 points (eager calls, no graphs), with each step's inputs copied in from
 pinned host memory and its outputs copied back inside the timed region.
 
@@ -628,12 +631,14 @@ LINE_BUDGET = 2900  # characters of the printed line: a log tail keeps about 3,0
 def make_line(args, world, value, ms, launches, roofline, e2e, clock_info, step_ms, detail,
               sweep, prefill) -> dict:
     """The printed JSON line: the contract's keys, then the per-call figures in
-    compact rows (alone, cold L2: us, GB/s, % of 8 TB/s, % of the measured copy
-    peak, splits, partial-kernel us; then us per call back to back), the split
+    compact rows (cold L2: us from a sequence of reads and calls, us of the call
+    alone between events, GB/s, % of 8 TB/s, % of the measured copy peak, splits,
+    partial-kernel us; then us per call back to back), the split
     sweep (us at each count, then the best count) and prefill TFLOP/s."""
-    per_call = {"cols": ["us", "GBps", "pct_8TBs", "pct_meas", "P", "partial_us", "us_b2b"]}
+    per_call = {"cols": ["us", "us_iso", "GBps", "pct_8TBs", "pct_meas", "P", "partial_us",
+                         "us_b2b"]}
     for name, d in detail.items():
-        per_call[name] = [r1(d["us_per_call"]), round(d["GBps_per_call"]),
+        per_call[name] = [r1(d["us_per_call"]), r1(d["us_isolated"]), round(d["GBps_per_call"]),
                           r1(100 * d["frac_of_8TBs"]), r1(100 * d["frac_of_measured"]),
                           d["splits"], r1(d["partial_us"]), r1(d["us_stream"])]
     line = {"metric": METRIC, "value": r1(value), "unit": "GB/s", "n_gpus": world,
@@ -823,9 +828,51 @@ def main():
     # buffer is READ between calls: reads leave no dirty lines to write back)
     flush = torch.ones(int(256e6) // 4, dtype=torch.float32, device=dev)
 
-    def per_call_us(c, reps):
-        """One call alone: its graph replayed after a 256 MB read (cold L2), the
-        mean over `reps` replays (the event clock ticks in about 1 us steps)."""
+    def graph_of(fn):
+        """fn() captured once as a CUDA graph (after one run outside capture)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def replay_us(g, reps=7):
+        """Median duration of a graph replay between events on the stream."""
+        ts = []
+        for _ in range(reps):
+            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b.record(stream)
+            g.replay()
+            e.record(stream)
+            torch.cuda.synchronize()
+            ts.append(b.elapsed_time(e) * 1e3)
+        return statistics.median(ts)
+
+    SEQ = 10  # (read, call) pairs per graph in the cold per-call figure
+    g_reads = graph_of(lambda: [flush.sum() for _ in range(SEQ)])
+    read_us = replay_us(g_reads) / SEQ  # one 256 MB read, as it runs inside the sequence
+
+    def per_call_us(c, reps, seq=SEQ):
+        """One call at a time with a cold L2, two ways.
+
+        us: one graph of `seq` (256 MB read, call) pairs over the rotating pool
+        copies, its replay time less that of `seq` reads alone, per call -- the
+        call's device time with a cold L2 and cold code, its launches queued as
+        an engine queues them.
+        us_iso: the call's own graph replayed alone after a 256 MB read, between
+        two events (mean of `reps`; the event clock ticks in ~1 us steps); this
+        adds the event and graph-launch latency of an idle GPU (a graph of one
+        trivial kernel measures ~5-7 us this way)."""
+        g = graph_of(lambda: [(flush.sum(), c.run(r % ROTATE)) for r in range(seq)])
+        us_seq = (replay_us(g) - read_us * seq) / seq
+        del g
         cg, _ = capture([c])
         times = []
         for it in range(reps):
@@ -837,7 +884,7 @@ def main():
             torch.cuda.synchronize()
             times.append(b.elapsed_time(e) * 1e3)
         del cg
-        return statistics.mean(times)
+        return us_seq, statistics.mean(times)
 
     l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 << 20
 
@@ -874,12 +921,12 @@ def main():
 
     reps = max(20, min(args.steps, 50))
     for c in calls + extra:
-        us = per_call_us(c, reps)
+        us, us_iso = per_call_us(c, reps)
         us_s = stream_us(c)
         gbps = c.bytes / (us * 1e-6) / 1e9
         detail[c.name].update({
             "us_stream": us_s, "GBps_stream": c.bytes / (us_s * 1e-6) / 1e9,
-            "us_per_call": us, "GBps_per_call": gbps,
+            "us_per_call": us, "GBps_per_call": gbps, "us_isolated": us_iso,
             "frac_of_8TBs": gbps / NOMINAL_HBM_GBS, "frac_of_measured": gbps / peak,
             "splits": c.splits or (pskv.pskv_plan_splits(c.layouts[0], c.case.num_q_heads,
                                                          c.lens_host)
@@ -896,7 +943,7 @@ def main():
             for p in args.sweep:
                 c.splits = p
                 c.ws = pskv.workspace(1, 32, 512, p, dev)
-                res[p] = per_call_us(c, 20)
+                res[p] = per_call_us(c, 20, seq=6)[0]
             c.splits, c.ws = s0, ws0
             best = min(res, key=res.get)
             sweep[c.name] = {"us": res, "best_splits": best, "best_us": res[best],

@@ -18,7 +18,8 @@ def test_the_default_line_fits_the_budget():
              + [f"verify_{args.verify_context}x{t}" for t in args.verify_tokens]
              + [f"tree_{args.verify_context}x{t}" for t in args.tree_tokens] + ["ragged16"])
     big = dict(us_per_call=1234.56, GBps_per_call=12345.6, frac_of_8TBs=1.2345,
-               frac_of_measured=1.2345, splits=1024, partial_us=1234.56, us_stream=1234.56)
+               frac_of_measured=1.2345, splits=1024, partial_us=1234.56, us_stream=1234.56,
+               us_isolated=1234.56)
     detail = {n: dict(big) for n in names}
     sweep = {n: {"us": {p: 12345.67 for p in args.sweep}, "best_splits": 256}
              for n in names if n.startswith("global")}
