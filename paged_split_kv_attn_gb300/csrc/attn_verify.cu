@@ -557,19 +557,24 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
         x[c] = vis ? x[c] : -CUDART_INF_F;
       }
     }
-    // ---- does some column's reference max have to move?
-    bool rise = false;
+    // ---- does some column's reference max have to move?  (The first tile sets
+    // every column's reference: no vote.)
+    bool moved = true;
+    if (j > 0) {
+      bool rise = false;
 #pragma unroll
-    for (int c = 0; c < NC; c += 4) {
-      const float4 m4 = *reinterpret_cast<const float4 *>(m_sm + c);
-      rise |= x[c] > m4.x + kSlack || x[c + 1] > m4.y + kSlack || x[c + 2] > m4.z + kSlack ||
-              x[c + 3] > m4.w + kSlack;
+      for (int c = 0; c < NC; c += 4) {
+        const float4 m4 = *reinterpret_cast<const float4 *>(m_sm + c);
+        rise |= x[c] > m4.x + kSlack || x[c + 1] > m4.y + kSlack || x[c + 2] > m4.z + kSlack ||
+                x[c + 3] > m4.w + kSlack;
+      }
+      const int vote = __any_sync(0xffffffffu, rise);
+      if (lane == 0) flags[4 * r + w] = vote;
+      ok = meet(bars, ph, abort_flag, a.status) && ok;
+      moved = ok && (flags[4 * r] | flags[4 * r + 1] | flags[4 * r + 2] | flags[4 * r + 3]);
     }
-    const int vote = __any_sync(0xffffffffu, rise);
-    if (lane == 0) flags[4 * r + w] = vote;
-    ok = meet(bars, ph, abort_flag, a.status) && ok;
     if (!ok || *abort_flag) return false;
-    if (flags[4 * r] | flags[4 * r + 1] | flags[4 * r + 2] | flags[4 * r + 3]) {
+    if (moved) {
       // the tile's column maxima: per warp, then over the four warps
       float mx[NC / 32];
       fold<true, NC>(x, lane, mx);
@@ -594,9 +599,9 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
       bool resc_any = false;
 #pragma unroll
       for (int i = 0; i < NC / 32; ++i) resc_any = resc_any || flags[8 + i];
-      // this thread's shares of the sums, then (a reference moved) the O^T columns once
-      // the values of tile j - 1 are in
-      if (!resc_any || j == 0) {
+      // this thread's shares of the sums (still 0 at the first tile), then (a
+      // reference moved) the O^T columns once the values of tile j - 1 are in
+      if (j > 0 && !resc_any) {
 #pragma unroll 1
         for (int h = 0; h < NC / 32; ++h) {
           uint32_t v[32];
@@ -609,7 +614,7 @@ __device__ __forceinline__ bool softmax_loop(const TcArgs &a, const VPlan &pl, u
             v[c] = __float_as_uint(__uint_as_float(v[c]) * a_sm[32 * h + c]);
           tc::st32(addr, v);
         }
-      } else {
+      } else if (j > 0) {
         if (!wait_all(kPvDone + (j - 1) % L::kPBufs, ((j - 1) / L::kPBufs) & 1)) return false;
         tc::fence_after_sync();
         // the O^T blocks (hi and lo halves), then the sums: column q of them belongs to
