@@ -117,6 +117,7 @@ struct VLay {
   static constexpr int kOffFlag = kOffA + NC * 4;          // int[2][4] votes, int[4] rescale
   static constexpr int kOffSlot = kOffFlag + 16 * 4;
   static constexpr int kOffCOff = kOffP;  // size_t[NC] output row offsets, once P^T is done
+  static constexpr int kOffScale = kOffP + NC * 8;  // float[NC] output scales, likewise
   static constexpr int kOffAbort = kOffSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment of the dynamic base
   static_assert(kRingV >= 2 && kOffBar <= kDataBytes, "stages");
@@ -746,7 +747,7 @@ __device__ __forceinline__ bool write_cols(const TcArgs &a, const VPlan &pl, uns
   static_assert(NC * DT * 4 <= L::kRingK * kChunkBytes + L::kRingV * kChunkBytes, "staging");
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3, kr = 32 * w + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w) << 16);
-  const float *scale = reinterpret_cast<const float *>(sm + L::kOffRed) + NC;
+  const float *scale = reinterpret_cast<const float *>(sm + L::kOffScale);
   float *stage = reinterpret_cast<float *>(sm + L::kOffK);
 #pragma unroll 1
   for (int blk = 0; blk < L::kChunks; ++blk) {
@@ -929,14 +930,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < NC / 32; ++i) red[NC * (warp & 3) + (NC / 32) * lane + i] = sum[i];
       ok = meet(bars, ph, abort_flag, a.status);
     }
-    // column sums and output scales (the folds are read before the meet below)
-    float t = 0.f;
-    if (ok && kr < NC) t = (red[kr] + red[NC + kr]) + (red[2 * NC + kr] + red[3 * NC + kr]);
-    ok = ok && meet(bars, ph, abort_flag, a.status);
+    // column sums, output scales and output rows (thread kr, column kr; written
+    // apart from the folds they are made from)
     if (ok && kr < NC) {
+      const float t = (red[kr] + red[NC + kr]) + (red[2 * NC + kr] + red[3 * NC + kr]);
       a_sm[kr] = t;
       const bool seen = m_sm[kr] != -CUDART_INF_F;
-      red[NC + kr] = !seen ? 0.f : (a.direct ? (t > 0.f ? 1.f / t : 0.f) : 1.f);
+      reinterpret_cast<float *>(sm + L::kOffScale)[kr] =
+          !seen ? 0.f : (a.direct ? (t > 0.f ? 1.f / t : 0.f) : 1.f);
       reinterpret_cast<size_t *>(sm + L::kOffCOff)[kr] = col_offset(a, pl, kr, DT);
     }
     ok = ok && meet(bars, ph, abort_flag, a.status);
