@@ -207,52 +207,62 @@ struct VLoader {
     n_slots = (pl.len + a.page_size - 1) / a.page_size;  // table slots in use
   }
 
-  // Chunk c (head-dim columns [128 c, 128 c + 128)) of tile j: boxes of
-  // box_rows keys, each in two 64-column slabs; boxes past the row's keys are
-  // not loaded, nor are boxes whose page id lies outside the pool.
-  __device__ bool load(int j, int c) {
-    const int st = seq % ring;
-    if (seq >= ring && !warp_wait(bars + empty + st, ((seq / ring) - 1) & 1, abort_flag, a.status))
-      return false;
+  // The current tile's boxes: pool row of each box of box_rows keys (-1: not
+  // loaded: past the partition's keys, or a page id outside the pool) and the
+  // bytes one chunk of the tile brings.  Found once per tile, at its first chunk.
+  int ys[kKeys / 16];
+  uint32_t t_bytes = 0;
+
+  // Tile j's page ids and box rows (every lane), and its record (one lane).
+  __device__ void plan_tile(int j) {
     const int key0 = (pl.t_begin + j) * kKeys;
     const int vlo = max(0, pl.k_lo - key0), vhi = min(kKeys, pl.k_hi - key0);
     const int32_t *tbl = a.page_tables + (size_t)pl.b * a.table_stride;
     const int br = a.box_rows;
     uint32_t bad = 0, bytes = 0;
-    unsigned char *dst = stages + st * kChunkBytes;
-    uint64_t *bar = bars + full + st;
-    // page ids first (every lane), then one lane arms the barrier and issues
-    int pg[kKeys / 16];
 #pragma unroll
     for (int i = 0; i < kKeys / 16; ++i) {
-      pg[i] = -1;
+      ys[i] = -1;
       if (i * br >= kKeys || i * br >= vhi || (i + 1) * br <= vlo) continue;
-      const int page = pages.get(tbl, (key0 + i * br) / a.page_size, n_slots, lane);
+      const int key = key0 + i * br;
+      const int page = pages.get(tbl, key / a.page_size, n_slots, lane);
       if (page < 0 || (long long)page >= a.num_pages) {
         bad |= (br == 16 ? 1u : 0xFu) << (i * br / 16);
         continue;
       }
-      pg[i] = page;
+      ys[i] = (page * a.num_kv_heads + pl.g) * a.page_size + key % a.page_size;
       bytes += (uint32_t)(br * 128 * 2);
     }
+    t_bytes = bytes;
     if (elect_one()) {
       if (bad) raise_fault(a.status, PSKV_FAULT_BAD_PAGE);
-      if (c == 0) {
-        TileInfo &t = info[j % kInfo];
-        t.vlo = vlo;
-        t.vhi = vhi;
-        t.bad = bad;
-        if (!is_v) mbar_arrive(bars + kInfoFull + j % kInfo);
-      }
-      mbar_arrive_expect_tx(bar, bytes);
+      TileInfo &t = info[j % kInfo];
+      t.vlo = vlo;
+      t.vhi = vhi;
+      t.bad = bad;
+      if (!is_v) mbar_arrive(bars + kInfoFull + j % kInfo);
+    }
+    __syncwarp();
+  }
+
+  // Chunk c (head-dim columns [128 c, 128 c + 128)) of tile j: the tile's boxes,
+  // each in two 64-column slabs.
+  __device__ bool load(int j, int c) {
+    const int st = seq % ring;
+    if (seq >= ring && !warp_wait(bars + empty + st, ((seq / ring) - 1) & 1, abort_flag, a.status))
+      return false;
+    if (c == 0) plan_tile(j);
+    unsigned char *dst = stages + st * kChunkBytes;
+    uint64_t *bar = bars + full + st;
+    const int br = a.box_rows;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(bar, t_bytes);
 #pragma unroll
       for (int i = 0; i < kKeys / 16; ++i) {
-        if (pg[i] < 0) continue;
-        const int key = key0 + i * br;
-        const int y = (pg[i] * a.num_kv_heads + pl.g) * a.page_size + key % a.page_size;
+        if (ys[i] < 0) continue;
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
-          tc::tma_load_2d(dst + sl * kSlab + i * br * 128, map, 128 * c + 64 * sl, y, bar);
+          tc::tma_load_2d(dst + sl * kSlab + i * br * 128, map, 128 * c + 64 * sl, ys[i], bar);
       }
     }
     __syncwarp();
