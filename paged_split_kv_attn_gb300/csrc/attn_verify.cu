@@ -53,6 +53,18 @@ namespace pskv {
 
 namespace {
 
+// mbarrier phase test that never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 using tc::elect_one;
 using tc::ex2;
 using tc::make_map;
@@ -429,18 +441,6 @@ __device__ __forceinline__ void drain_mma(uint64_t *bar, int32_t *status) {
   if (elect_one()) tc::commit(bar);
   __syncwarp();
   if (!mbar_wait(bar, 0) && (threadIdx.x & 31) == 0) raise_fault(status, PSKV_FAULT_WAIT_TIMEOUT);
-}
-
-// mbarrier phase test that never suspends the thread.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 // The softmax warps' meeting point (one arrival per warp); `ph` counts meetings.
