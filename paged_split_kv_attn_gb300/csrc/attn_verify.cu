@@ -34,12 +34,13 @@
 // j + 1 overlaps tile j's softmax), the value products take V chunks once P^T
 // of their tile is written (P^T double-buffered where shared memory allows).
 // Warp 0 issues the score MMAs, warp 7 the value MMAs, warps 1 and 6 the K and
-// V copies; warps 2-5 stage Q and run the softmax and the epilogue (warp w
-// owns tensor-memory lanes 32 (w % 4) .. + 31), which stages O through the
-// drained rings and writes whole rows.  The softmax warps meet on an mbarrier
-// of their own; every wait is bounded, and on expiry the CTA flags
-// PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its tensor
-// memory.
+// V copies (each finds a tile's page ids and pool rows once, at its first
+// chunk); warps 2-5 stage Q and run the softmax and the epilogue (warp w owns
+// tensor-memory lanes 32 (w % 4) .. + 31), which stages O through the drained
+// rings and writes whole rows.  The softmax warps meet on an mbarrier of their
+// own (polled: they arrive together); every wait is bounded, and on expiry the
+// CTA flags PSKV_FAULT_WAIT_TIMEOUT, lets what it issued finish and frees its
+// tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
